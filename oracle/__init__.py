@@ -1,0 +1,138 @@
+"""fp64 CPU oracle for the Mamba selective scan -- TEST INFRASTRUCTURE ONLY.
+
+The arithmetic lives in ``scan_oracle.c`` (plain C, double precision, one
+sequential loop per (batch, channel) chain).  This module only compiles that
+file with gcc and marshals numpy arrays into it.
+
+Who may use it: the tests, the smoke check in ``__graft_entry__`` and the CPU
+baseline leg of ``bench.py``.  The CUDA library never imports, links or calls
+anything here, and nothing here imports the CUDA package.
+
+Every function takes float64 numpy arrays in the layouts documented in
+``scan_oracle.c`` (u/delta/z/y: [batch, dim, seqlen]; B/C: [batch, seqlen,
+dstate]; A_log: [dim, dstate]; D/delta_bias: [dim]; states: [batch, dim,
+dstate]).  bf16 or fp32 inputs are widened to float64 by the caller, so the
+oracle sees exactly the values the GPU sees.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "scan_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle_scan.so")
+_lock = threading.Lock()
+_lib = None
+
+# No fast-math and no FMA contraction: every fp64 operation rounds as written.
+GCC_FLAGS = ["-O2", "-fPIC", "-shared", "-std=c11", "-ffp-contract=off", "-fno-fast-math"]
+
+
+def build(src: str = _SRC, out: str = _LIB, extra_flags=()) -> str:
+    """Compile ``src`` into the shared library ``out`` with gcc; return ``out``."""
+    cmd = ["gcc", *GCC_FLAGS, *extra_flags, "-o", out, src, "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    return out
+
+
+def _declare(lib):
+    dp = ctypes.POINTER(ctypes.c_double)
+    i64 = ctypes.c_int64
+    lib.oracle_selective_scan_f64.restype = ctypes.c_int
+    lib.oracle_selective_scan_f64.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int,
+                                              dp, dp, dp, i64, i64, i64, i64, ctypes.c_int]
+    lib.oracle_selective_state_update_f64.restype = ctypes.c_int
+    lib.oracle_selective_state_update_f64.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp,
+                                                      ctypes.c_int, dp, i64, i64, i64]
+    lib.oracle_hw_threads.restype = ctypes.c_int
+    lib.oracle_hw_threads.argtypes = []
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the oracle library.
+
+    ``path`` selects another build of the same source (the mutation tests use
+    this to load deliberately broken copies); the default is the oracle itself.
+    """
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            if (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+                build()
+            _lib = _declare(ctypes.CDLL(_LIB))
+    return _lib
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _f64(a):
+    if a is None:
+        return None
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def hw_threads(lib=None) -> int:
+    return (lib or load()).oracle_hw_threads()
+
+
+def selective_scan(u, delta, A_log, B, C, D=None, z=None, delta_bias=None, softplus=True,
+                   h0=None, nthreads: int = 0, lib=None):
+    """Run the fp64 recurrence; return ``(y, last_state, threads_used)``.
+
+    Shapes: u/delta/z [batch, dim, L]; B/C [batch, L, N]; A_log [dim, N];
+    D/delta_bias [dim]; h0 (optional) [batch, dim, N].
+    """
+    lib = lib or load()
+    u, delta, A_log, B, C = map(_f64, (u, delta, A_log, B, C))
+    D, z, delta_bias, h0 = map(_f64, (D, z, delta_bias, h0))
+    batch, dim, L = u.shape
+    N = A_log.shape[1]
+    assert delta.shape == u.shape and A_log.shape == (dim, N)
+    assert B.shape == (batch, L, N) and C.shape == (batch, L, N)
+    assert z is None or z.shape == u.shape
+    assert D is None or D.shape == (dim,)
+    assert delta_bias is None or delta_bias.shape == (dim,)
+    assert h0 is None or h0.shape == (batch, dim, N)
+    y = np.empty((batch, dim, L), dtype=np.float64)
+    hL = np.empty((batch, dim, N), dtype=np.float64)
+    used = lib.oracle_selective_scan_f64(
+        _ptr(u), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+        int(bool(softplus)), _ptr(h0), _ptr(y), _ptr(hL), batch, dim, L, N, int(nthreads))
+    if used < 0:
+        raise ValueError(f"oracle_selective_scan_f64 rejected its arguments ({used})")
+    return y, hL, used
+
+
+def selective_state_update(state, x, dt, A_log, B, C, D=None, z=None, dt_bias=None,
+                           softplus=True, lib=None):
+    """One decode step.  Returns ``(out, new_state)``; the input is not modified.
+
+    Shapes: state [batch, dim, N]; x/dt/z [batch, dim]; B/C [batch, N];
+    A_log [dim, N]; D/dt_bias [dim].
+    """
+    lib = lib or load()
+    st = np.array(state, dtype=np.float64, copy=True, order="C")
+    x, dt, A_log, B, C = map(_f64, (x, dt, A_log, B, C))
+    D, z, dt_bias = map(_f64, (D, z, dt_bias))
+    batch, dim, N = st.shape
+    assert x.shape == (batch, dim) and dt.shape == (batch, dim)
+    assert B.shape == (batch, N) and C.shape == (batch, N) and A_log.shape == (dim, N)
+    out = np.empty((batch, dim), dtype=np.float64)
+    rc = lib.oracle_selective_state_update_f64(
+        _ptr(st), _ptr(x), _ptr(dt), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+        _ptr(dt_bias), int(bool(softplus)), _ptr(out), batch, dim, N)
+    if rc != 0:
+        raise ValueError(f"oracle_selective_state_update_f64 rejected its arguments ({rc})")
+    return out, st

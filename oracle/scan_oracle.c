@@ -1,0 +1,187 @@
+/*
+ * Reference oracle for the Mamba selective scan -- TEST INFRASTRUCTURE ONLY.
+ *
+ * This file is a plain, slow, sequential fp64 CPU restatement of the selective
+ * state-space recurrence.  It exists so that the CUDA library can be checked
+ * against something obviously correct.  Only the test-suite, the smoke check
+ * and the benchmark's CPU-baseline leg may load it; the product path never
+ * does, and it shares no code, header or constant with the CUDA sources.
+ *
+ * What it computes (sources are the pages' section names):
+ *   - "Selective SSM" Keras layer (highthink.cn page, "Mamba 的核心创新" and the
+ *     SelectiveSSM listing): A = -exp(A_log) diagonal, Abar = exp(A*dt),
+ *     Bbar = B*dt, state = Abar*state + Bbar*u, y = sum_n C*state + D*u,
+ *     initial state zero.
+ *   - Zero-order-hold formulas and the small-step simplification Bbar ~ dt*B
+ *     (luzhipeng.com tutorial, "数学基础" and step 1 "discrete_bilinear").
+ *   - Input-dependent step dt = softplus(Linear(x)) with a bias on the dt
+ *     projection (codechina.net overview, section 2.1; highthink.cn dt_proj
+ *     with use_bias=True).
+ *   - SiLU output gate on the z branch (highthink.cn "Mamba 整体架构" block
+ *     diagram: the SiLU branch multiplies the SSM output).
+ *
+ * Readings taken where the pages are silent or disagree:
+ *   - Bbar is the Euler form dt*B (not the exact ZOH inverse form).
+ *   - dt is per (batch, channel, time).
+ *   - y_t reads the state after the update at step t.
+ *   - out = (sum_n C h + D u) * SiLU(z); z, D and the bias are optional.
+ *   - softplus_flag == 0 uses dt = delta + bias as given.
+ *
+ * Layouts (row-major, contiguous):
+ *   u, delta, z, y : [batch][dim][seqlen]
+ *   B, C           : [batch][seqlen][dstate]   (shared by all channels)
+ *   A_log          : [dim][dstate]
+ *   D, delta_bias  : [dim]
+ *   h0, last_state : [batch][dim][dstate]
+ * Every array is double precision.  The caller widens bf16 or fp32 values.
+ *
+ * Parallelism: the (batch, channel) chains are independent; they are split
+ * over POSIX threads.  That changes no arithmetic: every chain is evaluated in
+ * exactly the order written below.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <unistd.h>
+
+/* softplus(x) = log(1 + e^x), written so that neither branch overflows. */
+static double oracle_softplus(double x) {
+    if (x > 0.0) return x + log1p(exp(-x));
+    return log1p(exp(x));
+}
+
+/* SiLU(z) = z * sigmoid(z) = z / (1 + e^-z). */
+static double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
+
+typedef struct {
+    const double *u, *delta, *A_log, *B, *C, *D, *z, *delta_bias, *h0;
+    double *y, *last_state;
+    int64_t batch, dim, seqlen, dstate;
+    int softplus_flag;
+    int64_t chain_begin, chain_end; /* chains are b*dim + d */
+} scan_job;
+
+/* One (b, d) chain: the recurrence of the Keras listing, step by step. */
+static void scan_one_chain(const scan_job *j, int64_t chain, double *h, double *A) {
+    const int64_t b = chain / j->dim, d = chain % j->dim;
+    const int64_t L = j->seqlen, N = j->dstate;
+    const double *u = j->u + chain * L;
+    const double *dl = j->delta + chain * L;
+    const double *zz = j->z ? j->z + chain * L : NULL;
+    const double *Bb = j->B + b * L * N;
+    const double *Cb = j->C + b * L * N;
+    double *y = j->y + chain * L;
+    const double Dd = j->D ? j->D[d] : 0.0;
+    const double bias = j->delta_bias ? j->delta_bias[d] : 0.0;
+
+    for (int64_t n = 0; n < N; ++n) {
+        A[n] = -exp(j->A_log[d * N + n]);          /* A = -exp(A_log) */
+        h[n] = j->h0 ? j->h0[chain * N + n] : 0.0;  /* zero initial state */
+    }
+    for (int64_t t = 0; t < L; ++t) {
+        const double raw = dl[t] + bias;
+        const double dt = j->softplus_flag ? oracle_softplus(raw) : raw;
+        const double ut = u[t];
+        double acc = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            const double abar = exp(dt * A[n]);        /* Abar = exp(A*dt)   */
+            const double bbar_u = dt * Bb[t * N + n] * ut; /* Bbar*u = dt*B*u */
+            h[n] = abar * h[n] + bbar_u;                /* state update       */
+            acc += Cb[t * N + n] * h[n];                /* C . state          */
+        }
+        const double yt = acc + Dd * ut;                /* + D*u skip         */
+        y[t] = zz ? yt * oracle_silu(zz[t]) : yt;       /* SiLU(z) gate       */
+    }
+    if (j->last_state)
+        for (int64_t n = 0; n < N; ++n) j->last_state[chain * N + n] = h[n];
+}
+
+static void *scan_worker(void *arg) {
+    const scan_job *j = (const scan_job *)arg;
+    double *h = (double *)malloc(sizeof(double) * (size_t)j->dstate);
+    double *A = (double *)malloc(sizeof(double) * (size_t)j->dstate);
+    if (h && A)
+        for (int64_t c = j->chain_begin; c < j->chain_end; ++c) scan_one_chain(j, c, h, A);
+    free(h);
+    free(A);
+    return NULL;
+}
+
+/* Number of hardware threads this process may use. */
+int oracle_hw_threads(void) {
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+/*
+ * Full selective scan.  h0 may be NULL (zero initial state, as on the pages);
+ * it exists so that splitting a sequence in two can be checked.  nthreads <= 0
+ * means all hardware threads.  Returns the number of threads used, or a
+ * negative value on a bad argument.
+ */
+int oracle_selective_scan_f64(const double *u, const double *delta, const double *A_log,
+                              const double *B, const double *C, const double *D,
+                              const double *z, const double *delta_bias, int softplus_flag,
+                              const double *h0, double *y, double *last_state,
+                              int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                              int nthreads) {
+    if (!u || !delta || !A_log || !B || !C || !y) return -1;
+    if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 0) return -2;
+    const int64_t chains = batch * dim;
+    if (nthreads <= 0) nthreads = oracle_hw_threads();
+    if (nthreads > chains) nthreads = chains > 0 ? (int)chains : 1;
+
+    scan_job base = {u, delta, A_log, B, C, D, z, delta_bias, h0, y, last_state,
+                     batch, dim, seqlen, dstate, softplus_flag, 0, 0};
+    scan_job *jobs = (scan_job *)malloc(sizeof(scan_job) * (size_t)nthreads);
+    pthread_t *tids = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    if (!jobs || !tids) { free(jobs); free(tids); return -3; }
+    for (int i = 0; i < nthreads; ++i) {
+        jobs[i] = base;
+        jobs[i].chain_begin = chains * i / nthreads;
+        jobs[i].chain_end = chains * (i + 1) / nthreads;
+    }
+    if (nthreads == 1) {
+        scan_worker(&jobs[0]);
+    } else {
+        for (int i = 0; i < nthreads; ++i) pthread_create(&tids[i], NULL, scan_worker, &jobs[i]);
+        for (int i = 0; i < nthreads; ++i) pthread_join(tids[i], NULL);
+    }
+    free(jobs);
+    free(tids);
+    return nthreads;
+}
+
+/*
+ * One decode step ("inference stays RNN-like": each new token touches only the
+ * previous state).  state [batch][dim][dstate] is updated in place; x, dt, z
+ * and out are [batch][dim]; B, C are [batch][dstate].
+ */
+int oracle_selective_state_update_f64(double *state, const double *x, const double *dt,
+                                      const double *A_log, const double *B, const double *C,
+                                      const double *D, const double *z, const double *dt_bias,
+                                      int softplus_flag, double *out,
+                                      int64_t batch, int64_t dim, int64_t dstate) {
+    if (!state || !x || !dt || !A_log || !B || !C || !out) return -1;
+    if (batch < 0 || dim < 0 || dstate < 0) return -2;
+    const int64_t N = dstate;
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t d = 0; d < dim; ++d) {
+            const int64_t e = b * dim + d;
+            const double raw = dt[e] + (dt_bias ? dt_bias[d] : 0.0);
+            const double step = softplus_flag ? oracle_softplus(raw) : raw;
+            double acc = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                const double A = -exp(A_log[d * N + n]);
+                const double abar = exp(step * A);
+                double *h = &state[e * N + n];
+                *h = abar * *h + step * B[b * N + n] * x[e];
+                acc += C[b * N + n] * *h;
+            }
+            const double yt = acc + (D ? D[d] : 0.0) * x[e];
+            out[e] = z ? yt * oracle_silu(z[e]) : yt;
+        }
+    }
+    return 0;
+}

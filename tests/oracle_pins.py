@@ -1,0 +1,316 @@
+"""Pins for the fp64 oracle: results fixed by the mathematics, not by the oracle.
+
+Each ``check_*`` function takes a loaded oracle library (the real one, or a
+deliberately broken copy in the mutation test) and raises ``AssertionError``
+when the oracle disagrees with a closed form, an invariant or an independent
+brute-force evaluation.  None of them re-types the oracle's loop: the expected
+values come from geometric-series sums, a causal convolution via
+``numpy.convolve``, explicit products over time, library softplus/sigmoid
+(``numpy.logaddexp``, ``scipy.special.expit``), or from the oracle itself
+under a transformation that must leave the answer unchanged (splitting the
+sequence, permuting channels or batches, linearity in u, a chain of decode
+steps).
+
+Steps pinned (see the page sections cited in ``oracle/scan_oracle.c``):
+  A = -exp(A_log), Abar = exp(dt*A), Bbar = dt*B, h_t = Abar h_{t-1} + Bbar u,
+  y = sum_n C h + D u, SiLU(z) gate, dt = softplus(delta + bias), zero h0.
+"""
+from __future__ import annotations
+
+import numpy as np
+from scipy.special import expit
+
+import oracle
+
+RTOL = 1e-12
+
+
+def _close(got, want, rtol=RTOL, atol=0.0, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    assert got.shape == want.shape, f"{what}: shape {got.shape} != {want.shape}"
+    scale = max(float(np.max(np.abs(want))) if want.size else 0.0, 1e-300)
+    err = float(np.max(np.abs(got - want))) if want.size else 0.0
+    assert err <= rtol * scale + atol, f"{what}: max abs err {err:.3e} (scale {scale:.3e})"
+
+
+def _softplus_inv(dt):
+    """raw such that log(1 + e^raw) == dt (inverse softplus, by expm1)."""
+    return np.log(np.expm1(dt))
+
+
+def _silu(z):
+    return z * expit(z)
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# --------------------------------------------------------------------------
+def check_delta_zero_limit(lib):
+    """dt = 0 (softplus off, zero delta, no bias): Abar = 1 and Bbar = 0, so the
+    state never leaves zero and out = D*u*SiLU(z) exactly."""
+    r = _rng(1)
+    b, d, L, N = 2, 3, 9, 4
+    u, z = r.normal(size=(b, d, L)), r.normal(size=(b, d, L))
+    B, C = r.normal(size=(b, L, N)), r.normal(size=(b, L, N))
+    D = r.normal(size=d)
+    A_log = np.log(r.uniform(0.5, 8, size=(d, N)))
+    y, hL, _ = oracle.selective_scan(u, np.zeros_like(u), A_log, B, C, D=D, z=z,
+                                     softplus=False, lib=lib)
+    assert np.all(hL == 0.0), "state must stay exactly zero when dt = 0"
+    _close(y, D[None, :, None] * u * _silu(z), rtol=1e-14, what="dt=0 output")
+
+
+def check_single_step(lib):
+    """L = 1 from a zero state: h = dt*B*u, out = (sum_n C h + D u) SiLU(z).
+    dt is fixed through the inverse softplus, with a nonzero bias, and spans
+    both softplus branches (dt below and above log 2)."""
+    r = _rng(2)
+    b, d, N = 3, 4, 5
+    dt = np.array([1e-4, 0.05, 0.9, 3.0])                 # per channel
+    bias = r.normal(size=d)
+    raw = np.broadcast_to((_softplus_inv(dt) - bias)[None, :, None], (b, d, 1)).copy()
+    u, z = r.normal(size=(b, d, 1)), r.normal(size=(b, d, 1))
+    B, C = r.normal(size=(b, 1, N)), r.normal(size=(b, 1, N))
+    D = r.normal(size=d)
+    A_log = r.normal(size=(d, N))
+    y, hL, _ = oracle.selective_scan(u, raw, A_log, B, C, D=D, z=z, delta_bias=bias,
+                                     softplus=True, lib=lib)
+    h = dt[None, :, None] * B[:, 0, None, :] * u[:, :, 0, None]      # [b, d, N]
+    _close(hL, h, rtol=1e-12, what="single-step state")
+    out = (np.einsum("bn,bdn->bd", C[:, 0, :], h) + D[None, :] * u[:, :, 0]) * _silu(z[:, :, 0])
+    _close(y[:, :, 0], out, rtol=1e-12, what="single-step output")
+
+
+def check_geometric_series(lib):
+    """Constant dt, B, C, u: h_t = Bbar u (1 - a^(t+1)) / (1 - a) with
+    a = exp(-dt k) for A_log = log k, and out_t = sum_n C_n h_t + D u.  B and C
+    differ per state and per batch; dt differs per channel (through the bias)
+    and softplus is off here, so dt is used as given."""
+    b, d, L, N = 2, 3, 300, 4
+    k = np.array([[1.0, 2.0, 3.0, 4.0], [0.5, 1.5, 7.0, 16.0], [1.0, 1.0, 2.0, 64.0]])
+    dt = np.array([0.05, 0.002, 0.3])
+    Bn = np.array([[0.7, -1.1, 0.3, 2.0], [-0.4, 0.9, 1.3, -0.2]])      # per batch, state
+    Cn = np.array([[1.2, 0.5, -0.8, 0.1], [0.3, -1.5, 0.6, 1.1]])
+    uc = np.array([[0.9, -0.6, 1.7], [-1.3, 0.4, 0.8]])                 # per batch, channel
+    D = np.array([0.25, -1.0, 2.0])
+    u = np.repeat(uc[:, :, None], L, axis=2)
+    B = np.repeat(Bn[:, None, :], L, axis=1)
+    C = np.repeat(Cn[:, None, :], L, axis=1)
+    bias = dt.copy()
+    y, hL, _ = oracle.selective_scan(u, np.zeros((b, d, L)), np.log(k), B, C, D=D,
+                                     delta_bias=bias, softplus=False, lib=lib)
+    a = np.exp(-dt[:, None] * k)                                          # [d, N]
+    t = np.arange(L)
+    bu = dt[None, :, None] * Bn[:, None, :] * uc[:, :, None]              # [b, d, N]
+    h = bu[:, :, None, :] * (1 - a[None, :, None, :] ** (t[None, None, :, None] + 1)) \
+        / (1 - a[None, :, None, :])                                       # [b, d, L, N]
+    _close(hL, h[:, :, -1, :], rtol=1e-11, what="geometric final state")
+    out = np.einsum("bn,bdtn->bdt", Cn, h) + D[None, :, None] * u
+    _close(y, out, rtol=1e-11, what="geometric outputs")
+
+
+def check_steady_state(lib):
+    """A long constant input drives the state to its fixed point Bbar u / (1 - a)."""
+    d, N, L = 2, 3, 20000
+    k = np.array([[1.0, 2.0, 3.0], [4.0, 5.0, 6.0]])
+    dt = np.array([0.01, 0.02])
+    Bn, uc = np.array([0.5, -1.0, 2.0]), np.array([1.5, -0.5])
+    u = np.repeat(uc[None, :, None], L, axis=2)
+    B = np.repeat(Bn[None, None, :], L, axis=1)
+    _, hL, _ = oracle.selective_scan(u, np.repeat(dt[None, :, None], L, axis=2), np.log(k), B,
+                                     np.ones((1, L, N)), softplus=False, lib=lib)
+    h_inf = dt[:, None] * Bn[None, :] * uc[:, None] / (1 - np.exp(-dt[:, None] * k))
+    _close(hL[0], h_inf, rtol=1e-10, what="steady state")
+
+
+def check_lti_convolution(lib):
+    """Time-invariant case (constant dt, B, C; random u): the recurrence equals
+    the causal convolution y_t = sum_{j<=t} K_j u_{t-j} + D u_t with the kernel
+    K_j = sum_n C_n a_n^j dt B_n (the recurrence/convolution equivalence of the
+    mhpn.cn article, section 3).  Evaluated with numpy.convolve."""
+    r = _rng(3)
+    b, d, L, N = 2, 3, 128, 6
+    k = r.uniform(0.5, 10.0, size=(d, N))
+    dt = np.array([0.03, 0.3, 0.001])
+    Bn, Cn = r.normal(size=(b, N)), r.normal(size=(b, N))
+    u = r.normal(size=(b, d, L))
+    D = r.normal(size=d)
+    B = np.repeat(Bn[:, None, :], L, axis=1)
+    C = np.repeat(Cn[:, None, :], L, axis=1)
+    raw = np.broadcast_to(_softplus_inv(dt)[None, :, None], (b, d, L)).copy()
+    y, _, _ = oracle.selective_scan(u, raw, np.log(k), B, C, D=D, softplus=True, lib=lib)
+    j = np.arange(L)
+    for bi in range(b):
+        for di in range(d):
+            a = np.exp(-dt[di] * k[di])                                      # [N]
+            K = (Cn[bi] * dt[di] * Bn[bi] * a[None, :] ** j[:, None]).sum(axis=1)
+            want = np.convolve(u[bi, di], K)[:L] + D[di] * u[bi, di]
+            _close(y[bi, di], want, rtol=1e-11, what=f"convolution b={bi} d={di}")
+
+
+def check_bruteforce_unrolled(lib):
+    """Everything time-varying, tiny sizes: the state written as an explicit
+    sum h_t = sum_{s<=t} (prod_{s<r<=t} Abar_r) Bbar_s u_s, with softplus via
+    numpy.logaddexp and the gate via scipy's expit."""
+    r = _rng(4)
+    b, d, L, N = 2, 3, 7, 3
+    u, z, raw = r.normal(size=(b, d, L)), r.normal(size=(b, d, L)), r.normal(size=(b, d, L))
+    B, C = r.normal(size=(b, L, N)), r.normal(size=(b, L, N))
+    A_log, D, bias = r.normal(size=(d, N)), r.normal(size=d), r.normal(size=d)
+    y, hL, _ = oracle.selective_scan(u, raw, A_log, B, C, D=D, z=z, delta_bias=bias,
+                                     softplus=True, lib=lib)
+    want_y = np.zeros((b, d, L))
+    want_h = np.zeros((b, d, N))
+    for bi in range(b):
+        for di in range(d):
+            dt = np.logaddexp(0.0, raw[bi, di] + bias[di])                 # [L]
+            A = -np.exp(A_log[di])                                         # [N]
+            for t in range(L):
+                h = np.zeros(N)
+                for s in range(t + 1):
+                    decay = np.ones(N)
+                    for rr in range(s + 1, t + 1):
+                        decay = decay * np.exp(dt[rr] * A)
+                    h = h + decay * dt[s] * B[bi, s] * u[bi, di, s]
+                yt = float(np.dot(C[bi, t], h)) + D[di] * u[bi, di, t]
+                want_y[bi, di, t] = yt * z[bi, di, t] * expit(z[bi, di, t])
+                if t == L - 1:
+                    want_h[bi, di] = h
+    _close(hL, want_h, rtol=1e-12, what="unrolled final state")
+    _close(y, want_y, rtol=1e-12, what="unrolled outputs")
+
+
+def check_linearity_in_u(lib):
+    """For fixed dt, B, C, z the map u -> (y, h_L) is linear."""
+    r = _rng(5)
+    b, d, L, N = 2, 4, 40, 4
+    raw, z = r.normal(size=(b, d, L)), r.normal(size=(b, d, L))
+    B, C = r.normal(size=(b, L, N)), r.normal(size=(b, L, N))
+    A_log, D, bias = r.normal(size=(d, N)), r.normal(size=d), r.normal(size=d)
+    u1, u2 = r.normal(size=(b, d, L)), r.normal(size=(b, d, L))
+    al, be = 0.75, -1.25
+    run = lambda uu: oracle.selective_scan(uu, raw, A_log, B, C, D=D, z=z, delta_bias=bias,
+                                           lib=lib)
+    y1, h1, _ = run(u1)
+    y2, h2, _ = run(u2)
+    y3, h3, _ = run(al * u1 + be * u2)
+    _close(y3, al * y1 + be * y2, rtol=1e-12, what="linearity y")
+    _close(h3, al * h1 + be * h2, rtol=1e-12, what="linearity state")
+
+
+def check_split_invariance(lib):
+    """Scanning [0, L) equals scanning [0, L1) and then [L1, L) from the state
+    reached at L1 (the chunk-carry property the GPU relies on)."""
+    r = _rng(6)
+    b, d, L, N, L1 = 2, 3, 50, 4, 19
+    u, z, raw = r.normal(size=(b, d, L)), r.normal(size=(b, d, L)), r.normal(size=(b, d, L))
+    B, C = r.normal(size=(b, L, N)), r.normal(size=(b, L, N))
+    A_log, D, bias = r.normal(size=(d, N)), r.normal(size=d), r.normal(size=d)
+    kw = dict(D=D, delta_bias=bias, softplus=True, lib=lib)
+    y, hL, _ = oracle.selective_scan(u, raw, A_log, B, C, z=z, **kw)
+    ya, ha, _ = oracle.selective_scan(u[..., :L1], raw[..., :L1], A_log, B[:, :L1], C[:, :L1],
+                                      z=z[..., :L1], **kw)
+    yb, hb, _ = oracle.selective_scan(u[..., L1:], raw[..., L1:], A_log, B[:, L1:], C[:, L1:],
+                                      z=z[..., L1:], h0=ha, **kw)
+    _close(y, np.concatenate([ya, yb], axis=-1), rtol=1e-12, what="split outputs")
+    _close(hL, hb, rtol=1e-12, what="split final state")
+
+
+def check_decode_chain(lib):
+    """L single-token decode steps from a zero state reproduce the scan."""
+    r = _rng(7)
+    b, d, L, N = 2, 3, 12, 4
+    u, z, raw = r.normal(size=(b, d, L)), r.normal(size=(b, d, L)), r.normal(size=(b, d, L))
+    B, C = r.normal(size=(b, L, N)), r.normal(size=(b, L, N))
+    A_log, D, bias = r.normal(size=(d, N)), r.normal(size=d), r.normal(size=d)
+    y, hL, _ = oracle.selective_scan(u, raw, A_log, B, C, D=D, z=z, delta_bias=bias, lib=lib)
+    st = np.zeros((b, d, N))
+    ys = []
+    for t in range(L):
+        out, st = oracle.selective_state_update(st, u[..., t], raw[..., t], A_log, B[:, t], C[:, t],
+                                                D=D, z=z[..., t], dt_bias=bias, lib=lib)
+        ys.append(out)
+    _close(np.stack(ys, axis=-1), y, rtol=1e-12, what="decode chain outputs")
+    _close(st, hL, rtol=1e-12, what="decode chain state")
+
+
+def check_decode_single_step(lib):
+    """One decode step from a known state: h' = exp(-dt k) h + dt B x and
+    out = (sum_n C h' + D x) SiLU(z), dt fixed through the inverse softplus."""
+    b, d, N = 2, 2, 3
+    k = np.array([[1.0, 2.0, 3.0], [0.5, 4.0, 9.0]])
+    dt = np.array([0.02, 1.5])
+    bias = np.array([0.3, -0.7])
+    x = np.array([[1.0, -2.0], [0.5, 3.0]])
+    z = np.array([[0.4, -1.2], [2.0, 0.0]])
+    B = np.array([[0.5, -1.0, 2.0], [1.5, 0.2, -0.3]])
+    C = np.array([[1.0, 0.25, -0.5], [-2.0, 0.5, 1.0]])
+    D = np.array([0.1, -0.4])
+    h = np.arange(b * d * N, dtype=np.float64).reshape(b, d, N) * 0.1 - 0.5
+    raw = np.broadcast_to(_softplus_inv(dt)[None, :] - bias[None, :], (b, d)).copy()
+    out, h1 = oracle.selective_state_update(h, x, raw,
+                                            np.log(k), B, C, D=D, z=z, dt_bias=bias, lib=lib)
+    want_h = np.exp(-dt[None, :, None] * k[None]) * h + dt[None, :, None] * B[:, None, :] * x[..., None]
+    _close(h1, want_h, rtol=1e-12, what="decode state")
+    want = (np.einsum("bn,bdn->bd", C, want_h) + D[None, :] * x) * _silu(z)
+    _close(out, want, rtol=1e-12, what="decode output")
+
+
+def check_permutations(lib):
+    """Permuting channels (u, delta, z, A_log, D, bias together) permutes the
+    outputs; swapping batches (u, delta, z, B, C together) swaps them."""
+    r = _rng(8)
+    b, d, L, N = 3, 5, 16, 4
+    u, z, raw = r.normal(size=(b, d, L)), r.normal(size=(b, d, L)), r.normal(size=(b, d, L))
+    B, C = r.normal(size=(b, L, N)), r.normal(size=(b, L, N))
+    A_log, D, bias = r.normal(size=(d, N)), r.normal(size=d), r.normal(size=d)
+    y, hL, _ = oracle.selective_scan(u, raw, A_log, B, C, D=D, z=z, delta_bias=bias, lib=lib)
+    p = np.array([3, 0, 4, 1, 2])
+    yp, hp, _ = oracle.selective_scan(u[:, p], raw[:, p], A_log[p], B, C, D=D[p], z=z[:, p],
+                                      delta_bias=bias[p], lib=lib)
+    _close(yp, y[:, p], rtol=1e-14, what="channel permutation y")
+    _close(hp, hL[:, p], rtol=1e-14, what="channel permutation state")
+    q = np.array([2, 0, 1])
+    yq, hq, _ = oracle.selective_scan(u[q], raw[q], A_log, B[q], C[q], D=D, z=z[q],
+                                      delta_bias=bias, lib=lib)
+    _close(yq, y[q], rtol=1e-14, what="batch permutation y")
+    _close(hq, hL[q], rtol=1e-14, what="batch permutation state")
+
+
+def check_optional_inputs(lib):
+    """No z: no gate.  No D: no skip.  No bias: delta used alone.  Each optional
+    input, when absent, must act like its neutral value supplied explicitly
+    (a gate that passes y through is z -> infinity; emulate with the explicit
+    ungated closed form instead)."""
+    r = _rng(9)
+    b, d, L, N = 1, 3, 10, 4
+    u, raw = r.normal(size=(b, d, L)), r.normal(size=(b, d, L))
+    B, C = r.normal(size=(b, L, N)), r.normal(size=(b, L, N))
+    A_log = r.normal(size=(d, N))
+    y0, h0, _ = oracle.selective_scan(u, raw, A_log, B, C, lib=lib)
+    y1, h1, _ = oracle.selective_scan(u, raw, A_log, B, C, D=np.zeros(d), delta_bias=np.zeros(d),
+                                      lib=lib)
+    _close(y0, y1, rtol=0, what="absent D/bias == zero D/bias")
+    _close(h0, h1, rtol=0, what="absent D/bias state")
+    z = r.normal(size=(b, d, L))
+    y2, _, _ = oracle.selective_scan(u, raw, A_log, B, C, z=z, lib=lib)
+    _close(y2, y0 * _silu(z), rtol=1e-13, what="gate multiplies the ungated output")
+
+
+ALL_CHECKS = [
+    check_delta_zero_limit,
+    check_single_step,
+    check_geometric_series,
+    check_steady_state,
+    check_lti_convolution,
+    check_bruteforce_unrolled,
+    check_linearity_in_u,
+    check_split_invariance,
+    check_decode_chain,
+    check_decode_single_step,
+    check_permutations,
+    check_optional_inputs,
+]

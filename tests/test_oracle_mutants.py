@@ -1,0 +1,56 @@
+"""Each plausible mistake planted in a copy of the oracle (on the CPU) must be
+caught by at least one pin.  This shows the pins constrain every step."""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_CHECKS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "scan_oracle.c")
+
+# (name, text in scan_oracle.c, replacement)
+MUTANTS = [
+    ("output_reads_state_before_update",
+     "h[n] = abar * h[n] + bbar_u;                /* state update       */\n"
+     "            acc += Cb[t * N + n] * h[n];                /* C . state          */",
+     "acc += Cb[t * N + n] * h[n];\n            h[n] = abar * h[n] + bbar_u;"),
+    ("dropped_D_skip", "const double yt = acc + Dd * ut;", "const double yt = acc;"),
+    ("sigmoid_gate_instead_of_silu", "return z / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(-z));"),
+    ("A_is_minus_A_log", "A[n] = -exp(j->A_log[d * N + n]);", "A[n] = -j->A_log[d * N + n];"),
+    ("A_positive", "A[n] = -exp(j->A_log[d * N + n]);", "A[n] = exp(j->A_log[d * N + n]);"),
+    ("Bbar_without_dt", "const double bbar_u = dt * Bb[t * N + n] * ut;",
+     "const double bbar_u = Bb[t * N + n] * ut;"),
+    ("Bbar_exact_zoh", "const double bbar_u = dt * Bb[t * N + n] * ut;",
+     "const double bbar_u = (abar - 1.0) / A[n] * Bb[t * N + n] * ut;"),
+    ("softplus_ignored", "j->softplus_flag ? oracle_softplus(raw) : raw", "raw"),
+    ("softplus_positive_branch_wrong", "if (x > 0.0) return x + log1p(exp(-x));",
+     "if (x > 0.0) return log1p(exp(-x));"),
+    ("bias_ignored", "const double raw = dl[t] + bias;", "const double raw = dl[t];"),
+    ("B_transposed", "const double bbar_u = dt * Bb[t * N + n] * ut;",
+     "const double bbar_u = dt * Bb[n * L + t] * ut;"),
+    ("C_is_B", "acc += Cb[t * N + n] * h[n];", "acc += Bb[t * N + n] * h[n];"),
+    ("B_ignores_batch", "const double *Bb = j->B + b * L * N;", "const double *Bb = j->B;"),
+    ("A_log_transposed", "A[n] = -exp(j->A_log[d * N + n]);", "A[n] = -exp(j->A_log[n * j->dim + d]);"),
+    ("gate_reads_first_z", "y[t] = zz ? yt * oracle_silu(zz[t]) : yt;",
+     "y[t] = zz ? yt * oracle_silu(zz[0]) : yt;"),
+    ("initial_state_ignored", "h[n] = j->h0 ? j->h0[chain * N + n] : 0.0;", "h[n] = 0.0;"),
+    ("decode_without_dt", "*h = abar * *h + step * B[b * N + n] * x[e];", "*h = abar * *h + B[b * N + n] * x[e];"),
+    ("decode_no_gate", "out[e] = z ? yt * oracle_silu(z[e]) : yt;", "out[e] = yt;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(tmp_path, name, old, new):
+    text = open(SRC).read()
+    assert text.count(old) == 1, f"mutation site for {name} not found exactly once"
+    src = tmp_path / "mutant.c"
+    src.write_text(text.replace(old, new))
+    lib = oracle.load(oracle.build(str(src), str(tmp_path / "libmutant.so")))
+    failed = []
+    for check in ALL_CHECKS:
+        try:
+            check(lib)
+        except AssertionError:
+            failed.append(check.__name__)
+    assert failed, f"no pin catches the planted mistake {name}"
