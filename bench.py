@@ -1,0 +1,623 @@
+#!/usr/bin/env python
+"""Benchmark of the fused selective scan (one step = one forward scan of the
+Mamba-1.4B-style layer: batch 4, d_inner 4096, L 4096, N 16, bf16 io).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs the
+same workload on its own GPU (independent problems, no collective on the data
+path: weak scaling); the step time is the max over ranks.
+
+Measured in the same run: the SFU ex2 rate (micro-benchmark) that sets the
+exp roofline, SM clocks and throttle reasons during the timed region (NVML),
+an end-to-end number through the C ABI with pinned host buffers, the decode
+step on its own workload, and the fp64 oracle on the host cores over a
+bounded sample of the workload (the CPU baseline).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "selective-scan state-updates/s (B·D·L·N) and GB/s as % of HBM/SFU roofline"
+UNIT = "state-updates/s"
+DEFAULT_WORKLOAD = "mamba1p4b_bf16"
+L2_BYTES = 126 * 1024 * 1024
+
+
+# ----------------------------------------------------------------------------
+# algorithmic counts (per launch)
+def scan_counts(cfg) -> dict:
+    s = 2 if cfg.io_dtype == "bf16" else 4
+    B, D, L, N = cfg.batch, cfg.dim, cfg.seqlen, cfg.dstate
+    elems = B * D * L
+    return {
+        "updates": elems * N,
+        "elems": elems,
+        # u, delta, z read + y written; B and C read once; last_state written;
+        # A_log, D and bias read.
+        "bytes": elems * 4 * s + 2 * B * L * N * s + 4 * B * D * N + 4 * D * N + 8 * D,
+        # one exp per update, plus the softplus and SiLU exponentials per element
+        "exps": elems * (N + 2),
+        "input_bytes": elems * 3 * s + 2 * B * L * N * s,
+        "output_bytes": elems * s + 4 * B * D * N,
+    }
+
+
+def decode_counts(cfg) -> dict:
+    s = 2 if cfg.io_dtype == "bf16" else 4
+    B, D, N = cfg.batch, cfg.dim, cfg.dstate
+    return {
+        "updates": B * D * N,
+        "bytes": 8 * B * D * N + 4 * B * D * s + 2 * B * N * s + 4 * D * N + 8 * D,
+    }
+
+
+def kernel_source_hash() -> str:
+    """Hash of the scan kernel sources, to match stored ncu traffic figures."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "selective_state_space_140_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as fh:
+                h.update(name.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload: str, kernel_hash: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"scan_fwd_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as fh:
+        for line in fh:
+            if line.startswith("- ") and ":" in line:
+                k, v = line[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_source_sha256_16") != kernel_hash:
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        d["_source"] = "measured"
+        return d
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "_source": "fallback"}
+
+
+# ----------------------------------------------------------------------------
+class _CtypesNvml:
+    """Minimal NVML reader over the driver's libnvidia-ml.so.1 (read-only
+    queries: clocks and clock-event reasons), used when pynvml is absent."""
+
+    NVML_CLOCK_SM = 1
+
+    def __init__(self):
+        import ctypes
+
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        rc = self.lib.nvmlInit_v2()
+        if rc != 0:
+            raise RuntimeError(f"nvmlInit_v2 failed ({rc})")
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self._reasons_fn = fn or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def handle(self, uuid: str | None, index: int):
+        h = self.ct.c_void_p()
+        if uuid is not None and self.lib.nvmlDeviceGetHandleByUUID(
+                self.ct.c_char_p(uuid.encode()), self.ct.byref(h)) == 0:
+            return h
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(self.ct.c_uint(index), self.ct.byref(h)) != 0:
+            raise RuntimeError("no NVML handle")
+        return h
+
+    def clock(self, h) -> int:
+        v = self.ct.c_uint()
+        self.lib.nvmlDeviceGetClockInfo(h, self.NVML_CLOCK_SM, self.ct.byref(v))
+        return v.value
+
+    def max_clock(self, h) -> int:
+        v = self.ct.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, self.ct.byref(v))
+        return v.value
+
+    def reasons(self, h) -> int:
+        v = self.ct.c_ulonglong()
+        self._reasons_fn(h, self.ct.byref(v))
+        return v.value
+
+
+class _PyNvml:
+    def __init__(self):
+        import pynvml
+
+        pynvml.nvmlInit()
+        self.nv = pynvml
+        fn = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self._reasons_fn = fn or pynvml.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def handle(self, uuid, index):
+        try:
+            return self.nv.nvmlDeviceGetHandleByUUID(uuid)
+        except Exception:
+            return self.nv.nvmlDeviceGetHandleByIndex(index)
+
+    def clock(self, h):
+        return self.nv.nvmlDeviceGetClockInfo(h, self.nv.NVML_CLOCK_SM)
+
+    def max_clock(self, h):
+        return self.nv.nvmlDeviceGetMaxClockInfo(h, self.nv.NVML_CLOCK_SM)
+
+    def reasons(self, h):
+        return self._reasons_fn(h)
+
+
+class ClockSampler:
+    """Samples the SM clock and the clock-event (throttle) reasons through
+    NVML in a background thread while the timed region runs.  Read-only."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x2: "applications_clocks_setting", 0x1: "gpu_idle", 0x10: "sync_boost"}
+
+    def __init__(self, device_index: int, period_s: float = 0.002):
+        self.period = period_s
+        self.samples, self.reasons = [], set()
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self.handle = None
+        self.error = None
+        try:
+            import torch
+
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            uuid = None
+        errors = []
+        for impl in (_PyNvml, _CtypesNvml):
+            try:
+                self.nvml = impl()
+                self.handle = self.nvml.handle(uuid, device_index)
+                self.max_mhz = self.nvml.max_clock(self.handle)
+                self.backend = impl.__name__
+                break
+            except Exception as e:
+                errors.append(repr(e))
+                self.handle = None
+        if self.handle is None:
+            self.error = "; ".join(errors)
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self.nvml.clock(self.handle))
+                r = self.nvml.reasons(self.handle)
+                for bit, name in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.handle is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._thread:
+            self._thread.join()
+
+    def summary(self) -> dict:
+        if self.handle is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": self.error}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons - {"gpu_idle"}),
+                "samples": len(self.samples), "source": f"NVML ({self.backend})"}
+
+
+# ----------------------------------------------------------------------------
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def barrier_max(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------
+def _oracle_sample(cfg, x, nb: int, k: int):
+    """fp64 arguments for the first nb whole batches, or (nb == 0) for the
+    first k channels of batch 0."""
+    from selective_state_space_140_b300 import workloads
+
+    f = workloads.to_f64
+    if nb > 0:
+        sl = lambda t: None if t is None else f(t[0:nb])
+        a = (sl(x["u"]), sl(x["delta"]), f(x["A_log"]), sl(x["B"]), sl(x["C"]))
+        kw = dict(D=f(x["D"]), z=sl(x["z"]), delta_bias=f(x["delta_bias"]))
+        chains = nb * cfg.dim
+        what = (f"all {cfg.batch} batches" if nb == cfg.batch else f"batches 0..{nb - 1}") + \
+            f" x {cfg.dim} channels"
+    else:
+        sl = lambda t: None if t is None else f(t[0:1, 0:k])
+        sd = lambda t: None if t is None else f(t[0:k])
+        a = (sl(x["u"]), sl(x["delta"]), f(x["A_log"][0:k]), f(x["B"][0:1]), f(x["C"][0:1]))
+        kw = dict(D=sd(x["D"]), z=sl(x["z"]), delta_bias=sd(x["delta_bias"]))
+        chains = k
+        what = f"channels 0..{k - 1} of batch 0"
+    kw["softplus"] = x["softplus"]
+    return a, kw, chains, what
+
+
+def choose_sample(cfg, x, seconds: float):
+    """Calibrate the oracle on a few chains and pick the largest prefix of the
+    workload (whole batches, else channels of batch 0) that fits `seconds`."""
+    import oracle
+
+    lib = oracle.load()
+    cores = oracle.hw_threads(lib)
+    k0 = max(1, min(cfg.dim, cores))
+    a, kw, chains, _ = _oracle_sample(cfg, x, 0, k0)
+    t0 = time.perf_counter()
+    oracle.selective_scan(*a, nthreads=0, lib=lib, **kw)
+    per_chain = (time.perf_counter() - t0) / chains
+    fit = seconds / max(per_chain, 1e-12)
+    if fit >= cfg.dim:
+        return min(cfg.batch, int(fit // cfg.dim)), 0
+    return 0, max(k0, int(fit))
+
+
+def cpu_oracle_rate(cfg, x, seconds: float):
+    """The fp64 oracle, as it stands, on all host cores over a bounded sample
+    of the workload sized to take about `seconds`."""
+    import oracle
+
+    nb, k = choose_sample(cfg, x, seconds)
+    a, kw, chains, what = _oracle_sample(cfg, x, nb, k)
+    t0 = time.perf_counter()
+    _, _, used = oracle.selective_scan(*a, nthreads=0, **kw)
+    dt = time.perf_counter() - t0
+    updates = chains * cfg.seqlen * cfg.dstate
+    return {"value": updates / dt, "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": f"fp64 oracle over {what}, full L={cfg.seqlen}, N={cfg.dstate} "
+                      f"({updates:.3g} updates in {dt:.2f} s)"}
+
+
+# ----------------------------------------------------------------------------
+def measure_ex2_rate(ub, device) -> dict:
+    """Peak SFU ex2 throughput of this GPU, measured now (best of 5)."""
+    import ctypes
+
+    import torch
+
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    blocks, threads, iters = sms * 8, 256, 2048
+    out = torch.empty(blocks * threads, device=device)
+    s = torch.cuda.current_stream(device)
+    best = None
+    for fn_name in ("mamba_ubench_ex2", "mamba_ubench_ffma2"):
+        fn = getattr(ub, fn_name)
+        fn.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+        times = []
+        for _ in range(6):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            rc = fn(out.data_ptr(), blocks, threads, iters, s.cuda_stream)
+            e1.record(s)
+            e1.synchronize()
+            assert rc == 0, f"{fn_name} failed ({rc})"
+            times.append(e0.elapsed_time(e1) / 1e3)
+        ops = blocks * threads * iters * 8
+        rate = ops / min(times[1:])
+        if fn_name == "mamba_ubench_ex2":
+            best = {"ex2_per_s": rate}
+        else:
+            best["ffma2_per_s"] = rate
+    best["sms"] = sms
+    return best
+
+
+def run_ours(args, cfg, dcfg, rank, world, local):
+    import ctypes
+
+    import torch
+
+    from selective_state_space_140_b300 import abi, build, workloads
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+    build.build()
+    lib = abi.load()
+    ub = ctypes.CDLL(build.UBENCH_LIB)
+    cnt = scan_counts(cfg)
+    peaks = measured_peaks()
+
+    x = workloads.make_config_inputs(cfg)
+    xd = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    y = torch.empty_like(xd["u"])
+    h = torch.empty((cfg.batch, cfg.dim, cfg.dstate), device=device, dtype=torch.float32)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        abi.mamba_selective_scan_fwd(xd["u"], xd["delta"], xd["A_log"], xd["B"], xd["C"],
+                                     D=xd["D"], z=xd["z"], delta_bias=xd["delta_bias"],
+                                     softplus=xd["softplus"], y=y, last_state=h, stream=stream)
+
+    sfu = measure_ex2_rate(ub, device)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        e1.synchronize()
+        torch.cuda.synchronize()
+        barrier(world)
+    t_total = e0.elapsed_time(e1) / 1e3
+    t_total = barrier_max(t_total, world, device)
+    t_step = t_total / args.steps
+
+    value = world * cnt["updates"] / t_step
+    gbs = cnt["bytes"] / t_step / 1e9
+    hbm_peak = float(peaks["hbm_gbs"])
+    exp_rate = cnt["exps"] / t_step
+    t_hbm = cnt["bytes"] / (hbm_peak * 1e9)
+    t_sfu = cnt["exps"] / sfu["ex2_per_s"]
+    khash = kernel_source_hash()
+    traffic = stored_traffic(args.workload, khash)
+    roof_hbm = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(gbs / hbm_peak, 4), "traffic": traffic,
+                "peak_source": f"{peaks['_source']} hbm_gbs (MEASURED_PEAKS.json)"}
+    roof_sfu = {"bound": "alu", "achieved": round(exp_rate / 1e9, 1),
+                "peak": round(sfu["ex2_per_s"] / 1e9, 1), "unit": "Gexp/s",
+                "frac": round(exp_rate / sfu["ex2_per_s"], 4), "traffic": traffic,
+                "peak_source": "ex2.approx throughput micro-benchmark, this GPU, this run",
+                "exps_per_launch": cnt["exps"]}
+    binding = roof_sfu if t_sfu >= t_hbm else roof_hbm
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": cfg.io_dtype, "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: {cfg.description}", "batch": cfg.batch,
+                   "dim": cfg.dim, "seqlen": cfg.seqlen, "dstate": cfg.dstate,
+                   "io_dtype": cfg.io_dtype, "state_dtype": "f32",
+                   "parallelism": f"replicas x{world} (independent batches, no collective)",
+                   "l2": f"inputs {cnt['input_bytes'] / 2**20:.0f} MiB > L2 126 MiB; no flush"},
+        "gbs": round(gbs, 1),
+        "roofline": binding,
+        "roofline_hbm": roof_hbm,
+        "roofline_sfu": roof_sfu,
+        "binding_unit": "sfu" if t_sfu >= t_hbm else "hbm",
+        "t_floor_us": {"hbm": round(t_hbm * 1e6, 1), "sfu": round(t_sfu * 1e6, 1)},
+        "ubench": {k: (round(v / 1e9, 1) if k.endswith("_per_s") else v) for k, v in sfu.items()},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "kernel_source_sha256_16": khash,
+        "algorithmic_bytes_per_launch": cnt["bytes"],
+    }
+
+    if not args.no_decode:
+        result["decode"] = bench_decode(args, dcfg, device, peaks)
+    if not args.no_e2e:
+        result["e2e"] = bench_e2e(args, cfg, x, device, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_oracle_rate(cfg, x, args.cpu_seconds)
+    elif rank == 0:
+        result["cpu_baseline"] = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return result
+
+
+def bench_decode(args, dcfg, device, peaks) -> dict:
+    """Decode step on its own workload; the state rotates over enough buffers
+    that each step's state is out of L2 when it is reused."""
+    import torch
+
+    from selective_state_space_140_b300 import abi, workloads
+
+    x = workloads.make_decode_inputs(dcfg.batch, dcfg.dim, dcfg.dstate, dcfg.io_dtype, dcfg.seed)
+    xd = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    nbuf = max(2, int(2 * L2_BYTES // xd["state"].numel() // 4) + 2)
+    states = [xd["state"].clone() for _ in range(nbuf)]
+    out = torch.empty_like(xd["x"])
+    stream = torch.cuda.current_stream(device)
+    cnt = decode_counts(dcfg)
+
+    def step(i):
+        abi.mamba_selective_state_update(states[i % nbuf], xd["x"], xd["dt"], xd["A_log"], xd["B"],
+                                         xd["C"], D=xd["D"], z=xd["z"], dt_bias=xd["dt_bias"],
+                                         softplus=True, out=out, stream=stream)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    steps = max(20, min(args.steps, 2000))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    e1.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / steps
+    gbs = cnt["bytes"] / t / 1e9
+    return {"workload": f"{dcfg.name}: {dcfg.description}", "us_per_step": round(t * 1e6, 2),
+            "state_updates_per_s": cnt["updates"] / t, "gbs": round(gbs, 1),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
+                         "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
+                         "frac": round(gbs / float(peaks["hbm_gbs"]), 4), "traffic": None},
+            "steps": steps, "state_buffers": nbuf, "gpu_launches": steps}
+
+
+def bench_e2e(args, cfg, x, device, world) -> dict:
+    """Same metric through the public binding with pinned host buffers: each
+    step copies its inputs host->device, runs the scan and copies y and the
+    final state back, all inside the timed region."""
+    import torch
+
+    from selective_state_space_140_b300 import abi
+
+    names = ("u", "delta", "z", "B", "C")
+    host = {k: x[k].pin_memory() for k in names}
+    dev = {k: torch.empty_like(host[k], device=device) for k in names}
+    params = {k: x[k].to(device) for k in ("A_log", "D", "delta_bias")}
+    y_d = torch.empty_like(dev["u"])
+    h_d = torch.empty((cfg.batch, cfg.dim, cfg.dstate), device=device)
+    y_h = torch.empty(y_d.shape, dtype=y_d.dtype).pin_memory()
+    h_h = torch.empty(h_d.shape, dtype=h_d.dtype).pin_memory()
+    stream = torch.cuda.current_stream(device)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in names)
+    d2h = y_h.numel() * y_h.element_size() + h_h.numel() * h_h.element_size()
+
+    def step():
+        for k in names:
+            dev[k].copy_(host[k], non_blocking=True)
+        abi.mamba_selective_scan_fwd(dev["u"], dev["delta"], params["A_log"], dev["B"], dev["C"],
+                                     D=params["D"], z=dev["z"], delta_bias=params["delta_bias"],
+                                     softplus=True, y=y_d, last_state=h_d, stream=stream)
+        y_h.copy_(y_d, non_blocking=True)
+        h_h.copy_(h_d, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, args.e2e_steps))
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    t = time.perf_counter() - t0
+    t = barrier_max(t, world, device)
+    updates = world * cfg.batch * cfg.dim * cfg.seqlen * cfg.dstate
+    return {"value": updates * steps / t, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(t / steps * 1e3, 3),
+            "api": "selective_state_space_140_b300.abi.mamba_selective_scan_fwd (C ABI)",
+            "note": "A_log, D and bias are parameters kept on the device"}
+
+
+def run_reference(args, cfg) -> dict:
+    """The oracle as it stands, on the host cores, each step a bounded sample."""
+    import oracle
+    from selective_state_space_140_b300 import workloads
+
+    x = workloads.make_config_inputs(cfg)
+    per_step = max(0.05, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    nb, k = choose_sample(cfg, x, per_step)
+    a, kw, chains, what = _oracle_sample(cfg, x, nb, k)
+    for _ in range(args.warmup):
+        oracle.selective_scan(*a, nthreads=0, **kw)
+    t0 = time.perf_counter()
+    used = 0
+    for _ in range(args.steps):
+        _, _, used = oracle.selective_scan(*a, nthreads=0, **kw)
+    t = time.perf_counter() - t0
+    updates = chains * cfg.seqlen * cfg.dstate
+    value = updates * args.steps / t
+    sample = (f"fp64 oracle over {what}, full L={cfg.seqlen}, N={cfg.dstate} per step "
+              f"({updates:.3g} updates)")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: {cfg.description}", "batch": cfg.batch,
+                   "dim": cfg.dim, "seqlen": cfg.seqlen, "dstate": cfg.dstate,
+                   "io_dtype": cfg.io_dtype},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    args.steps = max(1, args.steps)
+
+    from selective_state_space_140_b300 import workloads
+
+    cfg = workloads.SCAN_CONFIGS[args.workload]
+    dcfg = workloads.DECODE_CONFIGS["decode_bf16"]
+    rank, world, local = dist_info()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, cfg)), flush=True)
+        return 0
+
+    result = run_ours(args, cfg, dcfg, rank, world, local)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,137 @@
+/*
+ * mamba_scan.h -- C ABI of libmamba_scan.so, a B300 (sm_103a) implementation
+ * of the Mamba selective scan and its single-token decode step.
+ *
+ * Operation (definitions restated from the pages this library follows):
+ *   - Discrete state-space recurrence h_t = Abar_t h_{t-1} + Bbar_t u_t,
+ *     y_t = C_t h_t + D u_t, started from h = 0 ("图解 Mamba 状态空间模型"
+ *     tutorial, "数学基础"; highthink.cn Keras SelectiveSSM listing, where the
+ *     scan's initial state is zeros and D*u is added to C.state).
+ *   - Diagonal A = -exp(A_log) per (channel, state), Abar = exp(dt*A), and the
+ *     small-step form Bbar = dt*B (highthink.cn listing; tutorial step 1, where
+ *     Bbar ~ dt*B "when dt is small").
+ *   - Input-dependent step dt = softplus(delta + bias) (codechina.net
+ *     overview, section 2.1; highthink.cn dt_proj with a bias).
+ *   - The result is gated by SiLU(z), the second branch of the Mamba block
+ *     (highthink.cn block diagram: x -> SSM, multiplied by the SiLU branch).
+ *   - One fused kernel: parameters are read from HBM once, discretisation and
+ *     recurrence happen on chip, and only the result is written (codechina.net
+ *     overview, section 1 "硬件感知算法" and section 2.2 "核融合").
+ *
+ * So for every batch b, channel d, time t and state n:
+ *   dt      = softplus_flag ? softplus(delta[b,d,t] + bias[d]) : delta[b,d,t] + bias[d]
+ *   h[n]    = exp(dt * -exp(A_log[d,n])) * h[n] + dt * B[b,t,n] * u[b,d,t]
+ *   out     = (sum_n C[b,t,n] * h[n] + D[d] * u[b,d,t]) * SiLU(z[b,d,t])
+ *   y[b,d,t] = out;  last_state[b,d,n] = h[n] after t = seqlen-1.
+ *
+ * Conventions shared by every entry point
+ *   - All pointers are DEVICE pointers owned by the caller.  Arrays are dense
+ *     row-major with the shapes given below.  The library keeps no state
+ *     between calls and allocates no memory.
+ *   - io_dtype (MAMBA_F32 or MAMBA_BF16) is the element type of every
+ *     "io" array (u, delta, z, B, C, y; x, dt, z, B, C, out for decode).
+ *     A_log, D, the bias and the state are always fp32.  Arithmetic is fp32;
+ *     bf16 results are rounded to nearest even.
+ *   - Work is enqueued on `stream` (0 = legacy default stream) and runs
+ *     asynchronously; the call does not synchronise.  A non-zero return means
+ *     nothing was launched (argument errors) or the launch failed
+ *     (MAMBA_ERR_LAUNCH, with the CUDA error left for cudaGetLastError).
+ *   - Pointers must be aligned to their element size (4 bytes for fp32, 2 for
+ *     bf16), else MAMBA_ERR_ALIGN.  Wider alignment (16 bytes, with row
+ *     lengths that keep it) lets the kernels use 128-bit accesses; any other
+ *     aligned input takes a scalar path and gives the same results.
+ *   - Outputs must not overlap inputs (MAMBA_ERR_ALIAS), except that the
+ *     decode state is updated in place by design.
+ *   - A required array that has no elements (a zero size) may be NULL.
+ */
+#ifndef MAMBA_SCAN_H
+#define MAMBA_SCAN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so that this header needs no CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st *mamba_stream_t;
+
+typedef enum { MAMBA_F32 = 0, MAMBA_BF16 = 1 } mamba_dtype_t;
+
+typedef enum {
+    MAMBA_OK = 0,
+    MAMBA_ERR_NULL = 1,    /* a required pointer is NULL                         */
+    MAMBA_ERR_SIZE = 2,    /* a size is negative or the problem is too large     */
+    MAMBA_ERR_DSTATE = 3,  /* dstate outside [1, MAMBA_MAX_DSTATE]               */
+    MAMBA_ERR_ALIGN = 4,   /* a pointer is not aligned to its element size       */
+    MAMBA_ERR_DTYPE = 5,   /* io_dtype is not a mamba_dtype_t                    */
+    MAMBA_ERR_LAUNCH = 6,  /* the CUDA launch failed (see cudaGetLastError)      */
+    MAMBA_ERR_TIMEOUT = 7, /* reserved: a bounded device-side wait gave up       */
+    MAMBA_ERR_ALIAS = 8    /* an output overlaps an input                        */
+} mamba_status_t;
+
+#define MAMBA_MAX_DSTATE 256
+
+/*
+ * Selective scan, forward.
+ *
+ *   u, delta, z : [batch, dim, seqlen] io_dtype (time contiguous)
+ *   B, C        : [batch, seqlen, dstate] io_dtype, shared by all channels
+ *   A_log       : [dim, dstate] fp32;  A = -exp(A_log)
+ *   D           : [dim] fp32 or NULL (no skip term)
+ *   z           : NULL means no gate
+ *   delta_bias  : [dim] fp32 or NULL (no bias)
+ *   softplus_flag: non-zero applies softplus to delta + bias
+ *   y           : [batch, dim, seqlen] io_dtype, written
+ *   last_state  : [batch, dim, dstate] fp32 or NULL; receives h after the last
+ *                 step (zeros when seqlen == 0)
+ *
+ * batch, dim, seqlen may be zero (nothing to compute; last_state is still
+ * zeroed when seqlen == 0).  Returns MAMBA_OK or an error code as above.
+ */
+int mamba_selective_scan_fwd(const void *u, const void *delta, const float *A_log,
+                             const void *B, const void *C, const float *D, const void *z,
+                             const float *delta_bias, int softplus_flag, void *y,
+                             float *last_state, int64_t batch, int64_t dim, int64_t seqlen,
+                             int64_t dstate, int io_dtype, mamba_stream_t stream);
+
+/*
+ * Single-token decode step (recurrent inference: each new token touches only
+ * the previous state -- tutorial "核心概念"; mhpn.cn article section 3).
+ *
+ *   state       : [batch, dim, dstate] fp32, read and updated IN PLACE
+ *   x, dt, z    : [batch, dim] io_dtype (z may be NULL: no gate)
+ *   A_log       : [dim, dstate] fp32
+ *   B, C        : [batch, dstate] io_dtype
+ *   D, dt_bias  : [dim] fp32 or NULL
+ *   out         : [batch, dim] io_dtype, written
+ *
+ * Same as one step of mamba_selective_scan_fwd started from `state`.
+ */
+int mamba_selective_state_update(float *state, const void *x, const void *dt,
+                                 const float *A_log, const void *B, const void *C,
+                                 const float *D, const void *z, const float *dt_bias,
+                                 int softplus_flag, void *out, int64_t batch, int64_t dim,
+                                 int64_t dstate, int io_dtype, mamba_stream_t stream);
+
+/*
+ * Wait for the work queued on `stream`, then report and clear the device-side
+ * error word of this library's kernels on the current device: MAMBA_ERR_TIMEOUT
+ * if a bounded on-device wait (for a bulk copy into shared memory) gave up, in
+ * which case the outputs of the affected call are not valid.  Returns
+ * MAMBA_ERR_LAUNCH if the synchronisation itself reports a CUDA error.
+ */
+int mamba_device_status(mamba_stream_t stream);
+
+/* Human-readable name of a mamba_status_t; never NULL. */
+const char *mamba_status_string(int status);
+
+/* Version of this ABI (major * 10000 + minor * 100 + patch). */
+int mamba_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAMBA_SCAN_H */

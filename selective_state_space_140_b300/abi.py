@@ -1,0 +1,189 @@
+"""Thin ctypes binding of libmamba_scan.so (declared in include/mamba_scan.h).
+
+The functions here carry the C entry points' names and do argument
+marshalling only: device pointers, sizes, the io dtype and the current CUDA
+stream go straight into the C call, and a non-zero status raises
+``MambaError``.  Every step of the scan runs in the library's CUDA kernels;
+there is no fallback of any kind, and a missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmamba_scan.so")
+
+MAMBA_F32, MAMBA_BF16 = 0, 1
+STATUS = {0: "MAMBA_OK", 1: "MAMBA_ERR_NULL", 2: "MAMBA_ERR_SIZE", 3: "MAMBA_ERR_DSTATE",
+          4: "MAMBA_ERR_ALIGN", 5: "MAMBA_ERR_DTYPE", 6: "MAMBA_ERR_LAUNCH",
+          7: "MAMBA_ERR_TIMEOUT", 8: "MAMBA_ERR_ALIAS"}
+MAX_DSTATE = 256
+
+# Every symbol include/mamba_scan.h declares.
+EXPORTED = ("mamba_selective_scan_fwd", "mamba_selective_state_update", "mamba_device_status",
+            "mamba_status_string", "mamba_abi_version")
+
+_lib = None
+
+
+class MambaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def _declare(lib):
+    vp, fp, i64, ci = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.mamba_selective_scan_fwd.restype = ci
+    lib.mamba_selective_scan_fwd.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, vp, fp,
+                                             i64, i64, i64, i64, ci, vp]
+    lib.mamba_selective_state_update.restype = ci
+    lib.mamba_selective_state_update.argtypes = [fp, vp, vp, fp, vp, vp, fp, vp, fp, ci, vp,
+                                                 i64, i64, i64, ci, vp]
+    lib.mamba_status_string.restype = ctypes.c_char_p
+    lib.mamba_status_string.argtypes = [ci]
+    lib.mamba_abi_version.restype = ci
+    lib.mamba_abi_version.argtypes = []
+    lib.mamba_device_status.restype = ci
+    lib.mamba_device_status.argtypes = [vp]
+    return lib
+
+
+def load(path: str = LIB_PATH):
+    """Load the CUDA library; raise if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -m selective_state_space_140_b300.build`")
+        _lib = _declare(ctypes.CDLL(path))
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().mamba_status_string(int(status)).decode()
+
+
+def abi_version() -> int:
+    return load().mamba_abi_version()
+
+
+def mamba_device_status(stream=None, device=None) -> int:
+    """Synchronise the stream and return (and clear) the device-side status:
+    0, or MAMBA_ERR_TIMEOUT (7) if an on-device bounded wait gave up."""
+    dev = device or torch.device("cuda", torch.cuda.current_device())
+    return load().mamba_device_status(_stream(stream, dev))
+
+
+def _io_dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return MAMBA_F32
+    if t.dtype == torch.bfloat16:
+        return MAMBA_BF16
+    raise TypeError(f"io tensors must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check(t, name, device, dtype=None):
+    if t is None:
+        return
+    if not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be on {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _stream(stream, device):
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def mamba_selective_scan_fwd(u, delta, A_log, B, C, D=None, z=None, delta_bias=None,
+                             softplus=True, y=None, last_state=None, want_last_state=True,
+                             stream=None):
+    """Launch the fused forward scan; return ``(y, last_state)``.
+
+    u, delta, z: [batch, dim, seqlen]; B, C: [batch, seqlen, dstate] (same io
+    dtype, float32 or bfloat16); A_log [dim, dstate], D and delta_bias [dim] are
+    float32.  ``y`` / ``last_state`` are allocated when not given
+    (``last_state`` only if ``want_last_state``).  Runs on ``stream`` (default:
+    the current stream) and does not synchronise.
+    """
+    dev = u.device
+    batch, dim, seqlen = u.shape
+    dstate = A_log.shape[-1]
+    io = _io_dtype(u)
+    for t, n in ((u, "u"), (delta, "delta"), (z, "z"), (B, "B"), (C, "C"), (y, "y")):
+        _check(t, n, dev, u.dtype)
+    for t, n in ((A_log, "A_log"), (D, "D"), (delta_bias, "delta_bias"),
+                 (last_state, "last_state")):
+        _check(t, n, dev, torch.float32)
+    if y is None:
+        y = torch.empty_like(u)
+    if last_state is None and want_last_state:
+        last_state = torch.empty((batch, dim, dstate), device=dev, dtype=torch.float32)
+    rc = load().mamba_selective_scan_fwd(
+        _ptr(u), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+        int(bool(softplus)), _ptr(y), _ptr(last_state), batch, dim, seqlen, dstate, io,
+        _stream(stream, dev))
+    if rc != 0:
+        raise MambaError(rc, "mamba_selective_scan_fwd")
+    return y, last_state
+
+
+def mamba_selective_state_update(state, x, dt, A_log, B, C, D=None, z=None, dt_bias=None,
+                                 softplus=True, out=None, stream=None):
+    """One decode step; ``state`` [batch, dim, dstate] fp32 is updated in place.
+
+    x, dt, z: [batch, dim]; B, C: [batch, dstate] (float32 or bfloat16).
+    Returns ``out`` [batch, dim].
+    """
+    dev = state.device
+    batch, dim, dstate = state.shape
+    io = _io_dtype(x)
+    _check(state, "state", dev, torch.float32)
+    for t, n in ((x, "x"), (dt, "dt"), (z, "z"), (B, "B"), (C, "C"), (out, "out")):
+        _check(t, n, dev, x.dtype)
+    for t, n in ((A_log, "A_log"), (D, "D"), (dt_bias, "dt_bias")):
+        _check(t, n, dev, torch.float32)
+    if out is None:
+        out = torch.empty_like(x)
+    rc = load().mamba_selective_state_update(
+        _ptr(state), _ptr(x), _ptr(dt), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+        _ptr(dt_bias), int(bool(softplus)), _ptr(out), batch, dim, dstate, io,
+        _stream(stream, dev))
+    if rc != 0:
+        raise MambaError(rc, "mamba_selective_state_update")
+    return out
+
+
+def raw_scan_fwd(u, delta, A_log, B, C, D, z, delta_bias, softplus_flag, y, last_state,
+                 batch, dim, seqlen, dstate, io_dtype, stream) -> int:
+    """The C entry point with plain integers as pointers; returns the status code.
+
+    Lets tests exercise the C validation (NULL pointers, bad sizes, misaligned
+    addresses) without building tensors.  No pointer is dereferenced on the
+    host; argument errors return before any CUDA call.
+    """
+    return load().mamba_selective_scan_fwd(u, delta, A_log, B, C, D, z, delta_bias,
+                                           softplus_flag, y, last_state, batch, dim, seqlen,
+                                           dstate, io_dtype, stream)
+
+
+def raw_state_update(state, x, dt, A_log, B, C, D, z, dt_bias, softplus_flag, out, batch, dim,
+                     dstate, io_dtype, stream) -> int:
+    """``mamba_selective_state_update`` with plain integers as pointers."""
+    return load().mamba_selective_state_update(state, x, dt, A_log, B, C, D, z, dt_bias,
+                                               softplus_flag, out, batch, dim, dstate, io_dtype,
+                                               stream)

@@ -1,0 +1,142 @@
+// C entry points of libmamba_scan.so: argument validation, then one launch.
+// The declarations, layouts and error conventions are in include/mamba_scan.h.
+#include "../../include/mamba_scan.h"
+#include "common.cuh"
+
+namespace {
+
+constexpr int64_t kMaxElems = int64_t(1) << 46;  // keeps every index far from overflow
+
+size_t io_size(int io_dtype) { return io_dtype == MAMBA_BF16 ? 2 : 4; }
+
+bool misaligned(const void* p, size_t align) {
+    return p != nullptr && (reinterpret_cast<uintptr_t>(p) % align) != 0;
+}
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+Range range_of(const void* p, int64_t elems, size_t esize) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return {lo, lo + uintptr_t(elems) * esize};
+}
+
+bool overlaps(Range a, Range b) {
+    if (a.lo == 0 || b.lo == 0 || a.lo == a.hi || b.lo == b.hi) return false;
+    return a.lo < b.hi && b.lo < a.hi;
+}
+
+bool size_ok(int64_t a, int64_t b, int64_t c) {
+    if (a < 0 || b < 0 || c < 0) return false;
+    if (a == 0 || b == 0 || c == 0) return true;
+    if (a > kMaxElems / b) return false;
+    return a * b <= kMaxElems / c;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mamba_abi_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+const char* mamba_status_string(int status) {
+    switch (status) {
+        case MAMBA_OK: return "MAMBA_OK";
+        case MAMBA_ERR_NULL: return "MAMBA_ERR_NULL: a required pointer is NULL";
+        case MAMBA_ERR_SIZE: return "MAMBA_ERR_SIZE: a size is negative or too large";
+        case MAMBA_ERR_DSTATE: return "MAMBA_ERR_DSTATE: dstate must be in [1, 256]";
+        case MAMBA_ERR_ALIGN: return "MAMBA_ERR_ALIGN: a pointer is not aligned to its element size";
+        case MAMBA_ERR_DTYPE: return "MAMBA_ERR_DTYPE: io_dtype must be MAMBA_F32 or MAMBA_BF16";
+        case MAMBA_ERR_LAUNCH: return "MAMBA_ERR_LAUNCH: the CUDA launch failed";
+        case MAMBA_ERR_TIMEOUT: return "MAMBA_ERR_TIMEOUT: a bounded device-side wait gave up";
+        case MAMBA_ERR_ALIAS: return "MAMBA_ERR_ALIAS: an output overlaps an input";
+        default: return "unknown mamba_status_t";
+    }
+}
+
+int mamba_selective_scan_fwd(const void* u, const void* delta, const float* A_log, const void* B,
+                             const void* C, const float* D, const void* z,
+                             const float* delta_bias, int softplus_flag, void* y,
+                             float* last_state, int64_t batch, int64_t dim, int64_t seqlen,
+                             int64_t dstate, int io_dtype, mamba_stream_t stream) {
+    if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
+    if (dstate < 1 || dstate > MAMBA_MAX_DSTATE) return MAMBA_ERR_DSTATE;
+    if (!size_ok(batch, dim, seqlen) || !size_ok(batch, seqlen, dstate) ||
+        !size_ok(batch, dim, dstate))
+        return MAMBA_ERR_SIZE;
+    // An array with no elements may be NULL (empty tensors have no storage).
+    const bool has_elems = batch * dim * seqlen > 0, has_bc = batch * seqlen > 0;
+    if ((has_elems && (!u || !delta || !y)) || (has_bc && (!B || !C)) || (dim > 0 && !A_log))
+        return MAMBA_ERR_NULL;
+    const size_t es = io_size(io_dtype);
+    if (misaligned(u, es) || misaligned(delta, es) || misaligned(z, es) || misaligned(B, es) ||
+        misaligned(C, es) || misaligned(y, es) || misaligned(A_log, 4) || misaligned(D, 4) ||
+        misaligned(delta_bias, 4) || misaligned(last_state, 4))
+        return MAMBA_ERR_ALIGN;
+    const int64_t elems = batch * dim * seqlen;
+    const Range ry = range_of(y, elems, es);
+    const Range rs = last_state ? range_of(last_state, batch * dim * dstate, 4) : Range{0, 0};
+    const Range ins[] = {range_of(u, elems, es), range_of(delta, elems, es),
+                         z ? range_of(z, elems, es) : Range{0, 0},
+                         range_of(B, batch * seqlen * dstate, es),
+                         range_of(C, batch * seqlen * dstate, es),
+                         range_of(A_log, dim * dstate, 4),
+                         D ? range_of(D, dim, 4) : Range{0, 0},
+                         delta_bias ? range_of(delta_bias, dim, 4) : Range{0, 0}};
+    for (const Range& r : ins)
+        if (overlaps(ry, r) || overlaps(rs, r)) return MAMBA_ERR_ALIAS;
+    if (overlaps(ry, rs)) return MAMBA_ERR_ALIAS;
+    if (batch == 0 || dim == 0) return MAMBA_OK;
+
+    mamba::ScanArgs a{u, delta, A_log, B, C, D, z, delta_bias, y, last_state,
+                      batch, dim, seqlen, int(dstate), softplus_flag != 0};
+    const cudaError_t err =
+        mamba::launch_scan_fwd(a, io_dtype == MAMBA_BF16, reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
+}
+
+int mamba_device_status(mamba_stream_t stream) {
+    unsigned int word = 0;
+    const cudaError_t err =
+        mamba::read_and_clear_device_error(&word, reinterpret_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return MAMBA_ERR_LAUNCH;
+    return (word & mamba::kErrWaitTimeout) ? MAMBA_ERR_TIMEOUT : MAMBA_OK;
+}
+
+int mamba_selective_state_update(float* state, const void* x, const void* dt,
+                                 const float* A_log, const void* B, const void* C,
+                                 const float* D, const void* z, const float* dt_bias,
+                                 int softplus_flag, void* out, int64_t batch, int64_t dim,
+                                 int64_t dstate, int io_dtype, mamba_stream_t stream) {
+    if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
+    if (dstate < 1 || dstate > MAMBA_MAX_DSTATE) return MAMBA_ERR_DSTATE;
+    if (!size_ok(batch, dim, dstate)) return MAMBA_ERR_SIZE;
+    if (batch * dim > 0 && (!state || !x || !dt || !out)) return MAMBA_ERR_NULL;
+    if ((batch > 0 && (!B || !C)) || (dim > 0 && !A_log)) return MAMBA_ERR_NULL;
+    const size_t es = io_size(io_dtype);
+    if (misaligned(state, 4) || misaligned(x, es) || misaligned(dt, es) || misaligned(z, es) ||
+        misaligned(B, es) || misaligned(C, es) || misaligned(out, es) || misaligned(A_log, 4) ||
+        misaligned(D, 4) || misaligned(dt_bias, 4))
+        return MAMBA_ERR_ALIGN;
+    const Range ro = range_of(out, batch * dim, es);
+    const Range rs = range_of(state, batch * dim * dstate, 4);
+    const Range ins[] = {range_of(x, batch * dim, es), range_of(dt, batch * dim, es),
+                         z ? range_of(z, batch * dim, es) : Range{0, 0},
+                         range_of(B, batch * dstate, es), range_of(C, batch * dstate, es),
+                         range_of(A_log, dim * dstate, 4),
+                         D ? range_of(D, dim, 4) : Range{0, 0},
+                         dt_bias ? range_of(dt_bias, dim, 4) : Range{0, 0}};
+    for (const Range& r : ins)
+        if (overlaps(ro, r) || overlaps(rs, r)) return MAMBA_ERR_ALIAS;
+    if (overlaps(ro, rs)) return MAMBA_ERR_ALIAS;
+    if (batch == 0 || dim == 0) return MAMBA_OK;
+
+    mamba::StateUpdateArgs a{state, x, dt, A_log, B, C, D, z, dt_bias, out,
+                             batch, dim, int(dstate), softplus_flag != 0};
+    const cudaError_t err = mamba::launch_state_update(a, io_dtype == MAMBA_BF16,
+                                                       reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
+}
+
+}  // extern "C"

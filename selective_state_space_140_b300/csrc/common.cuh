@@ -1,0 +1,208 @@
+// Internal helpers of libmamba_scan.so (not part of the public ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mamba {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Bit set in the scan's device error word when a bounded wait gives up.
+constexpr unsigned int kErrWaitTimeout = 1u;
+
+// ---- element access for the two io types --------------------------------
+template <typename T>
+struct Io;
+
+template <>
+struct Io<float> {
+    static constexpr int kVec = 4;  // elements per 16-byte vector
+    static __device__ __forceinline__ float load(const float* p) { return __ldg(p); }
+    static __device__ __forceinline__ void store(float* p, float v) { *p = v; }
+    // element i of a 16-byte vector
+    static __device__ __forceinline__ float get(const uint4& v, int i) {
+        return __uint_as_float(i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w);
+    }
+};
+
+template <>
+struct Io<__nv_bfloat16> {
+    static constexpr int kVec = 8;
+    static __device__ __forceinline__ float load(const __nv_bfloat16* p) {
+        return __bfloat162float(__ldg(p));
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16* p, float v) {
+        *p = __float2bfloat16_rn(v);
+    }
+    static __device__ __forceinline__ float get(const uint4& v, int i) {
+        const unsigned w = (i >> 1) == 0 ? v.x : (i >> 1) == 1 ? v.y : (i >> 1) == 2 ? v.z : v.w;
+        return __uint_as_float((i & 1) ? (w & 0xffff0000u) : (w << 16));
+    }
+};
+
+// ---- special-function unit and packed fp32 arithmetic -----------------------
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Two fp32 lanes in one 64-bit register (sm_100+ packed f32x2 arithmetic).
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack2(f32x2 v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// ---- pointwise functions --------------------------------------------------
+// softplus(x) = log(1 + e^x), accurate version (fp32 io): libdevice expf and
+// log1pf; above 20 the correction is below 2e-9 relative and x is returned.
+__device__ __forceinline__ float softplus_accurate(float x) {
+    return x > 20.f ? x : log1pf(expf(x));
+}
+
+// softplus(x) = max(x, 0) + log1p(e^-|x|), on the SFU (bf16 io, whose inputs
+// carry 2^-9 relative rounding already).  log1p(e) uses its Taylor series
+// e - e^2/2 + e^3/3 - e^4/4 below e = 2^-7 (truncation < e^5/5) and
+// lg2(1 + e) * ln2 above, where the lg2 result is at least 0.011.
+__device__ __forceinline__ float softplus_fast(float x) {
+    const float e = ex2_approx(-fabsf(x) * kLog2e);
+    const float series = e * fmaf(e, fmaf(e, fmaf(e, -0.25f, 0.333333343f), -0.5f), 1.f);
+    const float lg = lg2_approx(1.f + e) * kLn2;
+    return fmaxf(x, 0.f) + (e < 0.0078125f ? series : lg);
+}
+
+// SiLU(z) = z * sigmoid(z) = z / (1 + e^-z), on the SFU.  For z << 0 the
+// exponential overflows to +inf and the reciprocal gives 0, so SiLU -> -0.
+__device__ __forceinline__ float silu_fast(float z) {
+    return z * rcp_approx(1.f + ex2_approx(-z * kLog2e));
+}
+
+// ---- mbarrier and bulk-copy (TMA) primitives ------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile(
+        "{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(
+            smem_addr(bar)),
+        "r"(bytes)
+        : "memory");
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` on `bar`.  Both addresses
+// 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Bounded wait for phase `parity` of `bar`.  A copy that never lands must not
+// hang the GPU: after the iteration limit this returns false, the caller
+// records the failure in its error word and carries on (its results are then
+// garbage, which the host learns from mamba_device_status()).
+constexpr uint32_t kWaitLimit = 1u << 24;
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    const uint32_t a = smem_addr(bar);
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(ok)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+
+// Arguments of one forward scan, as validated by the C entry point.
+struct ScanArgs {
+    const void* u;
+    const void* delta;
+    const float* A_log;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    const float* delta_bias;
+    void* y;
+    float* last_state;
+    int64_t batch, dim, seqlen;
+    int dstate;
+    int softplus;
+};
+
+struct StateUpdateArgs {
+    float* state;
+    const void* x;
+    const void* dt;
+    const float* A_log;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    const float* dt_bias;
+    void* out;
+    int64_t batch, dim;
+    int dstate;
+    int softplus;
+};
+
+// Launchers (return the cudaError_t of the launch).
+cudaError_t launch_scan_fwd(const ScanArgs& a, bool bf16, cudaStream_t stream);
+// Synchronise `stream`, then read and clear the scan's device error word.
+cudaError_t read_and_clear_device_error(unsigned int* word, cudaStream_t stream);
+cudaError_t launch_state_update(const StateUpdateArgs& a, bool bf16, cudaStream_t stream);
+
+}  // namespace mamba

@@ -1,0 +1,129 @@
+"""Host-side checks of the C ABI (no GPU needed, no CUDA call is reached).
+
+The library must load, export every function include/mamba_scan.h declares,
+and reject bad arguments with the documented status before touching CUDA.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from selective_state_space_140_b300 import abi, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mamba_scan.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return abi.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(mamba_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_abi():
+    assert declared_functions() == sorted(abi.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} is declared but not exported"
+
+
+def test_version_and_status_strings(lib):
+    assert abi.abi_version() == 10000
+    for code, name in abi.STATUS.items():
+        assert abi.status_string(code).startswith(name)
+    assert abi.status_string(12345) == "unknown mamba_status_t"
+
+
+# Fake, never-dereferenced device addresses (16-byte aligned, far apart).
+P = [0x7f0000000000 + i * 0x100000000 for i in range(12)]
+GOOD = dict(u=P[0], delta=P[1], A_log=P[2], B=P[3], C=P[4], D=P[5], z=P[6], delta_bias=P[7],
+            softplus_flag=1, y=P[8], last_state=P[9], batch=2, dim=8, seqlen=16, dstate=16,
+            io_dtype=abi.MAMBA_BF16, stream=None)
+
+
+def scan(**over):
+    kw = dict(GOOD)
+    kw.update(over)
+    return abi.raw_scan_fwd(**kw)
+
+
+@pytest.mark.parametrize("name", ["u", "delta", "A_log", "B", "C", "y"])
+def test_scan_rejects_null_required_pointer(lib, name):
+    assert scan(**{name: None}) == 1  # MAMBA_ERR_NULL
+
+
+@pytest.mark.parametrize("field,value", [("batch", -1), ("dim", -3), ("seqlen", -1),
+                                         ("batch", 1 << 40), ("seqlen", 1 << 45)])
+def test_scan_rejects_bad_sizes(lib, field, value):
+    assert scan(**{field: value}) == 2  # MAMBA_ERR_SIZE
+
+
+@pytest.mark.parametrize("dstate", [0, -1, 257, 1 << 20])
+def test_scan_rejects_bad_dstate(lib, dstate):
+    assert scan(dstate=dstate) == 3  # MAMBA_ERR_DSTATE
+
+
+@pytest.mark.parametrize("io", [-1, 2, 7])
+def test_scan_rejects_bad_dtype(lib, io):
+    assert scan(io_dtype=io) == 5  # MAMBA_ERR_DTYPE
+
+
+@pytest.mark.parametrize("name,io", [("u", abi.MAMBA_BF16), ("y", abi.MAMBA_F32),
+                                     ("A_log", abi.MAMBA_BF16), ("last_state", abi.MAMBA_BF16),
+                                     ("B", abi.MAMBA_F32)])
+def test_scan_rejects_misaligned(lib, name, io):
+    assert scan(**{name: GOOD[name] + 1, "io_dtype": io}) == 4  # MAMBA_ERR_ALIGN
+
+
+def test_scan_rejects_aliasing(lib):
+    assert scan(y=P[0]) == 8                 # y == u
+    assert scan(y=P[3] + 32) == 8            # y starts inside B
+    assert scan(last_state=P[2]) == 8        # state over A_log
+    assert scan(last_state=P[8] + 64) == 8   # state inside y
+
+
+def test_scan_empty_problems_return_ok_without_launch(lib):
+    # Nothing to compute: returns before any CUDA call, so this is safe on CPU.
+    assert scan(batch=0) == 0
+    assert scan(dim=0) == 0
+
+
+DGOOD = dict(state=P[0], x=P[1], dt=P[2], A_log=P[3], B=P[4], C=P[5], D=P[6], z=P[7], dt_bias=P[8],
+             softplus_flag=1, out=P[9], batch=4, dim=8, dstate=16, io_dtype=abi.MAMBA_BF16,
+             stream=None)
+
+
+def upd(**over):
+    kw = dict(DGOOD)
+    kw.update(over)
+    return abi.raw_state_update(**kw)
+
+
+def test_state_update_validation(lib):
+    for name in ("state", "x", "dt", "A_log", "B", "C", "out"):
+        assert upd(**{name: None}) == 1
+    assert upd(batch=-1) == 2
+    assert upd(dstate=0) == 3 and upd(dstate=300) == 3
+    assert upd(io_dtype=3) == 5
+    assert upd(state=P[0] + 2) == 4
+    assert upd(x=P[1] + 1) == 4
+    assert upd(out=P[0]) == 8
+    assert upd(batch=0) == 0
+
+
+def test_binding_refuses_missing_library(tmp_path):
+    with pytest.raises(RuntimeError, match="missing"):
+        old, abi._lib = abi._lib, None
+        try:
+            abi.load(str(tmp_path / "nope.so"))
+        finally:
+            abi._lib = old

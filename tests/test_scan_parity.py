@@ -1,0 +1,171 @@
+"""GPU forward scan vs the fp64 oracle, element by element, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+from golden_io import load_tiny_f32
+from parity_util import TOL, gpu_scan, normwise, oracle_scan, rel_err, sample_chains, to_device
+from selective_state_space_140_b300 import abi, workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(x, device, **kw):
+    xd = to_device(x, device)
+    y, h = gpu_scan(xd, **kw)
+    torch.cuda.synchronize()
+    return y.float().cpu().numpy(), h.cpu().numpy()
+
+
+def _assert_close(x, yg, hg, yr, hr, tol=None, what=""):
+    tol = TOL[x["io_dtype"]] if tol is None else tol
+    ey, eh = rel_err(yg, yr), rel_err(hg, hr)
+    assert ey <= tol and eh <= tol, (f"{what}: y err {ey:.3e} (normwise {normwise(yg, yr):.2e}), "
+                                     f"state err {eh:.3e}, tol {tol}")
+    return ey, eh
+
+
+def test_tiny_config_matches_oracle_and_stored_fixture(cuda):
+    x = workloads.make_config_inputs(workloads.SCAN_CONFIGS["tiny_f32"])
+    yg, hg = _run(x, cuda)
+    yr, hr = oracle_scan(x)
+    _assert_close(x, yg, hg, yr, hr, what="tiny")
+    yf, hf = load_tiny_f32()
+    _assert_close(x, yg, hg, yf, hf, what="tiny vs fixture")
+
+
+SHAPES = [
+    # batch, dim, L, N, io
+    (1, 1, 1, 16, "bf16"), (1, 5, 2, 16, "f32"), (1, 3, 3, 4, "f32"), (2, 37, 33, 16, "bf16"),
+    (1, 33, 31, 4, "f32"), (2, 9, 63, 1, "f32"), (1, 3, 65, 3, "f32"), (1, 17, 2047, 16, "bf16"),
+    (1, 8, 2049, 16, "f32"), (2, 7, 100, 5, "bf16"), (1, 5, 70, 17, "f32"), (1, 6, 50, 64, "f32"),
+    (1, 4, 40, 100, "f32"), (1, 3, 30, 256, "f32"), (1, 130, 40, 8, "bf16"),
+    (3, 2, 129, 32, "bf16"), (2, 70, 1000, 16, "bf16"), (2, 70, 1000, 16, "f32"),
+    (1, 64, 4096, 16, "bf16"), (2, 40, 777, 64, "f32"),
+]
+
+
+@pytest.mark.parametrize("batch,dim,L,N,io", SHAPES, ids=lambda v: str(v))
+def test_shapes_match_oracle(cuda, batch, dim, L, N, io):
+    x = workloads.make_scan_inputs(batch, dim, L, N, io, seed=batch * 1000 + dim + L + N,
+                                   d_mode="normal")
+    yg, hg = _run(x, cuda)
+    yr, hr = oracle_scan(x)
+    _assert_close(x, yg, hg, yr, hr, what=f"{(batch, dim, L, N, io)}")
+
+
+@pytest.mark.parametrize("with_z,with_D,with_bias", [(False, True, True), (True, False, True),
+                                                      (True, True, False), (False, False, False)])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_optional_inputs(cuda, with_z, with_D, with_bias, io):
+    x = workloads.make_scan_inputs(2, 21, 150, 16, io, seed=7, d_mode="normal", with_z=with_z,
+                                   with_D=with_D, with_bias=with_bias)
+    yg, hg = _run(x, cuda)
+    yr, hr = oracle_scan(x)
+    _assert_close(x, yg, hg, yr, hr, what=f"z={with_z} D={with_D} bias={with_bias}")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_softplus_off_uses_delta_as_given(cuda, io):
+    x = workloads.make_scan_inputs(1, 12, 200, 16, io, seed=8, d_mode="normal", with_bias=False)
+    x["delta"] = (x["delta"].float().abs() * 0.05).to(x["delta"].dtype)
+    x["softplus"] = False
+    yg, hg = _run(x, cuda)
+    yr, hr = oracle_scan(x)
+    _assert_close(x, yg, hg, yr, hr, what="softplus off")
+
+
+def test_large_steps_take_the_upper_softplus_branch(cuda):
+    x = workloads.make_scan_inputs(1, 8, 64, 16, "f32", seed=9, d_mode="normal")
+    x["delta_bias"] = torch.linspace(-3.0, 25.0, 8)
+    yg, hg = _run(x, cuda)
+    yr, hr = oracle_scan(x)
+    _assert_close(x, yg, hg, yr, hr, what="large dt")
+
+
+def test_zero_steps_leave_the_state_zero(cuda):
+    """dt = 0 limit: out = D*u*SiLU(z) and the final state is exactly zero."""
+    x = workloads.make_scan_inputs(2, 10, 77, 16, "f32", seed=10, d_mode="normal",
+                                   with_bias=False)
+    x["delta"] = torch.zeros_like(x["delta"])
+    x["softplus"] = False
+    yg, hg = _run(x, cuda)
+    assert np.all(hg == 0.0)
+    yr, hr = oracle_scan(x)
+    _assert_close(x, yg, hg, yr, hr, what="dt=0")
+
+
+def test_empty_sequence_zeroes_the_state(cuda):
+    x = workloads.make_scan_inputs(2, 5, 0, 16, "bf16", seed=11)
+    xd = to_device(x, cuda)
+    h = torch.full((2, 5, 16), float("nan"), device=cuda)
+    y, h = gpu_scan(xd, last_state=h)
+    torch.cuda.synchronize()
+    assert y.numel() == 0 and torch.all(h == 0)
+
+
+def test_results_are_deterministic(cuda):
+    x = workloads.make_scan_inputs(2, 64, 513, 16, "bf16", seed=12)
+    y1, h1 = _run(x, cuda)
+    y2, h2 = _run(x, cuda)
+    assert np.array_equal(y1, y2) and np.array_equal(h1, h2)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_element_aligned_buffers_give_the_same_result(cuda, io):
+    """Inputs that start one element past a 16-byte boundary take the scalar
+    path and must give bitwise the same answer as aligned ones."""
+    x = workloads.make_scan_inputs(2, 24, 96, 16, io, seed=13)
+    xd = to_device(x, cuda)
+    y0, h0 = gpu_scan(xd)
+    shifted = {}
+    for k in ("u", "delta", "z", "B", "C"):
+        t = xd[k]
+        buf = torch.empty(t.numel() + 1, dtype=t.dtype, device=cuda)
+        v = buf[1:].view(t.shape)
+        v.copy_(t)
+        shifted[k] = v
+    xs = dict(xd, **shifted)
+    ybuf = torch.empty(y0.numel() + 1, dtype=y0.dtype, device=cuda)
+    y1, h1 = gpu_scan(xs, y=ybuf[1:].view(y0.shape))
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1) and torch.equal(h0, h1)
+
+
+def test_runs_on_a_side_stream(cuda):
+    x = workloads.make_scan_inputs(1, 32, 300, 16, "bf16", seed=14)
+    xd = to_device(x, cuda)
+    y0, h0 = gpu_scan(xd)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        y1, h1 = gpu_scan(xd)
+    s.synchronize()
+    assert torch.equal(y0, y1) and torch.equal(h0, h1)
+
+
+def test_reports_alias_error(cuda):
+    x = to_device(workloads.make_scan_inputs(1, 4, 16, 4, "f32", seed=15), cuda)
+    with pytest.raises(abi.MambaError, match="ALIAS"):
+        gpu_scan(x, y=x["u"])
+
+
+@pytest.mark.parametrize("name", ["mamba130m_bf16", "mamba1p4b_bf16", "dna_long_bf16",
+                                  "large_state_f32"])
+def test_full_size_configs_on_sampled_chains(cuda, name):
+    """Full-size launch as the benchmark runs it; the oracle recomputes a
+    sample of whole chains (first, last and random ones), compared element by
+    element along the full sequence, plus the final states of those chains."""
+    cfg = workloads.SCAN_CONFIGS[name]
+    x = workloads.make_config_inputs(cfg)
+    xd = to_device(x, cuda)
+    y, h = gpu_scan(xd)
+    torch.cuda.synchronize()
+    chains = sample_chains(cfg.batch, cfg.dim, 6 if cfg.seqlen > 10000 else 10, seed=cfg.seed)
+    bi = torch.tensor([c[0] for c in chains])
+    di = torch.tensor([c[1] for c in chains])
+    yg = y[bi, di].float().cpu().numpy()
+    hg = h[bi, di].cpu().numpy()
+    assert torch.isfinite(y).all() and torch.isfinite(h).all()
+    yr, hr = oracle_scan(x, chains)
+    _assert_close(x, yg, hg, yr, hr, what=name)
