@@ -1,4 +1,4 @@
-// Fused selective-scan forward kernel for sm_103a.
+// Fused selective-scan forward kernels for sm_103a.
 //
 // One launch does every step of the scan: dt = softplus(delta + bias),
 // Abar = exp(dt*A) with A = -exp(A_log), Bbar u = dt*B*u, the recurrence
@@ -18,17 +18,33 @@
 // of B and C in shared memory serves all of them.
 //
 // The sequence is processed in chunks of T steps; per chunk:
-//   A. B and C of the chunk have been brought into shared memory by a bulk
-//      copy (TMA, cp.async.bulk) issued two chunks ahead; bf16 values are
-//      widened once to fp32.  Each thread turns its 128-bit register-prefetched
-//      slice of delta and u into (dt, dt*u) for all states and issues the
-//      128-bit loads of the next chunk's delta, u, z.
+//   A. B and C of the chunk are in shared memory (bulk copies issued ahead of
+//      time) and are widened once to fp32.  Per element, dt = softplus(delta +
+//      bias) and dt*u are computed once, two elements per packed f32x2
+//      instruction, and left in shared memory for the state threads.
 //   B. The recurrence, two states per packed f32x2 instruction: per step and
 //      state one ex2 on the SFU, a multiply for dt*A, a multiply for dt*u*B,
-//      an fma for h and an fma for the C contraction.  Each thread leaves one
-//      partial sum of C.h per step in shared memory.
+//      an fma for h and an fma for the C contraction.  The operands and the
+//      exponentials of step t+1 are issued before the state update of step t,
+//      so the SFU and shared-memory latencies overlap the fma chain.  Each
+//      thread leaves one partial sum of C.h per step in shared memory.
 //   C. Per (chain, step): sum the G partials, add D*u, gate with SiLU(z),
-//      round and store y with 128-bit stores.
+//      round and store y.
+//
+// Two kernels share phases A to C and differ in how u, delta and z arrive:
+//   scan_tma_kernel  -- 2-D tensor-map bulk copies (cp.async.bulk.tensor) of
+//                       [CH chains x T steps] tiles into a ring of S stages,
+//                       issued S-1 chunks ahead, so that enough bytes are in
+//                       flight per SM to stream from HBM; out-of-range rows
+//                       and the ragged time tail are zero-filled by the copy.
+//                       Used whenever the rows are 16-byte aligned.
+//   scan_reg_kernel  -- 128-bit (or element-wise) loads prefetched into
+//                       registers one chunk ahead; the fallback for rows that
+//                       are not 16-byte aligned.
+#include <cuda.h>
+#include <stdlib.h>
+
+#include <mutex>
 #include <type_traits>
 
 #include "common.cuh"
@@ -40,61 +56,778 @@ __device__ unsigned int g_scan_error;
 
 namespace {
 
-template <typename io_t, int NPL_, int G_, int CH_, int T_>
-struct Cfg {
-    using io = io_t;
-    static constexpr int NPL = NPL_, G = G_, CH = CH_, T = T_;
-    static constexpr int NTH = CH * G;
-    static constexpr int NP = NPL * G;          // padded states per chain
-    static constexpr int VEC = Io<io_t>::kVec;  // io elements per 16 bytes
-    static constexpr int SEGROW = T / VEC;      // 16-byte segments per chain per chunk
-    static constexpr int NSEG = CH * SEGROW;
-    static constexpr int SPT = (NSEG + NTH - 1) / NTH;
-    static constexpr int ES = sizeof(io_t);
-    static constexpr int NQ = NPL / 4;          // quads of states per thread
-    static_assert(NPL % 4 == 0 && T % VEC == 0 && T % 4 == 0, "tile shape");
-    static_assert((T / 4 & (T / 4 - 1)) == 0, "T/4 must be a power of two");
-    // shared memory layout (bytes)
-    static constexpr size_t kBar = 0;                                   // 2 mbarriers
-    static constexpr size_t kStage = 128;                               // 2 x (B, C) raw
-    static constexpr size_t kStageBytes = size_t(T) * NP * ES;         // one array, one chunk
-    static constexpr size_t kBf = kStage + 4 * kStageBytes;             // fp32 B, C
-    static constexpr size_t kBfBytes = size_t(T) * NP * 4;
-    static constexpr size_t kDu = kBf + 2 * kBfBytes;                   // (dt,dt,du,du)
-    static constexpr size_t kY = kDu + size_t(T) * CH * 16;             // partial sums
-    static constexpr size_t kSmem = kY + size_t(NTH) * T * 4;
-    // DIRECT configurations (fp32 io with dstate == NP) skip the fp32 copy
-    static constexpr size_t kSmemDirect = kDu - 2 * kBfBytes + size_t(T) * CH * 16 +
-                                          size_t(NTH) * T * 4;
-};
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 splat2(float v) { return pack2(v, v); }
+
+// Elements (2q, 2q+1) of a vector of io values packed in 32-bit words, widened
+// to fp32.  fp32: word pair (2q, 2q+1).  bf16: word q holds both elements.
+template <typename io_t, typename V>
+__device__ __forceinline__ f32x2 get_pair(const V& v, int q) {
+    const unsigned* w = reinterpret_cast<const unsigned*>(&v);
+    if constexpr (sizeof(io_t) == 4) {
+        return pack2(__uint_as_float(w[2 * q]), __uint_as_float(w[2 * q + 1]));
+    } else {
+        return pack2(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xffff0000u));
+    }
+}
+
+// softplus on a pair: the bf16 path uses the SFU formulation of
+// softplus_fast, the fp32 path libdevice expf/log1pf.
+template <typename io_t>
+__device__ __forceinline__ f32x2 softplus_pair(f32x2 x) {
+    float x0, x1;
+    unpack2(x, x0, x1);
+    if constexpr (sizeof(io_t) == 4) {
+        return pack2(softplus_accurate(x0), softplus_accurate(x1));
+    } else {
+        const float e0 = ex2_approx(fabsf(x0) * -kLog2e), e1 = ex2_approx(fabsf(x1) * -kLog2e);
+        const f32x2 e = pack2(e0, e1);
+        f32x2 s = fma2(e, splat2(-0.25f), splat2(0.333333343f));
+        s = fma2(e, s, splat2(-0.5f));
+        s = fma2(e, s, splat2(1.f));
+        s = mul2(e, s);
+        float w0, w1;
+        unpack2(add2(e, splat2(1.f)), w0, w1);
+        float s0, s1;
+        unpack2(s, s0, s1);
+        const float l0 = e0 < 0.0078125f ? s0 : lg2_approx(w0) * kLn2;
+        const float l1 = e1 < 0.0078125f ? s1 : lg2_approx(w1) * kLn2;
+        return add2(pack2(fmaxf(x0, 0.f), fmaxf(x1, 0.f)), pack2(l0, l1));
+    }
+}
+
+// y * SiLU(z) on a pair: y * z / (1 + e^-z).
+__device__ __forceinline__ f32x2 gate_pair(f32x2 y, f32x2 z) {
+    float z0, z1;
+    unpack2(mul2(z, splat2(-kLog2e)), z0, z1);
+    float d0, d1;
+    unpack2(add2(pack2(ex2_approx(z0), ex2_approx(z1)), splat2(1.f)), d0, d1);
+    return mul2(mul2(y, z), pack2(rcp_approx(d0), rcp_approx(d1)));
+}
+
+// Pack NQ pairs of fp32 into io values (bf16: round to nearest even).
+template <typename io_t, int NPAIR>
+__device__ __forceinline__ void pack_out(const f32x2 (&val)[NPAIR], unsigned (&w)[NPAIR * sizeof(io_t) / 2]) {
+#pragma unroll
+    for (int q = 0; q < NPAIR; ++q) {
+        float a, b;
+        unpack2(val[q], a, b);
+        if constexpr (sizeof(io_t) == 4) {
+            w[2 * q] = __float_as_uint(a);
+            w[2 * q + 1] = __float_as_uint(b);
+        } else {
+            const __nv_bfloat162 pr = __floats2bfloat162_rn(a, b);
+            w[q] = *reinterpret_cast<const unsigned*>(&pr);
+        }
+    }
+}
+
+// Column of chain `cc` at step t in the (dt, dt*u) buffer: the XOR keeps the
+// per-element writes of phase A and the per-step reads of phase B free of
+// shared-memory bank conflicts.
+template <int CH>
+__device__ __forceinline__ int du_col(int t, int cc) {
+    return cc ^ (((t >> 2) << 1) & (CH - 1));
+}
 
 // Swizzle of the 16-byte chunk index within a row of partial sums, so that
-// both the per-step writes (consecutive rows) and the per-chain reads (rows
-// G apart) of one warp land in distinct banks.
+// the per-step writes (consecutive rows) of phase B land in distinct banks.
 template <int T>
 __device__ __forceinline__ int yswz(int row) {
     return (row ^ (row >> 2)) & (T / 4 - 1);
 }
 
-struct Layout {
-    uint64_t* bar;
-    unsigned char* stage;  // [2][B|C] raw io values, [T][N]
-    float* bf;             // [2 arrays][T][NP] fp32 (or the stage itself when DIRECT)
-    float4* du;            // [T][CH]
-    float* y;              // [NTH][T] swizzled
+// ---- phase B ------------------------------------------------------------
+// The recurrence over one chunk for one thread: NQ quads of states of chain
+// c (state group g).  sdu: (dt, dt, dt*u, dt*u) per [step][column]; sB, sC:
+// fp32 [T][NP]; sy: partial sums [NTH rows][T], 16-byte chunks swizzled.
+template <int NPL, int G, int CH, int T>
+__device__ __forceinline__ void recurrence(const float4* sdu, const float* sB, const float* sC,
+                                           float* sy, f32x2 (&h)[NPL / 2],
+                                           const f32x2 (&A2)[NPL / 2], int c, int g, int tid,
+                                           int tlen) {
+    constexpr int NQ = NPL / 4, NP = NPL * G;
+    const ulonglong2* du2 = reinterpret_cast<const ulonglong2*>(sdu);
+    const ulonglong2* b2 = reinterpret_cast<const ulonglong2*>(sB) + g * NQ;
+    const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(sC) + g * NQ;
+    float4* yrow = reinterpret_cast<float4*>(sy + tid * T);
+    const int sw = yswz<T>(tid);
+    struct Step {
+        ulonglong2 sd;  // (dt, dt), (dt*u, dt*u)
+        f32x2 a[2 * NQ];
+        ulonglong2 bq[NQ], cq[NQ];
+    };
+    auto fetch = [&](int t, Step& st) {
+        st.sd = du2[t * CH + du_col<CH>(t, c)];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            float x0, x1, x2, x3;
+            unpack2(mul2(st.sd.x, A2[2 * q]), x0, x1);
+            unpack2(mul2(st.sd.x, A2[2 * q + 1]), x2, x3);
+            st.a[2 * q] = pack2(ex2_approx(x0), ex2_approx(x1));
+            st.a[2 * q + 1] = pack2(ex2_approx(x2), ex2_approx(x3));
+            st.bq[q] = b2[t * (NP / 4) + q];
+            st.cq[q] = c2[t * (NP / 4) + q];
+        }
+    };
+    auto update = [&](const Step& st) -> float {
+        f32x2 acc = splat2(0.f);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            h[2 * q] = fma2(st.a[2 * q], h[2 * q], mul2(st.sd.y, st.bq[q].x));
+            h[2 * q + 1] = fma2(st.a[2 * q + 1], h[2 * q + 1], mul2(st.sd.y, st.bq[q].y));
+            acc = fma2(st.cq[q].x, h[2 * q], acc);
+            acc = fma2(st.cq[q].y, h[2 * q + 1], acc);
+        }
+        float lo, hi;
+        unpack2(acc, lo, hi);
+        return lo + hi;
+    };
+    Step cur;
+    fetch(0, cur);
+    if (tlen == T) {
+#pragma unroll
+        for (int tt = 0; tt < T; tt += 4) {
+            float part[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                Step nxt;
+                if (tt + j + 1 < T) fetch(tt + j + 1, nxt);
+                part[j] = update(cur);
+                if (tt + j + 1 < T) cur = nxt;
+            }
+            yrow[(tt / 4) ^ sw] = make_float4(part[0], part[1], part[2], part[3]);
+        }
+    } else {
+        for (int tt = 0; tt < tlen; tt += 4) {
+            float part[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int t = tt + j;
+                Step nxt;
+                if (t + 1 < tlen) fetch(t + 1, nxt);
+                part[j] = t < tlen ? update(cur) : 0.f;
+                if (t + 1 < tlen) cur = nxt;
+            }
+            yrow[(tt / 4) ^ sw] = make_float4(part[0], part[1], part[2], part[3]);
+        }
+    }
+}
+
+// Sum of the G partials of chain cc over the 4 steps [4*q4, 4*q4+4) of the
+// chunk, as two pairs.
+template <int G, int T>
+__device__ __forceinline__ void partial_sums(const float* sy, int cc, int q4, f32x2& s01,
+                                             f32x2& s23) {
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) {
+        const int r = cc * G + gg;
+        const ulonglong2 v = reinterpret_cast<const ulonglong2*>(sy + r * T)[q4 ^ yswz<T>(r)];
+        s01 = gg == 0 ? v.x : add2(s01, v.x);
+        s23 = gg == 0 ? v.y : add2(s23, v.y);
+    }
+}
+
+// Widen the chunk's B and C (raw io values [T][N]) into fp32 [T][NP], with
+// zero padding for states N..NP-1.
+template <typename io_t, int NP, int T, int NTH>
+__device__ __forceinline__ void widen_bc(const unsigned char* rawB, const unsigned char* rawC,
+                                         float* sB, float* sC, int N, int tid) {
+    constexpr int ES = sizeof(io_t);
+    if (N == NP && (N * ES) % 16 == 0) {
+        constexpr int PER = 16 / ES;  // io values per 16 bytes
+        const uint4* rb = reinterpret_cast<const uint4*>(rawB);
+        const uint4* rc = reinterpret_cast<const uint4*>(rawC);
+        for (int it = tid; it < T * NP / PER; it += NTH) {
+            const uint4 vb = rb[it], vc = rc[it];
+            ulonglong2* ob = reinterpret_cast<ulonglong2*>(sB + it * PER);
+            ulonglong2* oc = reinterpret_cast<ulonglong2*>(sC + it * PER);
+#pragma unroll
+            for (int q = 0; q < PER / 4; ++q) {
+                ob[q] = make_ulonglong2(get_pair<io_t>(vb, 2 * q), get_pair<io_t>(vb, 2 * q + 1));
+                oc[q] = make_ulonglong2(get_pair<io_t>(vc, 2 * q), get_pair<io_t>(vc, 2 * q + 1));
+            }
+        }
+    } else {
+        const io_t* rb = reinterpret_cast<const io_t*>(rawB);
+        const io_t* rc = reinterpret_cast<const io_t*>(rawC);
+        for (int idx = tid; idx < T * NP; idx += NTH) {
+            const int t = idx / NP, n = idx % NP;
+            const bool ok = n < N;
+            sB[idx] = ok ? float(rb[t * N + n]) : 0.f;
+            sC[idx] = ok ? float(rc[t * N + n]) : 0.f;
+        }
+    }
+}
+
+template <int NPL, int G>
+__device__ __forceinline__ void init_state(const ScanArgs& p, int64_t d, bool chain_ok, int g,
+                                           f32x2 (&A2)[NPL / 2], f32x2 (&h)[NPL / 2]) {
+    // A2 = -exp(A_log) * log2(e), so that Abar = 2^(dt * A2).
+#pragma unroll
+    for (int q = 0; q < NPL / 2; ++q) {
+        float a[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int n = g * NPL + 2 * q + e;
+            a[e] = (chain_ok && n < p.dstate) ? -expf(__ldg(p.A_log + d * p.dstate + n)) * kLog2e
+                                               : 0.f;
+        }
+        A2[q] = pack2(a[0], a[1]);
+        h[q] = splat2(0.f);
+    }
+}
+
+template <int NPL, int G>
+__device__ __forceinline__ void store_state(const ScanArgs& p, int64_t chain, int g,
+                                            const f32x2 (&h)[NPL / 2]) {
+    float* out = p.last_state + chain * p.dstate;
+#pragma unroll
+    for (int q = 0; q < NPL / 2; ++q) {
+        float v[2];
+        unpack2(h[q], v[0], v[1]);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int n = g * NPL + 2 * q + e;
+            if (n < p.dstate) out[n] = v[e];
+        }
+    }
+}
+
+// =========================================================================
+// Tensor-map (TMA) path
+// =========================================================================
+constexpr int kTmaT = 16;      // steps per chunk
+constexpr int kTmaStages = 4;  // ring depth: copies run 3 chunks ahead
+
+template <typename io_t, int NPL, int G, int CH>
+struct TmaCfg {
+    static constexpr int T = kTmaT, S = kTmaStages;
+    static constexpr int NTH = CH * G, NP = NPL * G, ES = sizeof(io_t);
+    static constexpr int PV = 4;                  // elements per thread access
+    static constexpr int SEGROW = T / PV;
+    static constexpr int NSEG = CH * SEGROW;
+    static constexpr int SPT = (NSEG + NTH - 1) / NTH;
+    static constexpr size_t rnd(size_t x) { return (x + 127) / 128 * 128; }
+    static constexpr size_t kTile = rnd(size_t(CH) * T * ES);   // u, delta or z tile
+    static constexpr size_t kRaw = rnd(size_t(T) * NP * ES);    // B or C, raw
+    static constexpr size_t kStage = 3 * kTile + 2 * kRaw;
+    static constexpr size_t kRing = 128;
+    static constexpr size_t kBf = kRing + S * kStage;
+    static constexpr size_t kDu = kBf + 2 * size_t(T) * NP * 4;
+    static constexpr size_t kY = kDu + size_t(T) * CH * 16;
+    static constexpr size_t kSmem = kY + size_t(NTH) * T * 4;
+    using quad_t = std::conditional_t<ES == 2, uint2, uint4>;  // PV io values
 };
 
-// 128-bit (or element-wise, at ragged edges) load of VEC consecutive io values.
-template <typename C, bool VECIO>
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+template <typename io_t, int NPL, int G, int CH>
+__global__ void __launch_bounds__(CH* G)
+    scan_tma_kernel(const ScanArgs p, const __grid_constant__ CUtensorMap tm_u,
+                    const __grid_constant__ CUtensorMap tm_d,
+                    const __grid_constant__ CUtensorMap tm_z, const int dblocks) {
+    using C = TmaCfg<io_t, NPL, G, CH>;
+    constexpr int T = C::T, S = C::S, NTH = C::NTH, NP = C::NP, PV = C::PV;
+    using quad_t = typename C::quad_t;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    float* sB = reinterpret_cast<float*>(smem + C::kBf);
+    float* sC = sB + T * NP;
+    float4* sdu = reinterpret_cast<float4*>(smem + C::kDu);
+    float* sy = reinterpret_cast<float*>(smem + C::kY);
+    auto tile = [&](int s, int which) { return smem + C::kRing + s * C::kStage + which * C::kTile; };
+    auto raw = [&](int s, int which) {
+        return smem + C::kRing + s * C::kStage + 3 * C::kTile + which * C::kRaw;
+    };
+
+    const int64_t L = p.seqlen, dim = p.dim;
+    const int N = p.dstate;
+    const int b = blockIdx.x / dblocks;
+    const int64_t d0 = int64_t(blockIdx.x % dblocks) * CH;
+    const int tid = threadIdx.x;
+    const int c = tid / G, g = tid % G;
+    const int64_t d = d0 + c;
+    const bool chain_ok = d < dim;
+    const int64_t nchunks = (L + T - 1) / T;
+    const int row0 = int(int64_t(b) * dim + d0);
+    const bool has_z = p.z != nullptr;
+    const io_t* Bg = static_cast<const io_t*>(p.B) + int64_t(b) * L * N;
+    const io_t* Cg = static_cast<const io_t*>(p.C) + int64_t(b) * L * N;
+
+    auto issue = [&](int64_t k) {  // one thread
+        const int s = int(k % S);
+        const int tl = L - k * T < T ? int(L - k * T) : T;
+        const uint32_t bc_bytes = uint32_t(tl) * N * C::ES;
+        const uint32_t tile_bytes = uint32_t(CH) * T * C::ES;
+        mbar_arrive_expect_tx(&bar[s], (has_z ? 3 : 2) * tile_bytes + 2 * bc_bytes);
+        tma_load_2d(tile(s, 0), &tm_u, int(k * T), row0, &bar[s]);
+        tma_load_2d(tile(s, 1), &tm_d, int(k * T), row0, &bar[s]);
+        if (has_z) tma_load_2d(tile(s, 2), &tm_z, int(k * T), row0, &bar[s]);
+        bulk_g2s(raw(s, 0), Bg + k * T * N, bc_bytes, &bar[s]);
+        bulk_g2s(raw(s, 1), Cg + k * T * N, bc_bytes, &bar[s]);
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        for (int64_t k = 0; k < S - 1 && k < nchunks; ++k) issue(k);
+    }
+    f32x2 A2[NPL / 2], h[NPL / 2];
+    init_state<NPL, G>(p, d, chain_ok, g, A2, h);
+    __syncthreads();
+
+    io_t* yy = static_cast<io_t*>(p.y);
+    for (int64_t k = 0; k < nchunks; ++k) {
+        const int s = int(k % S);
+        const int64_t t0 = k * T;
+        const int tlen = L - t0 < T ? int(L - t0) : T;
+        if (!mbar_wait(&bar[s], uint32_t(k / S) & 1u)) atomicOr(&g_scan_error, kErrWaitTimeout);
+
+        // ---- phase A ----
+        widen_bc<io_t, NP, T, NTH>(raw(s, 0), raw(s, 1), sB, sC, N, tid);
+#pragma unroll
+        for (int i = 0; i < C::SPT; ++i) {
+            const int sidx = tid + i * NTH;
+            if (sidx >= C::NSEG) break;
+            const int seg = sidx % C::SEGROW, cc = sidx / C::SEGROW;
+            const int64_t dd = d0 + cc;
+            const bool live = dd < dim && seg * PV < tlen;
+            const quad_t vd = reinterpret_cast<const quad_t*>(tile(s, 1))[cc * C::SEGROW + seg];
+            const quad_t vu = reinterpret_cast<const quad_t*>(tile(s, 0))[cc * C::SEGROW + seg];
+            const f32x2 bias2 = splat2((dd < dim && p.delta_bias) ? __ldg(p.delta_bias + dd) : 0.f);
+#pragma unroll
+            for (int q = 0; q < PV / 2; ++q) {
+                f32x2 dt = add2(get_pair<io_t>(vd, q), bias2);
+                if (p.softplus) dt = softplus_pair<io_t>(dt);
+                const f32x2 du = mul2(dt, get_pair<io_t>(vu, q));
+                float dt0, dt1, du0, du1;
+                unpack2(dt, dt0, dt1);
+                unpack2(du, du0, du1);
+                if (!live) dt0 = dt1 = du0 = du1 = 0.f;
+                const int t = seg * PV + 2 * q;
+                sdu[t * CH + du_col<CH>(t, cc)] = make_float4(dt0, dt0, du0, du0);
+                sdu[(t + 1) * CH + du_col<CH>(t + 1, cc)] = make_float4(dt1, dt1, du1, du1);
+            }
+        }
+        __syncthreads();
+        // The stage consumed one chunk ago is free: refill it S-1 chunks ahead.
+        if (tid == 0 && k + S - 1 < nchunks) {
+            fence_proxy_async_smem();
+            issue(k + S - 1);
+        }
+
+        // ---- phase B ----
+        recurrence<NPL, G, CH, T>(sdu, sB, sC, sy, h, A2, c, g, tid, tlen);
+        __syncthreads();
+
+        // ---- phase C ----
+#pragma unroll
+        for (int i = 0; i < C::SPT; ++i) {
+            const int sidx = tid + i * NTH;
+            if (sidx >= C::NSEG) break;
+            const int seg = sidx % C::SEGROW, cc = sidx / C::SEGROW;
+            const int64_t dd = d0 + cc;
+            if (dd >= dim || seg * PV >= tlen) continue;
+            f32x2 v[2];
+            partial_sums<G, T>(sy, cc, seg, v[0], v[1]);
+            const quad_t vu = reinterpret_cast<const quad_t*>(tile(s, 0))[cc * C::SEGROW + seg];
+            const f32x2 D2 = splat2(p.D ? __ldg(p.D + dd) : 0.f);
+            v[0] = fma2(D2, get_pair<io_t>(vu, 0), v[0]);
+            v[1] = fma2(D2, get_pair<io_t>(vu, 1), v[1]);
+            if (has_z) {
+                const quad_t vz = reinterpret_cast<const quad_t*>(tile(s, 2))[cc * C::SEGROW + seg];
+                v[0] = gate_pair(v[0], get_pair<io_t>(vz, 0));
+                v[1] = gate_pair(v[1], get_pair<io_t>(vz, 1));
+            }
+            unsigned w[PV * C::ES / 4];
+            pack_out<io_t, 2>(v, w);
+            *reinterpret_cast<quad_t*>(yy + (int64_t(b) * dim + dd) * L + t0 + seg * PV) =
+                *reinterpret_cast<const quad_t*>(w);
+        }
+    }
+    if (chain_ok && p.last_state) store_state<NPL, G>(p, int64_t(b) * dim + d, g, h);
+}
+
+// =========================================================================
+// Paired-chain tensor-map path (dstate == 4*G exactly)
+// =========================================================================
+// Two observations shape this kernel.
+//  * Shared-memory bandwidth: a 128-bit shared load costs four wavefronts per
+//    warp even when every lane reads the same address, so delivering B and C
+//    to each chain separately costs 8 bytes per state update.  Here each
+//    thread owns 4 states (n = 4g..4g+3) of TWO adjacent chains: one load of
+//    B and C (raw io values, widened in registers) serves both, and (dt,
+//    dt*u) of both chains arrive in one 16-byte load.  dt*A is paired across
+//    the two chains, B*dt*u and the state across the 4 states of one chain.
+//  * Latency: each chain is a serial walk over the whole sequence, so the
+//    time one warp needs per step bounds the kernel when the batch is small.
+//    The operands and exponentials of step t+1 are issued before the update
+//    of step t, and the per-element work of the neighbouring chunks (dt and
+//    dt*u of chunk k+1, the epilogue of chunk k-1) is interleaved with the
+//    recurrence of chunk k, four steps at a time; one CTA barrier per chunk,
+//    (dt, dt*u) and the partial sums are double-buffered.
+template <typename io_t, int G>
+struct PairCfg {
+    static constexpr int N = 4 * G, ES = sizeof(io_t), PV = 4, NPL = 4;
+    // Large B/C stages (fp32, dstate 64 and up) would leave too few CTAs per
+    // SM with double buffers: there the per-element phases run between two
+    // barriers instead of being interleaved with the recurrence.
+    static constexpr bool IL = N * ES < 256;
+    static constexpr int NBUF = IL ? 2 : 1;
+    static constexpr int T = 16;                     // steps per chunk
+    static constexpr int S = N * ES >= 128 || G == 1 ? 4 : 8;  // ring depth (power of two)
+    static constexpr int NGRP = T / 4;          // 4-step groups per chunk
+    static constexpr int NTH = 64;
+    static constexpr int NPAIR = NTH / G;  // chain pairs per CTA
+    static constexpr int CH = 2 * NPAIR;   // chains per CTA
+    static constexpr int SEGROW = T / PV;
+    static constexpr int NSEG = CH * SEGROW;
+    static constexpr int SPT = (NSEG + NTH - 1) / NTH;
+    static constexpr size_t rnd(size_t x) { return (x + 127) / 128 * 128; }
+    static constexpr size_t kTile = rnd(size_t(CH) * T * ES);
+    static constexpr size_t kRaw = rnd(size_t(T) * N * ES);
+    static constexpr size_t kStage = 3 * kTile + 2 * kRaw;
+    static constexpr size_t kRing = 128;
+    static constexpr size_t kSdBuf = size_t(T) * NPAIR * 16;      // [T][NPAIR] float4
+    static constexpr size_t kSd = kRing + S * kStage;
+    static constexpr size_t kYBuf = size_t(CH) * G * T * 4;       // [CH*G rows][T]
+    static constexpr size_t kY = kSd + NBUF * kSdBuf;
+    static constexpr size_t kSmem = kY + NBUF * kYBuf;
+    using quad_t = std::conditional_t<ES == 2, uint2, uint4>;
+    static_assert(CH <= 256, "tensor-map box height");
+    static_assert((S & (S - 1)) == 0, "ring depth must be a power of two");
+};
+
+// Column of chain pair p at step t in the (dt, dt*u) buffer.
+template <int NPAIR>
+__device__ __forceinline__ int pair_col(int t, int p) {
+    return p ^ ((t >> 2) & (NPAIR - 1));
+}
+
+template <typename io_t, int G>
+__global__ void __launch_bounds__(64)
+    scan_pair_kernel(const ScanArgs p, const __grid_constant__ CUtensorMap tm_u,
+                     const __grid_constant__ CUtensorMap tm_d,
+                     const __grid_constant__ CUtensorMap tm_z, const int dblocks) {
+    using C = PairCfg<io_t, G>;
+    constexpr int T = C::T, S = C::S, NTH = C::NTH, NPAIR = C::NPAIR, CH = C::CH, N = C::N;
+    constexpr int PV = C::PV, NGRP = C::NGRP, SPT = C::SPT;
+    using quad_t = typename C::quad_t;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    // chunk indices fit in 32 bits (seqlen < 2^31 on this path)
+    auto stage = [&](int k) { return smem + C::kRing + (k & (S - 1)) * C::kStage; };
+    auto tile = [&](int k, int which) { return stage(k) + which * C::kTile; };
+    auto raw = [&](int k, int which) { return stage(k) + 3 * C::kTile + which * C::kRaw; };
+    auto sdbuf = [&](int k) {
+        return reinterpret_cast<float*>(smem + C::kSd + (k & (C::NBUF - 1)) * C::kSdBuf);
+    };
+    auto ybuf = [&](int k) {
+        return reinterpret_cast<float*>(smem + C::kY + (k & (C::NBUF - 1)) * C::kYBuf);
+    };
+
+    const int L = int(p.seqlen);
+    const int64_t dim = p.dim;
+    const int b = blockIdx.x / dblocks;
+    const int64_t d0 = int64_t(blockIdx.x % dblocks) * CH;
+    const int tid = threadIdx.x;
+    const int pr = tid / G, g = tid % G;  // chain pair, state group
+    const int64_t da = d0 + 2 * pr, db = da + 1;
+    const int nchunks = (L + T - 1) / T;
+    const int row0 = int(int64_t(b) * dim + d0);
+    const bool has_z = p.z != nullptr;
+    const io_t* Bg = static_cast<const io_t*>(p.B) + int64_t(b) * L * N;
+    const io_t* Cg = static_cast<const io_t*>(p.C) + int64_t(b) * L * N;
+    io_t* yy = static_cast<io_t*>(p.y);
+    auto chunk_len = [&](int k) { return L - k * T < T ? L - k * T : T; };
+
+    auto issue = [&](int k) {  // one thread
+        const uint32_t bc_bytes = uint32_t(chunk_len(k)) * N * C::ES;
+        const uint32_t tile_bytes = uint32_t(CH) * T * C::ES;
+        uint64_t* br = &bar[k & (S - 1)];
+        unsigned char* st = stage(k);
+        mbar_arrive_expect_tx(br, (has_z ? 3 : 2) * tile_bytes + 2 * bc_bytes);
+        tma_load_2d(st, &tm_u, k * T, row0, br);
+        tma_load_2d(st + C::kTile, &tm_d, k * T, row0, br);
+        if (has_z) tma_load_2d(st + 2 * C::kTile, &tm_z, k * T, row0, br);
+        bulk_g2s(st + 3 * C::kTile, Bg + int64_t(k) * T * N, bc_bytes, br);
+        bulk_g2s(st + 3 * C::kTile + C::kRaw, Cg + int64_t(k) * T * N, bc_bytes, br);
+    };
+    auto wait_chunk = [&](int k) {
+        if (!mbar_wait(&bar[k & (S - 1)], uint32_t(k / S) & 1u))
+            atomicOr(&g_scan_error, kErrWaitTimeout);
+    };
+
+    // ---- per-element prologue of chunk k, quad item i: (dt, dt*u) ----
+    auto elem_prologue = [&](int k, int i) {
+        const int sidx = tid + i * NTH;
+        if (sidx >= C::NSEG) return;
+        const int seg = sidx % C::SEGROW, cc = sidx / C::SEGROW;
+        const int64_t dd = d0 + cc;
+        const bool live = dd < dim && seg * PV < chunk_len(k);
+        const quad_t vd = reinterpret_cast<const quad_t*>(tile(k, 1))[cc * C::SEGROW + seg];
+        const quad_t vu = reinterpret_cast<const quad_t*>(tile(k, 0))[cc * C::SEGROW + seg];
+        const f32x2 bias2 = splat2((dd < dim && p.delta_bias) ? __ldg(p.delta_bias + dd) : 0.f);
+        float* sdf = sdbuf(k);
+#pragma unroll
+        for (int q = 0; q < PV / 2; ++q) {
+            f32x2 dt = add2(get_pair<io_t>(vd, q), bias2);
+            if (p.softplus) dt = softplus_pair<io_t>(dt);
+            const f32x2 du = mul2(dt, get_pair<io_t>(vu, q));
+            float dt0, dt1, du0, du1;
+            unpack2(dt, dt0, dt1);
+            unpack2(du, du0, du1);
+            if (!live) dt0 = dt1 = du0 = du1 = 0.f;
+            const int t = seg * PV + 2 * q;
+            float* w0 = sdf + (t * NPAIR + pair_col<NPAIR>(t, cc >> 1)) * 4 + (cc & 1);
+            float* w1 = sdf + ((t + 1) * NPAIR + pair_col<NPAIR>(t + 1, cc >> 1)) * 4 + (cc & 1);
+            w0[0] = dt0;
+            w0[2] = du0;
+            w1[0] = dt1;
+            w1[2] = du1;
+        }
+    };
+    // ---- per-element epilogue of chunk k, quad item i: y ----
+    auto elem_epilogue = [&](int k, int i) {
+        const int sidx = tid + i * NTH;
+        if (sidx >= C::NSEG) return;
+        const int seg = sidx % C::SEGROW, cc = sidx / C::SEGROW;
+        const int64_t dd = d0 + cc;
+        if (dd >= dim || seg * PV >= chunk_len(k)) return;
+        f32x2 v[2];
+        partial_sums<G, T>(ybuf(k), cc, seg, v[0], v[1]);
+        const quad_t vu = reinterpret_cast<const quad_t*>(tile(k, 0))[cc * C::SEGROW + seg];
+        const f32x2 D2 = splat2(p.D ? __ldg(p.D + dd) : 0.f);
+        v[0] = fma2(D2, get_pair<io_t>(vu, 0), v[0]);
+        v[1] = fma2(D2, get_pair<io_t>(vu, 1), v[1]);
+        if (has_z) {
+            const quad_t vz = reinterpret_cast<const quad_t*>(tile(k, 2))[cc * C::SEGROW + seg];
+            v[0] = gate_pair(v[0], get_pair<io_t>(vz, 0));
+            v[1] = gate_pair(v[1], get_pair<io_t>(vz, 1));
+        }
+        unsigned w[PV * C::ES / 4];
+        pack_out<io_t, 2>(v, w);
+        *reinterpret_cast<quad_t*>(yy + (int64_t(b) * dim + dd) * L + int64_t(k) * T + seg * PV) =
+            *reinterpret_cast<const quad_t*>(w);
+    };
+    // quad items of this thread handled in 4-step group grp
+    auto items_in_group = [&](int i, int grp) { return i * NGRP / SPT == grp; };
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        // chunks kept in flight ahead of the one computed (see the loop)
+        for (int k = 0; k < (C::IL ? S - 2 : S - 1) && k < nchunks; ++k) issue(k);
+    }
+
+    // A2 pairs across the two chains, per state; states in pairs per chain.
+    f32x2 A2p[4], ha[2], hb[2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int n = 4 * g + j;
+        const float aa = da < dim ? -expf(__ldg(p.A_log + da * N + n)) * kLog2e : 0.f;
+        const float ab = db < dim ? -expf(__ldg(p.A_log + db * N + n)) * kLog2e : 0.f;
+        A2p[j] = pack2(aa, ab);
+    }
+    ha[0] = ha[1] = hb[0] = hb[1] = splat2(0.f);
+    __syncthreads();
+    if (C::IL && nchunks > 0) {
+        wait_chunk(0);
+#pragma unroll
+        for (int i = 0; i < SPT; ++i) elem_prologue(0, i);
+    }
+    __syncthreads();
+
+    const int ra = (2 * pr) * G + g, rb = ra + G;  // partial-sum rows of chains a, b
+    const int swa = yswz<T>(ra), swb = yswz<T>(rb);
+
+    struct Step {
+        ulonglong2 sd;  // (dt_a, dt_b), (du_a, du_b)
+        f32x2 aa01, aa23, ab01, ab23;
+        f32x2 b01, b23, c01, c23;
+    };
+
+    for (int k = 0; k < nchunks; ++k) {
+        // Interleaved: refill the stage of chunk k-3 (its epilogue ran before
+        // the previous barrier) with chunk k+S-3.  Otherwise the per-element
+        // prologue of chunk k runs here, and the stage of chunk k-1 is
+        // refilled with chunk k+S-2 after the barrier that follows.
+        if (C::IL && tid == 0 && k >= 1 && k + S - 3 < nchunks) {
+            fence_proxy_async_smem();
+            issue(k + S - 3);
+        }
+        const bool has_next = C::IL && k + 1 < nchunks, has_prev = C::IL && k >= 1;
+        if (has_next) wait_chunk(k + 1);
+        if (!C::IL) {
+            wait_chunk(k);
+#pragma unroll
+            for (int i = 0; i < SPT; ++i) elem_prologue(k, i);
+            __syncthreads();
+            if (tid == 0 && k >= 1 && k + S - 2 < nchunks) {
+                fence_proxy_async_smem();
+                issue(k + S - 2);
+            }
+        }
+        const int tlen = chunk_len(k);
+        const ulonglong2* sd2 = reinterpret_cast<const ulonglong2*>(sdbuf(k));
+        const quad_t* rB = reinterpret_cast<const quad_t*>(raw(k, 0));
+        const quad_t* rC = reinterpret_cast<const quad_t*>(raw(k, 1));
+        float4* yra = reinterpret_cast<float4*>(ybuf(k) + ra * T);
+        float4* yrb = reinterpret_cast<float4*>(ybuf(k) + rb * T);
+
+        auto fetch = [&](int t, Step& st) {
+            st.sd = sd2[t * NPAIR + pair_col<NPAIR>(t, pr)];
+            float xa[4], xb[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) unpack2(mul2(st.sd.x, A2p[j]), xa[j], xb[j]);
+            st.aa01 = pack2(ex2_approx(xa[0]), ex2_approx(xa[1]));
+            st.aa23 = pack2(ex2_approx(xa[2]), ex2_approx(xa[3]));
+            st.ab01 = pack2(ex2_approx(xb[0]), ex2_approx(xb[1]));
+            st.ab23 = pack2(ex2_approx(xb[2]), ex2_approx(xb[3]));
+            const quad_t bq = rB[t * G + g], cq = rC[t * G + g];
+            st.b01 = get_pair<io_t>(bq, 0);
+            st.b23 = get_pair<io_t>(bq, 1);
+            st.c01 = get_pair<io_t>(cq, 0);
+            st.c23 = get_pair<io_t>(cq, 1);
+        };
+        auto update = [&](const Step& st, float& pa, float& pb) {
+            float dua, dub;
+            unpack2(st.sd.y, dua, dub);
+            const f32x2 DA = splat2(dua), DB = splat2(dub);
+            ha[0] = fma2(st.aa01, ha[0], mul2(DA, st.b01));
+            ha[1] = fma2(st.aa23, ha[1], mul2(DA, st.b23));
+            hb[0] = fma2(st.ab01, hb[0], mul2(DB, st.b01));
+            hb[1] = fma2(st.ab23, hb[1], mul2(DB, st.b23));
+            const f32x2 ya = fma2(st.c23, ha[1], mul2(st.c01, ha[0]));
+            const f32x2 yb = fma2(st.c23, hb[1], mul2(st.c01, hb[0]));
+            float l, h;
+            unpack2(ya, l, h);
+            pa = l + h;
+            unpack2(yb, l, h);
+            pb = l + h;
+        };
+
+        if (tlen == T) {
+            Step cur;
+            fetch(0, cur);
+#pragma unroll
+            for (int grp = 0; grp < NGRP; ++grp) {
+                float pa[4], pb[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int t = 4 * grp + j;
+                    Step nxt;
+                    if (t + 1 < T) fetch(t + 1, nxt);
+                    update(cur, pa[j], pb[j]);
+                    if (t + 1 < T) cur = nxt;
+                }
+                yra[grp ^ swa] = make_float4(pa[0], pa[1], pa[2], pa[3]);
+                yrb[grp ^ swb] = make_float4(pb[0], pb[1], pb[2], pb[3]);
+                if (C::IL) {
+#pragma unroll
+                    for (int i = 0; i < SPT; ++i) {
+                        if (!items_in_group(i, grp)) continue;
+                        if (has_next) elem_prologue(k + 1, i);
+                        if (has_prev) elem_epilogue(k - 1, i);
+                    }
+                }
+            }
+        } else {
+            // ragged last chunk: plain steps, then the neighbours' work
+            for (int tt = 0; tt < tlen; tt += 4) {
+                float pa[4], pb[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int t = tt + j;
+                    pa[j] = pb[j] = 0.f;
+                    if (t < tlen) {
+                        Step st;
+                        fetch(t, st);
+                        update(st, pa[j], pb[j]);
+                    }
+                }
+                yra[(tt / 4) ^ swa] = make_float4(pa[0], pa[1], pa[2], pa[3]);
+                yrb[(tt / 4) ^ swb] = make_float4(pb[0], pb[1], pb[2], pb[3]);
+            }
+#pragma unroll
+            for (int i = 0; i < SPT; ++i) {
+                if (has_next) elem_prologue(k + 1, i);
+                if (has_prev) elem_epilogue(k - 1, i);
+            }
+        }
+        __syncthreads();
+        if (!C::IL) {
+#pragma unroll
+            for (int i = 0; i < SPT; ++i) elem_epilogue(k, i);
+        }
+    }
+    if (C::IL && nchunks > 0) {
+#pragma unroll
+        for (int i = 0; i < SPT; ++i) elem_epilogue(nchunks - 1, i);
+    }
+    if (p.last_state) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int64_t dd = e == 0 ? da : db;
+            if (dd >= dim) continue;
+            float* out = p.last_state + (int64_t(b) * dim + dd) * N + 4 * g;
+            const f32x2* hh = e == 0 ? ha : hb;
+            float v0, v1, v2, v3;
+            unpack2(hh[0], v0, v1);
+            unpack2(hh[1], v2, v3);
+            out[0] = v0;
+            out[1] = v1;
+            out[2] = v2;
+            out[3] = v3;
+        }
+    }
+}
+
+// =========================================================================
+// Register-prefetch path (rows not 16-byte aligned)
+// =========================================================================
+template <typename io_t, int NPL_, int G_, int CH_, int T_>
+struct RegCfg {
+    using io = io_t;
+    static constexpr int NPL = NPL_, G = G_, CH = CH_, T = T_;
+    static constexpr int NTH = CH * G;
+    static constexpr int NP = NPL * G;
+    static constexpr int VEC = Io<io_t>::kVec;  // io elements per 16 bytes
+    static constexpr int SEGROW = T / VEC;
+    static constexpr int NSEG = CH * SEGROW;
+    static constexpr int SPT = (NSEG + NTH - 1) / NTH;
+    static constexpr int ES = sizeof(io_t);
+    static_assert(NPL % 4 == 0 && T % VEC == 0 && T % 4 == 0, "tile shape");
+    static_assert((T / 4 & (T / 4 - 1)) == 0, "T/4 must be a power of two");
+    static constexpr size_t kStageBytes = size_t(T) * NP * ES;
+    static constexpr size_t kStage = 128;
+    static constexpr size_t kBf = kStage + 4 * kStageBytes;
+    static constexpr size_t kBfBytes = size_t(T) * NP * 4;
+    static constexpr size_t kDuBytes = size_t(T) * CH * 16;
+    static constexpr size_t kYBytes = size_t(NTH) * T * 4;
+    static constexpr size_t kSmem = kBf + 2 * kBfBytes + kDuBytes + kYBytes;
+};
+
+// Element-wise load of VEC consecutive io values (zero past L).
+template <typename C>
 __device__ __forceinline__ uint4 load_seg(const typename C::io* row, int64_t t, int64_t L,
                                           bool valid) {
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (!valid) return v;
-    if (VECIO) {
-        if (t + C::VEC <= L) v = __ldg(reinterpret_cast<const uint4*>(row + t));
-        return v;
-    }
     unsigned w[4] = {0u, 0u, 0u, 0u};
+    if (!valid) return make_uint4(0u, 0u, 0u, 0u);
     if constexpr (C::ES == 4) {
         const unsigned* r = reinterpret_cast<const unsigned*>(row);
 #pragma unroll
@@ -109,47 +842,18 @@ __device__ __forceinline__ uint4 load_seg(const typename C::io* row, int64_t t, 
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-template <typename C, bool VECIO>
-__device__ __forceinline__ void store_seg(typename C::io* row, int64_t t, int64_t L,
-                                          const float (&val)[C::VEC]) {
-    if constexpr (C::ES == 4) {
-        if (VECIO && t + 4 <= L) {
-            *reinterpret_cast<float4*>(row + t) = make_float4(val[0], val[1], val[2], val[3]);
-            return;
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if (t + e < L) reinterpret_cast<float*>(row)[t + e] = val[e];
-    } else {
-        unsigned w[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const __nv_bfloat162 p = __floats2bfloat162_rn(val[2 * q], val[2 * q + 1]);
-            w[q] = *reinterpret_cast<const unsigned*>(&p);
-        }
-        if (VECIO && t + 8 <= L) {
-            *reinterpret_cast<uint4*>(row + t) = make_uint4(w[0], w[1], w[2], w[3]);
-            return;
-        }
-        unsigned short* r = reinterpret_cast<unsigned short*>(row);
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            if (t + e < L) r[t + e] = static_cast<unsigned short>(w[e >> 1] >> (16 * (e & 1)));
-    }
-}
-
-template <typename io_t, int NPL, int G, int CH, int T, bool VECIO, bool DIRECT>
+template <typename io_t, int NPL, int G, int CH, int T>
 __global__ void __launch_bounds__(CH* G)
-    scan_fwd_kernel(const ScanArgs p, const int dblocks, const int tma_ok) {
-    using C = Cfg<io_t, NPL, G, CH, T>;
-    constexpr int NTH = C::NTH, NP = C::NP, VEC = C::VEC, NQ = C::NQ;
+    scan_reg_kernel(const ScanArgs p, const int dblocks, const int tma_ok) {
+    using C = RegCfg<io_t, NPL, G, CH, T>;
+    constexpr int NTH = C::NTH, NP = C::NP, VEC = C::VEC;
     extern __shared__ __align__(128) unsigned char smem[];
-    Layout s;
-    s.bar = reinterpret_cast<uint64_t*>(smem + C::kBar);
-    s.stage = smem + C::kStage;
-    s.bf = reinterpret_cast<float*>(smem + C::kBf);
-    s.du = reinterpret_cast<float4*>(smem + (DIRECT ? C::kBf : C::kDu));
-    s.y = reinterpret_cast<float*>(smem + (DIRECT ? C::kBf + size_t(T) * CH * 16 : C::kY));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    unsigned char* stage = smem + C::kStage;
+    float* sB = reinterpret_cast<float*>(smem + C::kBf);
+    float* sC = sB + T * NP;
+    float4* sdu = reinterpret_cast<float4*>(smem + C::kBf + 2 * C::kBfBytes);
+    float* sy = reinterpret_cast<float*>(smem + C::kBf + 2 * C::kBfBytes + C::kDuBytes);
 
     const int64_t L = p.seqlen, dim = p.dim;
     const int N = p.dstate;
@@ -164,20 +868,19 @@ __global__ void __launch_bounds__(CH* G)
     const io_t* Bg = static_cast<const io_t*>(p.B) + int64_t(b) * L * N;
     const io_t* Cg = static_cast<const io_t*>(p.C) + int64_t(b) * L * N;
     const uint32_t stage_bytes = uint32_t(T) * N * C::ES;
-
-    auto stageB = [&](int k) { return s.stage + size_t(2 * (k & 1)) * C::kStageBytes; };
-    auto stageC = [&](int k) { return s.stage + size_t(2 * (k & 1) + 1) * C::kStageBytes; };
+    auto stageB = [&](int64_t k) { return stage + size_t(2 * (k & 1)) * C::kStageBytes; };
+    auto stageC = [&](int64_t k) { return stage + size_t(2 * (k & 1) + 1) * C::kStageBytes; };
     auto chunk_by_tma = [&](int64_t k) { return tma_ok && (k + 1) * T <= L; };
-    auto issue = [&](int64_t k) {  // thread 0 only
+    auto issue = [&](int64_t k) {  // one thread
         const int64_t off = k * T * N;
-        mbar_arrive_expect_tx(&s.bar[k & 1], 2 * stage_bytes);
-        bulk_g2s(stageB(int(k)), Bg + off, stage_bytes, &s.bar[k & 1]);
-        bulk_g2s(stageC(int(k)), Cg + off, stage_bytes, &s.bar[k & 1]);
+        mbar_arrive_expect_tx(&bar[k & 1], 2 * stage_bytes);
+        bulk_g2s(stageB(k), Bg + off, stage_bytes, &bar[k & 1]);
+        bulk_g2s(stageC(k), Cg + off, stage_bytes, &bar[k & 1]);
     };
 
     if (tid == 0) {
-        mbar_init(&s.bar[0], 1);
-        mbar_init(&s.bar[1], 1);
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
         fence_mbar_init();
         fence_proxy_async_smem();
     }
@@ -186,23 +889,10 @@ __global__ void __launch_bounds__(CH* G)
         if (nchunks > 0 && chunk_by_tma(0)) issue(0);
         if (nchunks > 1 && chunk_by_tma(1)) issue(1);
     }
+    f32x2 A2[NPL / 2], h[NPL / 2];
+    init_state<NPL, G>(p, d, chain_ok, g, A2, h);
 
-    // Per-thread constants: A2 = -exp(A_log) * log2(e), so Abar = 2^(dt*A2).
-    f32x2 A2[2 * NQ], h[2 * NQ];
-#pragma unroll
-    for (int q = 0; q < 2 * NQ; ++q) {
-        float a[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int n = g * NPL + 2 * q + e;
-            a[e] = (chain_ok && n < N) ? -expf(__ldg(p.A_log + d * N + n)) * kLog2e : 0.f;
-        }
-        A2[q] = pack2(a[0], a[1]);
-        h[q] = pack2(0.f, 0.f);
-    }
-
-    // Register prefetch of delta, u, z: slice s = tid + i*NTH is chain
-    // s % CH, 16-byte segment s / CH of the chunk.
+    // slice s = tid + i*NTH is chain s % CH, 16-byte segment s / CH
     const io_t* dl = static_cast<const io_t*>(p.delta);
     const io_t* uu = static_cast<const io_t*>(p.u);
     const io_t* zz = static_cast<const io_t*>(p.z);
@@ -218,9 +908,9 @@ __global__ void __launch_bounds__(CH* G)
             const bool ok = sidx < C::NSEG && dd < dim && k < nchunks;
             const int64_t row = (int64_t(b) * dim + (ok ? dd : 0)) * L;
             const int64_t t = k * T + seg * VEC;
-            vd[i] = load_seg<C, VECIO>(dl + row, t, L, ok);
-            vu[i] = load_seg<C, VECIO>(uu + row, t, L, ok);
-            vz[i] = zz ? load_seg<C, VECIO>(zz + row, t, L, ok) : make_uint4(0u, 0u, 0u, 0u);
+            vd[i] = load_seg<C>(dl + row, t, L, ok);
+            vu[i] = load_seg<C>(uu + row, t, L, ok);
+            vz[i] = zz ? load_seg<C>(zz + row, t, L, ok) : make_uint4(0u, 0u, 0u, 0u);
         }
     };
     prefetch(0, cur_d, cur_u, cur_z);
@@ -229,21 +919,11 @@ __global__ void __launch_bounds__(CH* G)
         const int64_t t0 = k * T;
         const int tlen = L - t0 < T ? int(L - t0) : T;
 
-        // ---- phase A: B/C to fp32 shared memory, (dt, dt*u) per element ----
-        float* sB = DIRECT ? reinterpret_cast<float*>(stageB(int(k))) : s.bf;
-        float* sC = DIRECT ? reinterpret_cast<float*>(stageC(int(k))) : s.bf + T * NP;
+        // ---- phase A ----
         if (chunk_by_tma(k)) {
-            if (!mbar_wait(&s.bar[k & 1], uint32_t(k >> 1) & 1u)) atomicOr(&g_scan_error, kErrWaitTimeout);
-            if (!DIRECT) {
-                const io_t* rb = reinterpret_cast<const io_t*>(stageB(int(k)));
-                const io_t* rc = reinterpret_cast<const io_t*>(stageC(int(k)));
-                for (int idx = tid; idx < T * NP; idx += NTH) {
-                    const int t = idx / NP, n = idx % NP;
-                    const bool ok = n < N;
-                    sB[idx] = ok ? float(rb[t * N + n]) : 0.f;
-                    sC[idx] = ok ? float(rc[t * N + n]) : 0.f;
-                }
-            }
+            if (!mbar_wait(&bar[k & 1], uint32_t(k >> 1) & 1u))
+                atomicOr(&g_scan_error, kErrWaitTimeout);
+            widen_bc<io_t, NP, T, NTH>(stageB(k), stageC(k), sB, sC, N, tid);
         } else {
             for (int idx = tid; idx < T * NP; idx += NTH) {
                 const int t = idx / NP, n = idx % NP;
@@ -258,73 +938,35 @@ __global__ void __launch_bounds__(CH* G)
             if (sidx >= C::NSEG) break;
             const int cc = sidx % CH, seg = sidx / CH;
             const int64_t dd = d0 + cc;
-            const float bias = (dd < dim && p.delta_bias) ? __ldg(p.delta_bias + dd) : 0.f;
+            const bool live = dd < dim;
+            const f32x2 bias2 = splat2((live && p.delta_bias) ? __ldg(p.delta_bias + dd) : 0.f);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const int t = seg * VEC + e;
-                float dt = Io<io_t>::get(cur_d[i], e) + bias;
-                if (p.softplus) dt = C::ES == 2 ? softplus_fast(dt) : softplus_accurate(dt);
-                float du = dt * Io<io_t>::get(cur_u[i], e);
-                if (!(dd < dim && t < tlen)) dt = du = 0.f;
-                s.du[t * CH + cc] = make_float4(dt, dt, du, du);
+            for (int q = 0; q < VEC / 2; ++q) {
+                f32x2 dt = add2(get_pair<io_t>(cur_d[i], q), bias2);
+                if (p.softplus) dt = softplus_pair<io_t>(dt);
+                const f32x2 du = mul2(dt, get_pair<io_t>(cur_u[i], q));
+                float dt0, dt1, du0, du1;
+                unpack2(dt, dt0, dt1);
+                unpack2(du, du0, du1);
+                const int t = seg * VEC + 2 * q;
+                if (!(live && t < tlen)) dt0 = du0 = 0.f;
+                if (!(live && t + 1 < tlen)) dt1 = du1 = 0.f;
+                sdu[t * CH + du_col<CH>(t, cc)] = make_float4(dt0, dt0, du0, du0);
+                sdu[(t + 1) * CH + du_col<CH>(t + 1, cc)] = make_float4(dt1, dt1, du1, du1);
             }
         }
         prefetch(k + 1, nxt_d, nxt_u, nxt_z);
         __syncthreads();
 
-        // ---- phase B: the recurrence ----
-        auto run_steps = [&](auto full_tag) {
-            constexpr bool FULL = decltype(full_tag)::value;
-            const ulonglong2* du2 = reinterpret_cast<const ulonglong2*>(s.du);
-            const ulonglong2* b2 = reinterpret_cast<const ulonglong2*>(sB);
-            const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(sC);
-            float4* yrow = reinterpret_cast<float4*>(s.y + tid * T);
-            const int sw = yswz<T>(tid);
-#pragma unroll 2
-            for (int tt = 0; tt < T; tt += 4) {
-                if (!FULL && tt >= tlen) break;
-                float part[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int t = tt + j;
-                    if (FULL || t < tlen) {
-                        const ulonglong2 sd = du2[t * CH + c];  // (dt,dt), (du,du)
-                        f32x2 acc = pack2(0.f, 0.f);
-#pragma unroll
-                        for (int q = 0; q < NQ; ++q) {
-                            const ulonglong2 bq = b2[(t * NP + g * NPL) / 4 + q];
-                            const ulonglong2 cq = c2[(t * NP + g * NPL) / 4 + q];
-                            float x0, x1, x2, x3;
-                            unpack2(mul2(sd.x, A2[2 * q]), x0, x1);
-                            unpack2(mul2(sd.x, A2[2 * q + 1]), x2, x3);
-                            const f32x2 a01 = pack2(ex2_approx(x0), ex2_approx(x1));
-                            const f32x2 a23 = pack2(ex2_approx(x2), ex2_approx(x3));
-                            h[2 * q] = fma2(a01, h[2 * q], mul2(sd.y, bq.x));
-                            h[2 * q + 1] = fma2(a23, h[2 * q + 1], mul2(sd.y, bq.y));
-                            acc = fma2(cq.x, h[2 * q], acc);
-                            acc = fma2(cq.y, h[2 * q + 1], acc);
-                        }
-                        float lo, hi;
-                        unpack2(acc, lo, hi);
-                        part[j] = lo + hi;
-                    } else {
-                        part[j] = 0.f;
-                    }
-                }
-                yrow[(tt / 4) ^ sw] = make_float4(part[0], part[1], part[2], part[3]);
-            }
-        };
-        if (tlen == T)
-            run_steps(std::integral_constant<bool, true>());
-        else
-            run_steps(std::integral_constant<bool, false>());
+        // ---- phase B ----
+        recurrence<NPL, G, CH, T>(sdu, sB, sC, sy, h, A2, c, g, tid, tlen);
         __syncthreads();
         if (tid == 0 && k + 2 < nchunks && chunk_by_tma(k + 2)) {
             fence_proxy_async_smem();
             issue(k + 2);
         }
 
-        // ---- phase C: reduce over state groups, skip, gate, store ----
+        // ---- phase C ----
 #pragma unroll
         for (int i = 0; i < C::SPT; ++i) {
             const int sidx = tid + i * NTH;
@@ -332,31 +974,32 @@ __global__ void __launch_bounds__(CH* G)
             const int cc = sidx % CH, seg = sidx / CH;
             const int64_t dd = d0 + cc;
             if (dd >= dim || seg * VEC >= tlen) continue;
-            float acc[VEC];
+            f32x2 v[VEC / 2];
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+            for (int q4 = 0; q4 < VEC / 4; ++q4)
+                partial_sums<G, T>(sy, cc, seg * (VEC / 4) + q4, v[2 * q4], v[2 * q4 + 1]);
+            const f32x2 D2 = splat2(p.D ? __ldg(p.D + dd) : 0.f);
 #pragma unroll
-            for (int gg = 0; gg < G; ++gg) {
-                const int r = cc * G + gg;
-                const float4* yr = reinterpret_cast<const float4*>(s.y + r * T);
-                const int sw = yswz<T>(r);
-#pragma unroll
-                for (int q = 0; q < VEC / 4; ++q) {
-                    const float4 v = yr[(seg * (VEC / 4) + q) ^ sw];
-                    acc[4 * q] += v.x;
-                    acc[4 * q + 1] += v.y;
-                    acc[4 * q + 2] += v.z;
-                    acc[4 * q + 3] += v.w;
-                }
+            for (int q = 0; q < VEC / 2; ++q) {
+                f32x2 o = fma2(D2, get_pair<io_t>(cur_u[i], q), v[q]);
+                if (zz) o = gate_pair(o, get_pair<io_t>(cur_z[i], q));
+                v[q] = o;
             }
-            const float Dd = p.D ? __ldg(p.D + dd) : 0.f;
+            unsigned w[4];
+            pack_out<io_t, VEC / 2>(v, w);
+            io_t* row = yy + (int64_t(b) * dim + dd) * L;
+            const int64_t t = t0 + seg * VEC;
+            if constexpr (C::ES == 4) {
+                unsigned* r = reinterpret_cast<unsigned*>(row);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                float v = fmaf(Dd, Io<io_t>::get(cur_u[i], e), acc[e]);
-                if (zz) v *= silu_fast(Io<io_t>::get(cur_z[i], e));
-                acc[e] = v;
+                for (int e = 0; e < 4; ++e)
+                    if (t + e < L) r[t + e] = w[e];
+            } else {
+                unsigned short* r = reinterpret_cast<unsigned short*>(row);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (t + e < L) r[t + e] = static_cast<unsigned short>(w[e >> 1] >> (16 * (e & 1)));
             }
-            store_seg<C, VECIO>(yy + (int64_t(b) * dim + dd) * L, t0 + seg * VEC, L, acc);
         }
 #pragma unroll
         for (int i = 0; i < C::SPT; ++i) {
@@ -365,63 +1008,173 @@ __global__ void __launch_bounds__(CH* G)
             cur_z[i] = nxt_z[i];
         }
     }
+    if (chain_ok && p.last_state) store_state<NPL, G>(p, int64_t(b) * dim + d, g, h);
+}
 
-    if (chain_ok && p.last_state) {
-        float* out = p.last_state + (int64_t(b) * dim + d) * N;
-#pragma unroll
-        for (int q = 0; q < 2 * NQ; ++q) {
-            float v[2];
-            unpack2(h[q], v[0], v[1]);
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int n = g * NPL + 2 * q + e;
-                if (n < N) out[n] = v[e];
-            }
-        }
-    }
+// =========================================================================
+// host side
+// =========================================================================
+int env_int(const char* name) {
+    const char* v = getenv(name);
+    return v ? atoi(v) : 0;
+}
+
+bool al16(const void* q) { return q == nullptr || (reinterpret_cast<uintptr_t>(q) & 15) == 0; }
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+    static EncodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(f);
+    });
+    return fn;
+}
+
+// Tensor map of a [rows][L] io array, box = [T steps] x [CH rows].
+bool make_map(CUtensorMap* m, const void* base, bool bf16, int64_t rows, int64_t L, int T, int CH) {
+    EncodeTiled enc = encode_fn();
+    if (!enc) return false;
+    const size_t es = bf16 ? 2 : 4;
+    const cuuint64_t dims[2] = {cuuint64_t(L), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(L) * es};
+    const cuuint32_t box[2] = {cuuint32_t(T), cuuint32_t(CH)};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+               const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename K, typename... Args>
+cudaError_t launch(K kern, size_t smem, int64_t blocks, int threads, cudaStream_t stream,
+                   Args... args) {
+    cudaError_t err =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (err != cudaSuccess) return err;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    kern<<<unsigned(blocks), threads, smem, stream>>>(args...);
+    return cudaGetLastError();
+}
+
+template <typename io_t, int NPL, int G, int CH>
+bool try_tma(const ScanArgs& a, cudaStream_t stream, cudaError_t* err) {
+    using C = TmaCfg<io_t, NPL, G, CH>;
+    const int64_t es = sizeof(io_t);
+    const bool ok = al16(a.u) && al16(a.delta) && al16(a.z) && al16(a.B) && al16(a.C) &&
+                    (reinterpret_cast<uintptr_t>(a.y) % (C::PV * es)) == 0 &&
+                    (a.seqlen * es) % 16 == 0 && a.batch * a.dim <= 0x7fffffff &&
+                    a.seqlen <= 0x7fffffff;
+    if (!ok) return false;
+    CUtensorMap mu, md, mz;
+    const bool bf = sizeof(io_t) == 2;
+    const int64_t rows = a.batch * a.dim;
+    if (!make_map(&mu, a.u, bf, rows, a.seqlen, C::T, CH) ||
+        !make_map(&md, a.delta, bf, rows, a.seqlen, C::T, CH))
+        return false;
+    if (!make_map(&mz, a.z ? a.z : a.u, bf, rows, a.seqlen, C::T, CH)) return false;
+    const int64_t dblocks = (a.dim + CH - 1) / CH;
+    *err = launch(scan_tma_kernel<io_t, NPL, G, CH>, C::kSmem, dblocks * a.batch, C::NTH, stream,
+                  a, mu, md, mz, int(dblocks));
+    return true;
 }
 
 template <typename io_t, int NPL, int G, int CH, int T>
-cudaError_t launch_cfg(const ScanArgs& a, cudaStream_t stream) {
-    using C = Cfg<io_t, NPL, G, CH, T>;
-    const size_t es = sizeof(io_t);
-    auto al16 = [](const void* q) { return q == nullptr || (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
-    const bool vecio = al16(a.u) && al16(a.delta) && al16(a.z) && al16(a.y) &&
-                       (a.seqlen * int64_t(es)) % 16 == 0;
-    const bool direct = es == 4 && a.dstate == C::NP;
-    const int tma_ok = al16(a.B) && al16(a.C) && (a.seqlen * a.dstate * int64_t(es)) % 16 == 0 &&
-                       (int64_t(T) * a.dstate * int64_t(es)) % 16 == 0;
+cudaError_t launch_reg(const ScanArgs& a, cudaStream_t stream) {
+    using C = RegCfg<io_t, NPL, G, CH, T>;
+    const int64_t es = sizeof(io_t);
+    const int tma_ok = al16(a.B) && al16(a.C) && (a.seqlen * a.dstate * es) % 16 == 0 &&
+                       (int64_t(T) * a.dstate * es) % 16 == 0;
     const int64_t dblocks = (a.dim + CH - 1) / CH;
-    const int64_t blocks = dblocks * a.batch;
-    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    return launch(scan_reg_kernel<io_t, NPL, G, CH, T>, C::kSmem, dblocks * a.batch, C::NTH,
+                  stream, a, int(dblocks), tma_ok);
+}
 
-    auto go = [&](auto kern, size_t smem) -> cudaError_t {
-        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               int(smem));
-        if (err != cudaSuccess) return err;
-        kern<<<unsigned(blocks), C::NTH, smem, stream>>>(a, int(dblocks), tma_ok);
-        return cudaGetLastError();
-    };
-    if constexpr (sizeof(io_t) == 4) {
-        if (direct) {
-            if (vecio) return go(scan_fwd_kernel<io_t, NPL, G, CH, T, true, true>, C::kSmemDirect);
-            return go(scan_fwd_kernel<io_t, NPL, G, CH, T, false, true>, C::kSmemDirect);
-        }
+template <typename io_t, int G>
+bool try_pair(const ScanArgs& a, cudaStream_t stream, cudaError_t* err) {
+    using C = PairCfg<io_t, G>;
+    const int64_t es = sizeof(io_t);
+    const bool ok = a.dstate == C::N && al16(a.u) && al16(a.delta) && al16(a.z) && al16(a.B) &&
+                    al16(a.C) && (reinterpret_cast<uintptr_t>(a.y) % (C::PV * es)) == 0 &&
+                    (a.seqlen * es) % 16 == 0 && a.batch * a.dim <= 0x7fffffff &&
+                    a.seqlen <= 0x7fffffff;
+    if (!ok) return false;
+    CUtensorMap mu, md, mz;
+    const bool bf = sizeof(io_t) == 2;
+    const int64_t rows = a.batch * a.dim;
+    if (!make_map(&mu, a.u, bf, rows, a.seqlen, C::T, C::CH) ||
+        !make_map(&md, a.delta, bf, rows, a.seqlen, C::T, C::CH) ||
+        !make_map(&mz, a.z ? a.z : a.u, bf, rows, a.seqlen, C::T, C::CH))
+        return false;
+    const int64_t dblocks = (a.dim + C::CH - 1) / C::CH;
+    *err = launch(scan_pair_kernel<io_t, G>, C::kSmem, dblocks * a.batch, C::NTH, stream, a, mu,
+                  md, mz, int(dblocks));
+    return true;
+}
+
+// Kernel and tile choice.  Rows that are 16-byte aligned use tensor-map
+// kernels: dstate == 16 the single-chain tile with 8 states x 2 threads per
+// chain (fastest there; 4 x 4 when there are fewer chains than about 64 per
+// SM), dstate in {4, 8, 32, 64, 128} the paired-chain tile,
+// other dstate the single-chain tile sized for it.  Unaligned rows use the
+// register-prefetch kernel.  MAMBA_SCAN_TILE overrides the choice (1: single
+// chain 8x2, 2: single chain 4 states x 4 threads, 3: paired chains) and
+// MAMBA_SCAN_PATH=reg forces the register-prefetch kernel; every choice
+// computes the same recurrence, and the tests check them against each other.
+bool force_reg() {
+    const char* v = getenv("MAMBA_SCAN_PATH");
+    return v && v[0] == 'r';
+}
+
+template <typename io_t>
+bool try_pair_n(const ScanArgs& a, cudaStream_t stream, cudaError_t* err) {
+    switch (a.dstate) {
+        case 4: return try_pair<io_t, 1>(a, stream, err);
+        case 8: return try_pair<io_t, 2>(a, stream, err);
+        case 16: return try_pair<io_t, 4>(a, stream, err);
+        case 32: return try_pair<io_t, 8>(a, stream, err);
+        case 64: return try_pair<io_t, 16>(a, stream, err);
+        case 128: return try_pair<io_t, 32>(a, stream, err);
+        default: return false;
     }
-    if (vecio) return go(scan_fwd_kernel<io_t, NPL, G, CH, T, true, false>, C::kSmem);
-    return go(scan_fwd_kernel<io_t, NPL, G, CH, T, false, false>, C::kSmem);
+}
+
+template <typename io_t, int NPL, int G, int CH, int TREG>
+cudaError_t run(const ScanArgs& a, cudaStream_t stream, bool pair_first) {
+    cudaError_t err = cudaSuccess;
+    if (!force_reg()) {
+        if (pair_first && try_pair_n<io_t>(a, stream, &err)) return err;
+        if (try_tma<io_t, NPL, G, CH>(a, stream, &err)) return err;
+    }
+    return launch_reg<io_t, NPL, G, CH, TREG>(a, stream);
 }
 
 template <typename io_t>
 cudaError_t dispatch(const ScanArgs& a, cudaStream_t stream) {
     const int N = a.dstate;
-    if (N <= 4) return launch_cfg<io_t, 4, 1, 64, 8>(a, stream);
-    if (N <= 8) return launch_cfg<io_t, 4, 2, 32, 16>(a, stream);
-    if (N <= 16) return launch_cfg<io_t, 4, 4, 16, 32>(a, stream);
-    if (N <= 32) return launch_cfg<io_t, 4, 8, 8, 32>(a, stream);
-    if (N <= 64) return launch_cfg<io_t, 4, 16, 4, 16>(a, stream);
-    if (N <= 128) return launch_cfg<io_t, 4, 32, 2, 16>(a, stream);
-    return launch_cfg<io_t, 8, 32, 2, 8>(a, stream);
+    const int tile = env_int("MAMBA_SCAN_TILE");
+    const bool pair = tile == 3 || (tile == 0 && N != 16);
+    if (N <= 4) return run<io_t, 4, 1, 64, 8>(a, stream, pair);
+    if (N <= 8) return run<io_t, 4, 2, 32, 16>(a, stream, pair);
+    if (N <= 16) {
+        // Few chains (long sequences, small batch): more threads per chain.
+        const bool few = a.batch * a.dim < 148 * 64;
+        if (tile == 2 || (tile == 0 && few)) return run<io_t, 4, 4, 16, 32>(a, stream, false);
+        return run<io_t, 8, 2, 32, 16>(a, stream, pair);
+    }
+    if (N <= 32) return run<io_t, 4, 8, 8, 32>(a, stream, pair);
+    if (N <= 64) return run<io_t, 4, 16, 4, 16>(a, stream, pair);
+    if (N <= 128) return run<io_t, 4, 32, 2, 16>(a, stream, pair);
+    return run<io_t, 8, 32, 2, 8>(a, stream, pair);
 }
 
 }  // namespace

@@ -169,3 +169,37 @@ def test_full_size_configs_on_sampled_chains(cuda, name):
     assert torch.isfinite(y).all() and torch.isfinite(h).all()
     yr, hr = oracle_scan(x, chains)
     _assert_close(x, yg, hg, yr, hr, what=name)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("L,dim", [(336, 50), (4096, 33), (333, 50)])
+def test_all_tile_shapes_give_the_same_scan(cuda, io, L, dim, monkeypatch):
+    """dstate = 16 has three tile shapes: one chain x 8 states per thread
+    (default), one chain x 4 states, two chains x 4 states.  Each must match
+    the oracle and the others (odd channel counts leave half-used pairs)."""
+    x = workloads.make_scan_inputs(2, dim, L, 16, io, seed=16, d_mode="normal")
+    yr, hr = oracle_scan(x)
+    outs = []
+    for tile in ("0", "1", "2", "3"):
+        monkeypatch.setenv("MAMBA_SCAN_TILE", tile)
+        y, h = _run(x, cuda)
+        _assert_close(x, y, h, yr, hr, what=f"tile {tile}")
+        outs.append((y, h))
+    tol = TOL[io]
+    for y, h in outs[1:]:
+        assert rel_err(y, outs[0][0]) <= tol and rel_err(h, outs[0][1]) <= tol
+
+
+@pytest.mark.parametrize("io,N", [("bf16", 16), ("f32", 16), ("f32", 64), ("bf16", 4), ("f32", 200),
+                                  ("bf16", 8), ("f32", 32), ("bf16", 128)])
+def test_register_path_matches_tensor_map_path(cuda, io, N, monkeypatch):
+    """Rows that are 16-byte aligned go through the tensor-map (TMA) kernel;
+    the register-prefetch kernel is the fallback.  Forcing the fallback on the
+    same aligned inputs must give the same scan (ragged tail included)."""
+    x = workloads.make_scan_inputs(2, 37, 1000, N, io, seed=17, d_mode="normal")
+    y0, h0 = _run(x, cuda)
+    monkeypatch.setenv("MAMBA_SCAN_PATH", "reg")
+    y1, h1 = _run(x, cuda)
+    yr, hr = oracle_scan(x)
+    _assert_close(x, y0, h0, yr, hr, what="tma path")
+    _assert_close(x, y1, h1, yr, hr, what="register path")
