@@ -291,13 +291,14 @@ def _oracle_sample(cfg, x, nb: int, k: int):
 
 
 def choose_sample(cfg, x, seconds: float):
-    """Calibrate the oracle on a few chains and pick the largest prefix of the
-    workload (whole batches, else channels of batch 0) that fits `seconds`."""
+    """Calibrate the oracle on one batch's worth of chains (or fewer) and pick
+    the largest prefix of the workload (whole batches, else channels of batch
+    0) that fits `seconds`."""
     import oracle
 
     lib = oracle.load()
     cores = oracle.hw_threads(lib)
-    k0 = max(1, min(cfg.dim, cores))
+    k0 = max(1, min(cfg.dim, 8 * cores))
     a, kw, chains, _ = _oracle_sample(cfg, x, 0, k0)
     t0 = time.perf_counter()
     oracle.selective_scan(*a, nthreads=0, lib=lib, **kw)
