@@ -462,6 +462,204 @@ __global__ void __launch_bounds__(CH* G)
 }
 
 // =========================================================================
+// Warp-specialised tensor-map path
+// =========================================================================
+// Measured per 16-step chunk of the single-chain tile, two thirds of the
+// time went to the per-element work (dt, dt*u before the recurrence; the
+// G-partial sum, skip and gate after it) and to issuing and waiting for the
+// bulk copies, all done by the same warps between barriers while the
+// recurrence waited.  Here the CTA has two roles that overlap:
+//   recurrence warps (CH*G threads) -- the state update of chunk k;
+//   element warps (NE threads)      -- the bulk copies, the per-element
+//                                      prologue of chunk k+1 (and the fp32
+//                                      widening of its B and C) and the
+//                                      epilogue of chunk k-1.
+// Hand-off buffers are double-buffered and signalled with named barriers:
+// "prologue of chunk k ready" (element warps arrive, recurrence warps wait)
+// and "recurrence of chunk k done" (the reverse).
+template <typename io_t, int NPL, int G, int CH, int NE>
+struct WsCfg {
+    static constexpr int T = 16, S = 4;
+    static constexpr int NR = CH * G;  // recurrence threads
+    static constexpr int NTH = NR + NE;
+    static constexpr int NP = NPL * G, ES = sizeof(io_t), PV = 4;
+    static constexpr int SEGROW = T / PV;
+    static constexpr int NSEG = CH * SEGROW;
+    static constexpr int SPT = (NSEG + NE - 1) / NE;
+    static constexpr size_t rnd(size_t x) { return (x + 127) / 128 * 128; }
+    static constexpr size_t kTile = rnd(size_t(CH) * T * ES);
+    static constexpr size_t kRaw = rnd(size_t(T) * NP * ES);
+    static constexpr size_t kStage = 3 * kTile + 2 * kRaw;
+    static constexpr size_t kRing = 128;
+    static constexpr size_t kBcBuf = 2 * size_t(T) * NP * 4;  // fp32 B and C
+    static constexpr size_t kBc = kRing + S * kStage;
+    static constexpr size_t kDuBuf = size_t(T) * CH * 16;
+    static constexpr size_t kDu = kBc + 2 * kBcBuf;
+    static constexpr size_t kYBuf = size_t(NR) * T * 4;
+    static constexpr size_t kY = kDu + 2 * kDuBuf;
+    static constexpr size_t kSmem = kY + 2 * kYBuf;
+    using quad_t = std::conditional_t<ES == 2, uint2, uint4>;
+    static_assert(NR % 32 == 0 && NE % 32 == 0, "roles are whole warps");
+};
+
+__device__ __forceinline__ void named_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_arrive(int id, int count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+constexpr int kBarReady = 1;  // + (chunk & 1): prologue of the chunk written
+constexpr int kBarDone = 3;   // + (chunk & 1): recurrence of the chunk done
+constexpr int kBarElem = 5;   // element warps only
+
+template <typename io_t, int NPL, int G, int CH, int NE>
+__global__ void __launch_bounds__(CH* G + NE, 4)
+    scan_ws_kernel(const ScanArgs p, const __grid_constant__ CUtensorMap tm_u,
+                   const __grid_constant__ CUtensorMap tm_d,
+                   const __grid_constant__ CUtensorMap tm_z, const int dblocks) {
+    using C = WsCfg<io_t, NPL, G, CH, NE>;
+    constexpr int T = C::T, S = C::S, NR = C::NR, NTH = C::NTH, NP = C::NP, PV = C::PV;
+    using quad_t = typename C::quad_t;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    auto stage = [&](int k) { return smem + C::kRing + (k & (S - 1)) * C::kStage; };
+    auto tile = [&](int k, int which) { return stage(k) + which * C::kTile; };
+    auto raw = [&](int k, int which) { return stage(k) + 3 * C::kTile + which * C::kRaw; };
+    auto bcbuf = [&](int k) { return reinterpret_cast<float*>(smem + C::kBc + (k & 1) * C::kBcBuf); };
+    auto dubuf = [&](int k) { return reinterpret_cast<float4*>(smem + C::kDu + (k & 1) * C::kDuBuf); };
+    auto ybuf = [&](int k) { return reinterpret_cast<float*>(smem + C::kY + (k & 1) * C::kYBuf); };
+
+    const int L = int(p.seqlen);
+    const int64_t dim = p.dim;
+    const int N = p.dstate;
+    const int b = blockIdx.x / dblocks;
+    const int64_t d0 = int64_t(blockIdx.x % dblocks) * CH;
+    const int tid = threadIdx.x;
+    const int nchunks = (L + T - 1) / T;
+    const int row0 = int(int64_t(b) * dim + d0);
+    const bool has_z = p.z != nullptr;
+    const io_t* Bg = static_cast<const io_t*>(p.B) + int64_t(b) * L * N;
+    const io_t* Cg = static_cast<const io_t*>(p.C) + int64_t(b) * L * N;
+    auto chunk_len = [&](int k) { return L - k * T < T ? L - k * T : T; };
+
+    auto issue = [&](int k) {  // one element thread
+        const uint32_t bc_bytes = uint32_t(chunk_len(k)) * N * C::ES;
+        const uint32_t tile_bytes = uint32_t(CH) * T * C::ES;
+        uint64_t* br = &bar[k & (S - 1)];
+        unsigned char* st = stage(k);
+        mbar_arrive_expect_tx(br, (has_z ? 3 : 2) * tile_bytes + 2 * bc_bytes);
+        tma_load_2d(st, &tm_u, k * T, row0, br);
+        tma_load_2d(st + C::kTile, &tm_d, k * T, row0, br);
+        if (has_z) tma_load_2d(st + 2 * C::kTile, &tm_z, k * T, row0, br);
+        bulk_g2s(st + 3 * C::kTile, Bg + int64_t(k) * T * N, bc_bytes, br);
+        bulk_g2s(st + 3 * C::kTile + C::kRaw, Cg + int64_t(k) * T * N, bc_bytes, br);
+    };
+
+    if (tid == NR) {
+        for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        for (int k = 0; k < S && k < nchunks; ++k) issue(k);
+    }
+    __syncthreads();
+
+    if (tid < NR) {
+        // ---------------- recurrence warps ----------------
+        const int c = tid / G, g = tid % G;
+        const int64_t d = d0 + c;
+        f32x2 A2[NPL / 2], h[NPL / 2];
+        init_state<NPL, G>(p, d, d < dim, g, A2, h);
+        for (int k = 0; k < nchunks; ++k) {
+            named_sync(kBarReady + (k & 1), NTH);
+            const float* sB = bcbuf(k);
+            recurrence<NPL, G, CH, T>(dubuf(k), sB, sB + T * NP, ybuf(k), h, A2, c, g, tid,
+                                      chunk_len(k));
+            named_arrive(kBarDone + (k & 1), NTH);
+        }
+        if (d < dim && p.last_state) store_state<NPL, G>(p, int64_t(b) * dim + d, g, h);
+        return;
+    }
+
+    // ---------------- element warps ----------------
+    const int te = tid - NR;
+    io_t* yy = static_cast<io_t*>(p.y);
+    for (int j = 0; j <= nchunks; ++j) {
+        if (j < nchunks) {
+            // prologue of chunk j
+            if (!mbar_wait(&bar[j & (S - 1)], uint32_t(j / S) & 1u))
+                atomicOr(&g_scan_error, kErrWaitTimeout);
+            float* sB = bcbuf(j);
+            widen_bc<io_t, NP, T, NE>(raw(j, 0), raw(j, 1), sB, sB + T * NP, N, te);
+            const int tlen = chunk_len(j);
+            float4* sdu = dubuf(j);
+#pragma unroll
+            for (int i = 0; i < C::SPT; ++i) {
+                const int sidx = te + i * NE;
+                if (sidx >= C::NSEG) break;
+                const int seg = sidx % C::SEGROW, cc = sidx / C::SEGROW;
+                const int64_t dd = d0 + cc;
+                const bool live = dd < dim && seg * PV < tlen;
+                const quad_t vd = reinterpret_cast<const quad_t*>(tile(j, 1))[cc * C::SEGROW + seg];
+                const quad_t vu = reinterpret_cast<const quad_t*>(tile(j, 0))[cc * C::SEGROW + seg];
+                const f32x2 bias2 =
+                    splat2((dd < dim && p.delta_bias) ? __ldg(p.delta_bias + dd) : 0.f);
+#pragma unroll
+                for (int q = 0; q < PV / 2; ++q) {
+                    f32x2 dt = add2(get_pair<io_t>(vd, q), bias2);
+                    if (p.softplus) dt = softplus_pair<io_t>(dt);
+                    const f32x2 du = mul2(dt, get_pair<io_t>(vu, q));
+                    float dt0, dt1, du0, du1;
+                    unpack2(dt, dt0, dt1);
+                    unpack2(du, du0, du1);
+                    if (!live) dt0 = dt1 = du0 = du1 = 0.f;
+                    const int t = seg * PV + 2 * q;
+                    sdu[t * CH + du_col<CH>(t, cc)] = make_float4(dt0, dt0, du0, du0);
+                    sdu[(t + 1) * CH + du_col<CH>(t + 1, cc)] = make_float4(dt1, dt1, du1, du1);
+                }
+            }
+            named_arrive(kBarReady + (j & 1), NTH);
+        }
+        if (j >= 1) {
+            // epilogue of chunk k = j-1
+            const int k = j - 1;
+            named_sync(kBarDone + (k & 1), NTH);
+            const int tlen = chunk_len(k);
+            const float* sy = ybuf(k);
+#pragma unroll
+            for (int i = 0; i < C::SPT; ++i) {
+                const int sidx = te + i * NE;
+                if (sidx >= C::NSEG) break;
+                const int seg = sidx % C::SEGROW, cc = sidx / C::SEGROW;
+                const int64_t dd = d0 + cc;
+                if (dd >= dim || seg * PV >= tlen) continue;
+                f32x2 v[2];
+                partial_sums<G, T>(sy, cc, seg, v[0], v[1]);
+                const quad_t vu = reinterpret_cast<const quad_t*>(tile(k, 0))[cc * C::SEGROW + seg];
+                const f32x2 D2 = splat2(p.D ? __ldg(p.D + dd) : 0.f);
+                v[0] = fma2(D2, get_pair<io_t>(vu, 0), v[0]);
+                v[1] = fma2(D2, get_pair<io_t>(vu, 1), v[1]);
+                if (has_z) {
+                    const quad_t vz =
+                        reinterpret_cast<const quad_t*>(tile(k, 2))[cc * C::SEGROW + seg];
+                    v[0] = gate_pair(v[0], get_pair<io_t>(vz, 0));
+                    v[1] = gate_pair(v[1], get_pair<io_t>(vz, 1));
+                }
+                unsigned w[PV * C::ES / 4];
+                pack_out<io_t, 2>(v, w);
+                *reinterpret_cast<quad_t*>(yy + (int64_t(b) * dim + dd) * L + int64_t(k) * T +
+                                           seg * PV) = *reinterpret_cast<const quad_t*>(w);
+            }
+            // the stage of chunk k is no longer read: refill it with chunk k+S
+            named_sync(kBarElem, NE);
+            if (te == 0 && k + S < nchunks) {
+                fence_proxy_async_smem();
+                issue(k + S);
+            }
+        }
+    }
+}
+
+// =========================================================================
 // Paired-chain tensor-map path (dstate == 4*G exactly)
 // =========================================================================
 // Two observations shape this kernel.
@@ -1130,6 +1328,28 @@ bool try_pair(const ScanArgs& a, cudaStream_t stream, cudaError_t* err) {
 // chain 8x2, 2: single chain 4 states x 4 threads, 3: paired chains) and
 // MAMBA_SCAN_PATH=reg forces the register-prefetch kernel; every choice
 // computes the same recurrence, and the tests check them against each other.
+template <typename io_t, int NPL, int G, int CH, int NE>
+bool try_ws(const ScanArgs& a, cudaStream_t stream, cudaError_t* err) {
+    using C = WsCfg<io_t, NPL, G, CH, NE>;
+    const int64_t es = sizeof(io_t);
+    const bool ok = a.dstate == C::NP && al16(a.u) && al16(a.delta) && al16(a.z) && al16(a.B) &&
+                    al16(a.C) && (reinterpret_cast<uintptr_t>(a.y) % (C::PV * es)) == 0 &&
+                    (a.seqlen * es) % 16 == 0 && a.batch * a.dim <= 0x7fffffff &&
+                    a.seqlen <= 0x7fffffff;
+    if (!ok) return false;
+    CUtensorMap mu, md, mz;
+    const bool bf = sizeof(io_t) == 2;
+    const int64_t rows = a.batch * a.dim;
+    if (!make_map(&mu, a.u, bf, rows, a.seqlen, C::T, CH) ||
+        !make_map(&md, a.delta, bf, rows, a.seqlen, C::T, CH) ||
+        !make_map(&mz, a.z ? a.z : a.u, bf, rows, a.seqlen, C::T, CH))
+        return false;
+    const int64_t dblocks = (a.dim + CH - 1) / CH;
+    *err = launch(scan_ws_kernel<io_t, NPL, G, CH, NE>, C::kSmem, dblocks * a.batch, C::NTH,
+                  stream, a, mu, md, mz, int(dblocks));
+    return true;
+}
+
 bool force_reg() {
     const char* v = getenv("MAMBA_SCAN_PATH");
     return v && v[0] == 'r';
@@ -1168,6 +1388,10 @@ cudaError_t dispatch(const ScanArgs& a, cudaStream_t stream) {
     if (N <= 16) {
         // Few chains (long sequences, small batch): more threads per chain.
         const bool few = a.batch * a.dim < 148 * 64;
+        cudaError_t err = cudaSuccess;
+        if ((tile == 4 || (tile == 0 && !few)) && N == 16 && !force_reg() &&
+            try_ws<io_t, 8, 2, 32, 64>(a, stream, &err))
+            return err;
         if (tile == 2 || (tile == 0 && few)) return run<io_t, 4, 4, 16, 32>(a, stream, false);
         return run<io_t, 8, 2, 32, 16>(a, stream, pair);
     }

@@ -174,13 +174,14 @@ def test_full_size_configs_on_sampled_chains(cuda, name):
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 @pytest.mark.parametrize("L,dim", [(336, 50), (4096, 33), (333, 50)])
 def test_all_tile_shapes_give_the_same_scan(cuda, io, L, dim, monkeypatch):
-    """dstate = 16 has three tile shapes: one chain x 8 states per thread
-    (default), one chain x 4 states, two chains x 4 states.  Each must match
-    the oracle and the others (odd channel counts leave half-used pairs)."""
+    """dstate = 16 has four tile shapes: one chain x 8 states per thread with
+    separate recurrence and element warps (default), the same without the
+    split, one chain x 4 states, two chains x 4 states.  Each must match the
+    oracle and the others (odd channel counts leave half-used pairs)."""
     x = workloads.make_scan_inputs(2, dim, L, 16, io, seed=16, d_mode="normal")
     yr, hr = oracle_scan(x)
     outs = []
-    for tile in ("0", "1", "2", "3"):
+    for tile in ("0", "1", "2", "3", "4"):
         monkeypatch.setenv("MAMBA_SCAN_TILE", tile)
         y, h = _run(x, cuda)
         _assert_close(x, y, h, yr, hr, what=f"tile {tile}")
