@@ -134,11 +134,14 @@ __device__ __forceinline__ int du_col(int t, int cc) {
     return cc ^ (((t >> 2) << 1) & (CH - 1));
 }
 
-// Swizzle of the 16-byte chunk index within a row of partial sums, so that
-// the per-step writes (consecutive rows) of phase B land in distinct banks.
-template <int T>
-__device__ __forceinline__ int yswz(int row) {
-    return (row ^ (row >> 2)) & (T / 4 - 1);
+// Partial sums of the recurrence live in a quad-major layout: 16-byte chunk
+// (steps 4q..4q+3) of row `row` is chunk q * ROWS + (row ^ q).  The XOR keeps
+// both the per-step writes (32 consecutive rows, one quad) and the
+// per-element reads (G rows of 8 chains x 4 quads) free of bank conflicts.
+template <int ROWS>
+__device__ __forceinline__ int yunit(int q, int row) {
+    static_assert(ROWS % 16 == 0, "rows come in groups of 16");
+    return q * ROWS + (row ^ q);
 }
 
 // ---- phase B ------------------------------------------------------------
@@ -154,8 +157,7 @@ __device__ __forceinline__ void recurrence(const float4* sdu, const float* sB, c
     const ulonglong2* du2 = reinterpret_cast<const ulonglong2*>(sdu);
     const ulonglong2* b2 = reinterpret_cast<const ulonglong2*>(sB) + g * NQ;
     const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(sC) + g * NQ;
-    float4* yrow = reinterpret_cast<float4*>(sy + tid * T);
-    const int sw = yswz<T>(tid);
+    float4* y4 = reinterpret_cast<float4*>(sy);
     struct Step {
         ulonglong2 sd;  // (dt, dt), (dt*u, dt*u)
         f32x2 a[2 * NQ];
@@ -200,7 +202,7 @@ __device__ __forceinline__ void recurrence(const float4* sdu, const float* sB, c
                 part[j] = update(cur);
                 if (tt + j + 1 < T) cur = nxt;
             }
-            yrow[(tt / 4) ^ sw] = make_float4(part[0], part[1], part[2], part[3]);
+            y4[yunit<CH * G>(tt / 4, tid)] = make_float4(part[0], part[1], part[2], part[3]);
         }
     } else {
         for (int tt = 0; tt < tlen; tt += 4) {
@@ -213,20 +215,20 @@ __device__ __forceinline__ void recurrence(const float4* sdu, const float* sB, c
                 part[j] = t < tlen ? update(cur) : 0.f;
                 if (t + 1 < tlen) cur = nxt;
             }
-            yrow[(tt / 4) ^ sw] = make_float4(part[0], part[1], part[2], part[3]);
+            y4[yunit<CH * G>(tt / 4, tid)] = make_float4(part[0], part[1], part[2], part[3]);
         }
     }
 }
 
 // Sum of the G partials of chain cc over the 4 steps [4*q4, 4*q4+4) of the
 // chunk, as two pairs.
-template <int G, int T>
+template <int G, int T, int ROWS>
 __device__ __forceinline__ void partial_sums(const float* sy, int cc, int q4, f32x2& s01,
                                              f32x2& s23) {
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
         const int r = cc * G + gg;
-        const ulonglong2 v = reinterpret_cast<const ulonglong2*>(sy + r * T)[q4 ^ yswz<T>(r)];
+        const ulonglong2 v = reinterpret_cast<const ulonglong2*>(sy)[yunit<ROWS>(q4, r)];
         s01 = gg == 0 ? v.x : add2(s01, v.x);
         s23 = gg == 0 ? v.y : add2(s23, v.y);
     }
@@ -262,6 +264,41 @@ __device__ __forceinline__ void widen_bc(const unsigned char* rawB, const unsign
             sC[idx] = ok ? float(rc[t * N + n]) : 0.f;
         }
     }
+}
+
+// widen_bc with 8-byte pieces, so that more threads share the work (the
+// element warps of the warp-specialised kernel: T * NP / 4 pieces of 4 values).
+template <typename io_t, int NP, int T, int NTH>
+__device__ __forceinline__ void widen_bc_split(const unsigned char* rawB,
+                                               const unsigned char* rawC, float* sB, float* sC,
+                                               int N, int tid) {
+    if constexpr (sizeof(io_t) == 2) {
+        if (N == NP && (N * 2) % 16 == 0) {
+            const uint2* rb = reinterpret_cast<const uint2*>(rawB);
+            const uint2* rc = reinterpret_cast<const uint2*>(rawC);
+            uint2 vb[(T * NP / 4 + NTH - 1) / NTH], vc[(T * NP / 4 + NTH - 1) / NTH];
+#pragma unroll
+            for (int r = 0; r < (T * NP / 4 + NTH - 1) / NTH; ++r) {
+                const int it = tid + r * NTH;
+                if (it < T * NP / 4) {
+                    vb[r] = rb[it];
+                    vc[r] = rc[it];
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < (T * NP / 4 + NTH - 1) / NTH; ++r) {
+                const int it = tid + r * NTH;
+                if (it < T * NP / 4) {
+                    reinterpret_cast<ulonglong2*>(sB)[it] = make_ulonglong2(
+                        get_pair<io_t>(vb[r], 0), get_pair<io_t>(vb[r], 1));
+                    reinterpret_cast<ulonglong2*>(sC)[it] = make_ulonglong2(
+                        get_pair<io_t>(vc[r], 0), get_pair<io_t>(vc[r], 1));
+                }
+            }
+            return;
+        }
+    }
+    widen_bc<io_t, NP, T, NTH>(rawB, rawC, sB, sC, N, tid);
 }
 
 template <int NPL, int G>
@@ -442,7 +479,7 @@ __global__ void __launch_bounds__(CH* G)
             const int64_t dd = d0 + cc;
             if (dd >= dim || seg * PV >= tlen) continue;
             f32x2 v[2];
-            partial_sums<G, T>(sy, cc, seg, v[0], v[1]);
+            partial_sums<G, T, CH * G>(sy, cc, seg, v[0], v[1]);
             const quad_t vu = reinterpret_cast<const quad_t*>(tile(s, 0))[cc * C::SEGROW + seg];
             const f32x2 D2 = splat2(p.D ? __ldg(p.D + dd) : 0.f);
             v[0] = fma2(D2, get_pair<io_t>(vu, 0), v[0]);
@@ -469,23 +506,30 @@ __global__ void __launch_bounds__(CH* G)
 // G-partial sum, skip and gate after it) and to issuing and waiting for the
 // bulk copies, all done by the same warps between barriers while the
 // recurrence waited.  Here the CTA has two roles that overlap:
-//   recurrence warps (CH*G threads) -- the state update of chunk k;
-//   element warps (NE threads)      -- the bulk copies, the per-element
-//                                      prologue of chunk k+1 (and the fp32
-//                                      widening of its B and C) and the
-//                                      epilogue of chunk k-1.
+//   recurrence warps (NR threads) -- the state update of chunk k;
+//   element warps (NE threads)    -- the bulk copies, the per-element
+//                                    prologue of chunk k+1 (and the fp32
+//                                    widening of its B and C) and the
+//                                    epilogue of chunk k-1.
 // Hand-off buffers are double-buffered and signalled with named barriers:
 // "prologue of chunk k ready" (element warps arrive, recurrence warps wait)
 // and "recurrence of chunk k done" (the reverse).
-template <typename io_t, int NPL, int G, int CH, int NE>
+//
+// A recurrence thread owns NPL states of P chains.  B and C of a step are
+// shared by every channel of a batch row, so with P = 2 each B/C value read
+// from shared memory serves two chains: per state update the thread reads
+// 8/P bytes of B and C plus 16/NPL bytes of (dt, dt*u).
+template <typename io_t, int P, int NPL, int G, int NR, int NE>
 struct WsCfg {
     static constexpr int T = 16, S = 4;
-    static constexpr int NR = CH * G;  // recurrence threads
     static constexpr int NTH = NR + NE;
+    static constexpr int NGRP = NR / G;     // chain slots per chain set
+    static constexpr int CH = P * NGRP;     // chains per CTA
     static constexpr int NP = NPL * G, ES = sizeof(io_t), PV = 4;
     static constexpr int SEGROW = T / PV;
     static constexpr int NSEG = CH * SEGROW;
-    static constexpr int SPT = (NSEG + NE - 1) / NE;
+    static constexpr int SPT = NSEG / NE;   // segments per element thread
+    static constexpr int CW = CH / (NE / 32);  // chains per element warp
     static constexpr size_t rnd(size_t x) { return (x + 127) / 128 * 128; }
     static constexpr size_t kTile = rnd(size_t(CH) * T * ES);
     static constexpr size_t kRaw = rnd(size_t(T) * NP * ES);
@@ -495,12 +539,116 @@ struct WsCfg {
     static constexpr size_t kBc = kRing + S * kStage;
     static constexpr size_t kDuBuf = size_t(T) * CH * 16;
     static constexpr size_t kDu = kBc + 2 * kBcBuf;
-    static constexpr size_t kYBuf = size_t(NR) * T * 4;
+    static constexpr size_t kYBuf = size_t(CH) * G * T * 4;
     static constexpr size_t kY = kDu + 2 * kDuBuf;
     static constexpr size_t kSmem = kY + 2 * kYBuf;
     using quad_t = std::conditional_t<ES == 2, uint2, uint4>;
     static_assert(NR % 32 == 0 && NE % 32 == 0, "roles are whole warps");
+    static_assert(NSEG % NE == 0, "element threads share the segments evenly");
+    static_assert(NE == 64, "two element warps: one copies B, the other C");
+    static_assert(CW * SEGROW == 32 * SPT, "an element warp covers its chains exactly");
+    static_assert((T * NP * ES) % (32 * 16) == 0, "B and C split into 16-byte pieces per lane");
+    static_assert((size_t(CW) * T * ES) % 128 == 0, "per-warp tile rows stay 128-byte aligned");
+    static_assert((CH & (CH - 1)) == 0, "chain count per CTA is a power of two");
 };
+
+// The recurrence over one chunk for P chains x NPL states of one thread (the
+// multi-chain form of recurrence() above; rows of sy are chain * G + g).
+template <int P, int NPL, int G, int CH, int T>
+__device__ __forceinline__ void recurrence_multi(const float4* sdu, const float* sB,
+                                                 const float* sC, float* sy,
+                                                 f32x2 (&h)[P][NPL / 2],
+                                                 const f32x2 (&A2)[P][NPL / 2],
+                                                 const int (&cc)[P], int g, int tlen) {
+    constexpr int NQ = NPL / 4, NP = NPL * G;
+    const ulonglong2* du2 = reinterpret_cast<const ulonglong2*>(sdu);
+    const ulonglong2* b2 = reinterpret_cast<const ulonglong2*>(sB) + g * NQ;
+    const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(sC) + g * NQ;
+    float4* y4 = reinterpret_cast<float4*>(sy);
+    int row[P];
+#pragma unroll
+    for (int p = 0; p < P; ++p) row[p] = cc[p] * G + g;
+    struct Step {
+        ulonglong2 sd[P];  // (dt, dt), (dt*u, dt*u) per chain
+        f32x2 a[P][2 * NQ];
+        ulonglong2 bq[NQ], cq[NQ];
+    };
+    auto fetch = [&](int t, Step& st) {
+#pragma unroll
+        for (int p = 0; p < P; ++p) st.sd[p] = du2[t * CH + du_col<CH>(t, cc[p])];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            st.bq[q] = b2[t * (NP / 4) + q];
+            st.cq[q] = c2[t * (NP / 4) + q];
+        }
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+#pragma unroll
+            for (int q = 0; q < 2 * NQ; ++q) {
+                float x0, x1;
+                unpack2(mul2(st.sd[p].x, A2[p][q]), x0, x1);
+                st.a[p][q] = pack2(ex2_approx(x0), ex2_approx(x1));
+            }
+        }
+    };
+    auto update = [&](const Step& st, float (&out)[P]) {
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            f32x2 acc = splat2(0.f);
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                h[p][2 * q] = fma2(st.a[p][2 * q], h[p][2 * q], mul2(st.sd[p].y, st.bq[q].x));
+                h[p][2 * q + 1] =
+                    fma2(st.a[p][2 * q + 1], h[p][2 * q + 1], mul2(st.sd[p].y, st.bq[q].y));
+                acc = fma2(st.cq[q].x, h[p][2 * q], acc);
+                acc = fma2(st.cq[q].y, h[p][2 * q + 1], acc);
+            }
+            float lo, hi;
+            unpack2(acc, lo, hi);
+            out[p] = lo + hi;
+        }
+    };
+    Step cur;
+    fetch(0, cur);
+    if (tlen == T) {
+#pragma unroll
+        for (int tt = 0; tt < T; tt += 4) {
+            float part[4][P];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                Step nxt;
+                if (tt + j + 1 < T) fetch(tt + j + 1, nxt);
+                update(cur, part[j]);
+                if (tt + j + 1 < T) cur = nxt;
+            }
+#pragma unroll
+            for (int p = 0; p < P; ++p)
+                y4[yunit<CH * G>(tt / 4, row[p])] =
+                    make_float4(part[0][p], part[1][p], part[2][p], part[3][p]);
+        }
+    } else {
+        for (int tt = 0; tt < tlen; tt += 4) {
+            float part[4][P];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int t = tt + j;
+                Step nxt;
+                if (t + 1 < tlen) fetch(t + 1, nxt);
+                if (t < tlen) {
+                    update(cur, part[j]);
+                } else {
+#pragma unroll
+                    for (int p = 0; p < P; ++p) part[j][p] = 0.f;
+                }
+                if (t + 1 < tlen) cur = nxt;
+            }
+#pragma unroll
+            for (int p = 0; p < P; ++p)
+                y4[yunit<CH * G>(tt / 4, row[p])] =
+                    make_float4(part[0][p], part[1][p], part[2][p], part[3][p]);
+        }
+    }
+}
 
 __device__ __forceinline__ void named_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -512,13 +660,14 @@ constexpr int kBarReady = 1;  // + (chunk & 1): prologue of the chunk written
 constexpr int kBarDone = 3;   // + (chunk & 1): recurrence of the chunk done
 constexpr int kBarElem = 5;   // element warps only
 
-template <typename io_t, int NPL, int G, int CH, int NE>
-__global__ void __launch_bounds__(CH* G + NE, 4)
+template <typename io_t, int P, int NPL, int G, int NR, int NE, int MINB>
+__global__ void __launch_bounds__(NR + NE, MINB)
     scan_ws_kernel(const ScanArgs p, const __grid_constant__ CUtensorMap tm_u,
                    const __grid_constant__ CUtensorMap tm_d,
                    const __grid_constant__ CUtensorMap tm_z, const int dblocks) {
-    using C = WsCfg<io_t, NPL, G, CH, NE>;
-    constexpr int T = C::T, S = C::S, NR = C::NR, NTH = C::NTH, NP = C::NP, PV = C::PV;
+    using C = WsCfg<io_t, P, NPL, G, NR, NE>;
+    constexpr int T = C::T, S = C::S, NTH = C::NTH, NP = C::NP, PV = C::PV, CH = C::CH;
+    constexpr int SPT = C::SPT;
     using quad_t = typename C::quad_t;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
@@ -542,119 +691,215 @@ __global__ void __launch_bounds__(CH* G + NE, 4)
     const io_t* Cg = static_cast<const io_t*>(p.C) + int64_t(b) * L * N;
     auto chunk_len = [&](int k) { return L - k * T < T ? L - k * T : T; };
 
-    auto issue = [&](int k) {  // one element thread
+    // Each element warp w owns chains [w * CW, (w + 1) * CW) of the CTA and
+    // copies its own rows of the u / delta / z tiles; warp 0 also copies B and
+    // warp 1 C.  Every warp thus waits on its own mbarrier per stage and
+    // refills a stage as soon as it has finished with it, with no barrier
+    // across the element warps.
+    constexpr int CW = C::CW;
+    auto issue = [&](int k, int w) {  // lane 0 of element warp w
         const uint32_t bc_bytes = uint32_t(chunk_len(k)) * N * C::ES;
-        const uint32_t tile_bytes = uint32_t(CH) * T * C::ES;
-        uint64_t* br = &bar[k & (S - 1)];
-        unsigned char* st = stage(k);
-        mbar_arrive_expect_tx(br, (has_z ? 3 : 2) * tile_bytes + 2 * bc_bytes);
-        tma_load_2d(st, &tm_u, k * T, row0, br);
-        tma_load_2d(st + C::kTile, &tm_d, k * T, row0, br);
-        if (has_z) tma_load_2d(st + 2 * C::kTile, &tm_z, k * T, row0, br);
-        bulk_g2s(st + 3 * C::kTile, Bg + int64_t(k) * T * N, bc_bytes, br);
-        bulk_g2s(st + 3 * C::kTile + C::kRaw, Cg + int64_t(k) * T * N, bc_bytes, br);
+        const uint32_t rows_bytes = uint32_t(CW) * T * C::ES;
+        uint64_t* br = &bar[(k & (S - 1)) * 2 + w];
+        unsigned char* st = stage(k) + w * rows_bytes;
+        mbar_arrive_expect_tx(br, (has_z ? 3 : 2) * rows_bytes + bc_bytes);
+        tma_load_2d(st, &tm_u, k * T, row0 + w * CW, br);
+        tma_load_2d(st + C::kTile, &tm_d, k * T, row0 + w * CW, br);
+        if (has_z) tma_load_2d(st + 2 * C::kTile, &tm_z, k * T, row0 + w * CW, br);
+        bulk_g2s(raw(k, w), (w == 0 ? Bg : Cg) + int64_t(k) * T * N, bc_bytes, br);
     };
 
     if (tid == NR) {
-        for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+        for (int s = 0; s < 2 * S; ++s) mbar_init(&bar[s], 1);
         fence_mbar_init();
-        fence_proxy_async_smem();
-        for (int k = 0; k < S && k < nchunks; ++k) issue(k);
     }
     __syncthreads();
 
     if (tid < NR) {
         // ---------------- recurrence warps ----------------
-        const int c = tid / G, g = tid % G;
-        const int64_t d = d0 + c;
-        f32x2 A2[NPL / 2], h[NPL / 2];
-        init_state<NPL, G>(p, d, d < dim, g, A2, h);
+        const int grp = tid / G, g = tid % G;
+        int cc[P];
+        f32x2 A2[P][NPL / 2], h[P][NPL / 2];
+#pragma unroll
+        for (int q = 0; q < P; ++q) {
+            cc[q] = grp + q * C::NGRP;
+            init_state<NPL, G>(p, d0 + cc[q], d0 + cc[q] < dim, g, A2[q], h[q]);
+        }
         for (int k = 0; k < nchunks; ++k) {
             named_sync(kBarReady + (k & 1), NTH);
             const float* sB = bcbuf(k);
-            recurrence<NPL, G, CH, T>(dubuf(k), sB, sB + T * NP, ybuf(k), h, A2, c, g, tid,
-                                      chunk_len(k));
+            if constexpr (P == 1) {
+                recurrence<NPL, G, CH, T>(dubuf(k), sB, sB + T * NP, ybuf(k), h[0], A2[0], cc[0],
+                                          g, tid, chunk_len(k));
+            } else {
+                recurrence_multi<P, NPL, G, CH, T>(dubuf(k), sB, sB + T * NP, ybuf(k), h, A2, cc,
+                                                   g, chunk_len(k));
+            }
             named_arrive(kBarDone + (k & 1), NTH);
         }
-        if (d < dim && p.last_state) store_state<NPL, G>(p, int64_t(b) * dim + d, g, h);
+#pragma unroll
+        for (int q = 0; q < P; ++q)
+            if (d0 + cc[q] < dim && p.last_state)
+                store_state<NPL, G>(p, int64_t(b) * dim + d0 + cc[q], g, h[q]);
         return;
     }
 
     // ---------------- element warps ----------------
-    const int te = tid - NR;
-    io_t* yy = static_cast<io_t*>(p.y);
-    for (int j = 0; j <= nchunks; ++j) {
-        if (j < nchunks) {
-            // prologue of chunk j
-            if (!mbar_wait(&bar[j & (S - 1)], uint32_t(j / S) & 1u))
-                atomicOr(&g_scan_error, kErrWaitTimeout);
-            float* sB = bcbuf(j);
-            widen_bc<io_t, NP, T, NE>(raw(j, 0), raw(j, 1), sB, sB + T * NP, N, te);
-            const int tlen = chunk_len(j);
-            float4* sdu = dubuf(j);
+    // Lane l of element warp w handles segment (l % SEGROW) of the chains
+    // w * CW + l / SEGROW + i * (32 / SEGROW), i < SPT.  Their bias and D, and
+    // every shared-memory offset the thread uses, are fixed for the whole
+    // sequence.  One pass per chunk k finishes chunk k - 1 (partial sums, skip
+    // term, gate, store of y) and prepares chunk k + 1 (dt, dt * u, fp32 B or
+    // C), loading all of its shared-memory inputs first so that the two
+    // halves' dependency chains overlap.
+    const int te = tid - NR, w = te / 32, lane = te % 32;
+    const int seg = lane % C::SEGROW;
+    constexpr int ROWS = CH * G;
+    int ec[SPT], tq[SPT], dub[SPT], yu[SPT][G];
+    f32x2 bias2[SPT], Dv2[SPT];
+    bool chain_ok[SPT];
+    io_t* yg[SPT];
 #pragma unroll
-            for (int i = 0; i < C::SPT; ++i) {
-                const int sidx = te + i * NE;
-                if (sidx >= C::NSEG) break;
-                const int seg = sidx % C::SEGROW, cc = sidx / C::SEGROW;
-                const int64_t dd = d0 + cc;
-                const bool live = dd < dim && seg * PV < tlen;
-                const quad_t vd = reinterpret_cast<const quad_t*>(tile(j, 1))[cc * C::SEGROW + seg];
-                const quad_t vu = reinterpret_cast<const quad_t*>(tile(j, 0))[cc * C::SEGROW + seg];
-                const f32x2 bias2 =
-                    splat2((dd < dim && p.delta_bias) ? __ldg(p.delta_bias + dd) : 0.f);
+    for (int i = 0; i < SPT; ++i) {
+        ec[i] = w * CW + lane / C::SEGROW + i * (32 / C::SEGROW);
+        const int64_t dd = d0 + ec[i];
+        chain_ok[i] = dd < dim;
+        bias2[i] = splat2((chain_ok[i] && p.delta_bias) ? __ldg(p.delta_bias + dd) : 0.f);
+        Dv2[i] = splat2((chain_ok[i] && p.D) ? __ldg(p.D + dd) : 0.f);
+        tq[i] = ec[i] * C::SEGROW + seg;
+        dub[i] = seg * PV * CH + (ec[i] ^ ((2 * seg) & (CH - 1)));  // du_col of steps 4*seg..+3
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) yu[i][gg] = yunit<ROWS>(seg, ec[i] * G + gg);
+        yg[i] = static_cast<io_t*>(p.y) + (int64_t(b) * dim + dd) * L + seg * PV;
+    }
+    const bool all_chains = d0 + CH <= dim;
+    if (lane == 0) {
+        fence_proxy_async_smem();
+        for (int k = 0; k < S && k < nchunks; ++k) issue(k, w);
+    }
+    __syncwarp();
+
+    // ke: chunk to finish (or -1), kp: chunk to prepare (or -1)
+    auto pass = [&](int ke, int kp) {
+        // ---- loads ----
+        ulonglong2 ps[SPT][G];
+        quad_t eu[SPT], ez[SPT], pd[SPT], pu[SPT];
+        if (ke >= 0) {
+            const ulonglong2* sy = reinterpret_cast<const ulonglong2*>(ybuf(ke));
+            const quad_t* tu = reinterpret_cast<const quad_t*>(tile(ke, 0));
+            const quad_t* tz = reinterpret_cast<const quad_t*>(tile(ke, 2));
+#pragma unroll
+            for (int i = 0; i < SPT; ++i) {
+#pragma unroll
+                for (int gg = 0; gg < G; ++gg) ps[i][gg] = sy[yu[i][gg]];
+                eu[i] = tu[tq[i]];
+                if (has_z) ez[i] = tz[tq[i]];
+            }
+        }
+        constexpr int BCV = T * NP * C::ES / 32 / 16;  // 16-byte pieces of B or C per lane
+        uint4 rbc[BCV];
+        if (kp >= 0) {
+            if (!mbar_wait(&bar[(kp & (S - 1)) * 2 + w], uint32_t(kp / S) & 1u))
+                atomicOr(&g_scan_error, kErrWaitTimeout);
+            const quad_t* td = reinterpret_cast<const quad_t*>(tile(kp, 1));
+            const quad_t* tu = reinterpret_cast<const quad_t*>(tile(kp, 0));
+#pragma unroll
+            for (int i = 0; i < SPT; ++i) {
+                pd[i] = td[tq[i]];
+                pu[i] = tu[tq[i]];
+            }
+            const uint4* rw = reinterpret_cast<const uint4*>(raw(kp, w));
+#pragma unroll
+            for (int r = 0; r < BCV; ++r) rbc[r] = rw[lane * BCV + r];
+        }
+        // ---- finish chunk ke ----
+        if (ke >= 0) {
+            const bool seg_live = seg * PV < chunk_len(ke);
+#pragma unroll
+            for (int i = 0; i < SPT; ++i) {
+                f32x2 v0 = ps[i][0].x, v1 = ps[i][0].y;
+#pragma unroll
+                for (int gg = 1; gg < G; ++gg) {
+                    v0 = add2(v0, ps[i][gg].x);
+                    v1 = add2(v1, ps[i][gg].y);
+                }
+                v0 = fma2(Dv2[i], get_pair<io_t>(eu[i], 0), v0);
+                v1 = fma2(Dv2[i], get_pair<io_t>(eu[i], 1), v1);
+                if (has_z) {
+                    v0 = gate_pair(v0, get_pair<io_t>(ez[i], 0));
+                    v1 = gate_pair(v1, get_pair<io_t>(ez[i], 1));
+                }
+                f32x2 v[2] = {v0, v1};
+                unsigned wd[PV * C::ES / 4];
+                pack_out<io_t, 2>(v, wd);
+                if (chain_ok[i] && seg_live)
+                    *reinterpret_cast<quad_t*>(yg[i] + int64_t(ke) * T) =
+                        *reinterpret_cast<const quad_t*>(wd);
+            }
+        }
+        // ---- prepare chunk kp ----
+        if (kp >= 0) {
+            float4 o[SPT][PV];
+#pragma unroll
+            for (int i = 0; i < SPT; ++i) {
 #pragma unroll
                 for (int q = 0; q < PV / 2; ++q) {
-                    f32x2 dt = add2(get_pair<io_t>(vd, q), bias2);
+                    f32x2 dt = add2(get_pair<io_t>(pd[i], q), bias2[i]);
                     if (p.softplus) dt = softplus_pair<io_t>(dt);
-                    const f32x2 du = mul2(dt, get_pair<io_t>(vu, q));
+                    const f32x2 du = mul2(dt, get_pair<io_t>(pu[i], q));
                     float dt0, dt1, du0, du1;
                     unpack2(dt, dt0, dt1);
                     unpack2(du, du0, du1);
-                    if (!live) dt0 = dt1 = du0 = du1 = 0.f;
-                    const int t = seg * PV + 2 * q;
-                    sdu[t * CH + du_col<CH>(t, cc)] = make_float4(dt0, dt0, du0, du0);
-                    sdu[(t + 1) * CH + du_col<CH>(t + 1, cc)] = make_float4(dt1, dt1, du1, du1);
+                    o[i][2 * q] = make_float4(dt0, dt0, du0, du0);
+                    o[i][2 * q + 1] = make_float4(dt1, dt1, du1, du1);
                 }
             }
-            named_arrive(kBarReady + (j & 1), NTH);
-        }
-        if (j >= 1) {
-            // epilogue of chunk k = j-1
-            const int k = j - 1;
-            named_sync(kBarDone + (k & 1), NTH);
-            const int tlen = chunk_len(k);
-            const float* sy = ybuf(k);
+            if (!all_chains || chunk_len(kp) < T) {  // zero steps past the end, dead chains
+                const int tl = chunk_len(kp);
 #pragma unroll
-            for (int i = 0; i < C::SPT; ++i) {
-                const int sidx = te + i * NE;
-                if (sidx >= C::NSEG) break;
-                const int seg = sidx % C::SEGROW, cc = sidx / C::SEGROW;
-                const int64_t dd = d0 + cc;
-                if (dd >= dim || seg * PV >= tlen) continue;
-                f32x2 v[2];
-                partial_sums<G, T>(sy, cc, seg, v[0], v[1]);
-                const quad_t vu = reinterpret_cast<const quad_t*>(tile(k, 0))[cc * C::SEGROW + seg];
-                const f32x2 D2 = splat2(p.D ? __ldg(p.D + dd) : 0.f);
-                v[0] = fma2(D2, get_pair<io_t>(vu, 0), v[0]);
-                v[1] = fma2(D2, get_pair<io_t>(vu, 1), v[1]);
-                if (has_z) {
-                    const quad_t vz =
-                        reinterpret_cast<const quad_t*>(tile(k, 2))[cc * C::SEGROW + seg];
-                    v[0] = gate_pair(v[0], get_pair<io_t>(vz, 0));
-                    v[1] = gate_pair(v[1], get_pair<io_t>(vz, 1));
+                for (int i = 0; i < SPT; ++i)
+#pragma unroll
+                    for (int e = 0; e < PV; ++e)
+                        if (!chain_ok[i] || seg * PV + e >= tl) o[i][e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            float4* sdu = dubuf(kp);
+#pragma unroll
+            for (int i = 0; i < SPT; ++i)
+#pragma unroll
+                for (int e = 0; e < PV; ++e) sdu[dub[i] + e * CH] = o[i][e];
+            // fp32 copy of this warp's B (w = 0) or C (w = 1)
+            float* dst = bcbuf(kp) + w * T * NP + lane * BCV * (16 / C::ES);
+#pragma unroll
+            for (int r = 0; r < BCV; ++r) {
+                if constexpr (C::ES == 2) {
+                    reinterpret_cast<ulonglong2*>(dst)[2 * r] =
+                        make_ulonglong2(get_pair<io_t>(rbc[r], 0), get_pair<io_t>(rbc[r], 1));
+                    reinterpret_cast<ulonglong2*>(dst)[2 * r + 1] =
+                        make_ulonglong2(get_pair<io_t>(rbc[r], 2), get_pair<io_t>(rbc[r], 3));
+                } else {
+                    reinterpret_cast<uint4*>(dst)[r] = rbc[r];
                 }
-                unsigned w[PV * C::ES / 4];
-                pack_out<io_t, 2>(v, w);
-                *reinterpret_cast<quad_t*>(yy + (int64_t(b) * dim + dd) * L + int64_t(k) * T +
-                                           seg * PV) = *reinterpret_cast<const quad_t*>(w);
             }
-            // the stage of chunk k is no longer read: refill it with chunk k+S
-            named_sync(kBarElem, NE);
-            if (te == 0 && k + S < nchunks) {
-                fence_proxy_async_smem();
-                issue(k + S);
-            }
+        }
+    };
+
+    if (nchunks == 0) return;
+    pass(-1, 0);
+    named_arrive(kBarReady + 0, NTH);
+    if (nchunks > 1) {
+        pass(-1, 1);
+        named_arrive(kBarReady + 1, NTH);
+    }
+    for (int j = 1; j <= nchunks; ++j) {
+        named_sync(kBarDone + ((j - 1) & 1), NTH);
+        const int kp = j + 1 < nchunks ? j + 1 : -1;
+        pass(j - 1, kp);
+        if (kp >= 0) named_arrive(kBarReady + (kp & 1), NTH);
+        // this warp no longer reads the stage of chunk j - 1: refill it
+        __syncwarp();
+        if (lane == 0 && j - 1 + S < nchunks) {
+            fence_proxy_async_smem();
+            issue(j - 1 + S, w);
         }
     }
 }
@@ -806,7 +1051,7 @@ __global__ void __launch_bounds__(64)
         const int64_t dd = d0 + cc;
         if (dd >= dim || seg * PV >= chunk_len(k)) return;
         f32x2 v[2];
-        partial_sums<G, T>(ybuf(k), cc, seg, v[0], v[1]);
+        partial_sums<G, T, C::CH * G>(ybuf(k), cc, seg, v[0], v[1]);
         const quad_t vu = reinterpret_cast<const quad_t*>(tile(k, 0))[cc * C::SEGROW + seg];
         const f32x2 D2 = splat2(p.D ? __ldg(p.D + dd) : 0.f);
         v[0] = fma2(D2, get_pair<io_t>(vu, 0), v[0]);
@@ -851,7 +1096,6 @@ __global__ void __launch_bounds__(64)
     __syncthreads();
 
     const int ra = (2 * pr) * G + g, rb = ra + G;  // partial-sum rows of chains a, b
-    const int swa = yswz<T>(ra), swb = yswz<T>(rb);
 
     struct Step {
         ulonglong2 sd;  // (dt_a, dt_b), (du_a, du_b)
@@ -884,8 +1128,7 @@ __global__ void __launch_bounds__(64)
         const ulonglong2* sd2 = reinterpret_cast<const ulonglong2*>(sdbuf(k));
         const quad_t* rB = reinterpret_cast<const quad_t*>(raw(k, 0));
         const quad_t* rC = reinterpret_cast<const quad_t*>(raw(k, 1));
-        float4* yra = reinterpret_cast<float4*>(ybuf(k) + ra * T);
-        float4* yrb = reinterpret_cast<float4*>(ybuf(k) + rb * T);
+        float4* y4 = reinterpret_cast<float4*>(ybuf(k));
 
         auto fetch = [&](int t, Step& st) {
             st.sd = sd2[t * NPAIR + pair_col<NPAIR>(t, pr)];
@@ -933,8 +1176,8 @@ __global__ void __launch_bounds__(64)
                     update(cur, pa[j], pb[j]);
                     if (t + 1 < T) cur = nxt;
                 }
-                yra[grp ^ swa] = make_float4(pa[0], pa[1], pa[2], pa[3]);
-                yrb[grp ^ swb] = make_float4(pb[0], pb[1], pb[2], pb[3]);
+                y4[yunit<C::CH * G>(grp, ra)] = make_float4(pa[0], pa[1], pa[2], pa[3]);
+                y4[yunit<C::CH * G>(grp, rb)] = make_float4(pb[0], pb[1], pb[2], pb[3]);
                 if (C::IL) {
 #pragma unroll
                     for (int i = 0; i < SPT; ++i) {
@@ -958,8 +1201,8 @@ __global__ void __launch_bounds__(64)
                         update(st, pa[j], pb[j]);
                     }
                 }
-                yra[(tt / 4) ^ swa] = make_float4(pa[0], pa[1], pa[2], pa[3]);
-                yrb[(tt / 4) ^ swb] = make_float4(pb[0], pb[1], pb[2], pb[3]);
+                y4[yunit<C::CH * G>(tt / 4, ra)] = make_float4(pa[0], pa[1], pa[2], pa[3]);
+                y4[yunit<C::CH * G>(tt / 4, rb)] = make_float4(pb[0], pb[1], pb[2], pb[3]);
             }
 #pragma unroll
             for (int i = 0; i < SPT; ++i) {
@@ -1175,7 +1418,7 @@ __global__ void __launch_bounds__(CH* G)
             f32x2 v[VEC / 2];
 #pragma unroll
             for (int q4 = 0; q4 < VEC / 4; ++q4)
-                partial_sums<G, T>(sy, cc, seg * (VEC / 4) + q4, v[2 * q4], v[2 * q4 + 1]);
+                partial_sums<G, T, CH * G>(sy, cc, seg * (VEC / 4) + q4, v[2 * q4], v[2 * q4 + 1]);
             const f32x2 D2 = splat2(p.D ? __ldg(p.D + dd) : 0.f);
 #pragma unroll
             for (int q = 0; q < VEC / 2; ++q) {
@@ -1328,9 +1571,9 @@ bool try_pair(const ScanArgs& a, cudaStream_t stream, cudaError_t* err) {
 // chain 8x2, 2: single chain 4 states x 4 threads, 3: paired chains) and
 // MAMBA_SCAN_PATH=reg forces the register-prefetch kernel; every choice
 // computes the same recurrence, and the tests check them against each other.
-template <typename io_t, int NPL, int G, int CH, int NE>
+template <typename io_t, int P, int NPL, int G, int NR, int NE, int MINB>
 bool try_ws(const ScanArgs& a, cudaStream_t stream, cudaError_t* err) {
-    using C = WsCfg<io_t, NPL, G, CH, NE>;
+    using C = WsCfg<io_t, P, NPL, G, NR, NE>;
     const int64_t es = sizeof(io_t);
     const bool ok = a.dstate == C::NP && al16(a.u) && al16(a.delta) && al16(a.z) && al16(a.B) &&
                     al16(a.C) && (reinterpret_cast<uintptr_t>(a.y) % (C::PV * es)) == 0 &&
@@ -1340,13 +1583,13 @@ bool try_ws(const ScanArgs& a, cudaStream_t stream, cudaError_t* err) {
     CUtensorMap mu, md, mz;
     const bool bf = sizeof(io_t) == 2;
     const int64_t rows = a.batch * a.dim;
-    if (!make_map(&mu, a.u, bf, rows, a.seqlen, C::T, CH) ||
-        !make_map(&md, a.delta, bf, rows, a.seqlen, C::T, CH) ||
-        !make_map(&mz, a.z ? a.z : a.u, bf, rows, a.seqlen, C::T, CH))
+    if (!make_map(&mu, a.u, bf, rows, a.seqlen, C::T, C::CW) ||
+        !make_map(&md, a.delta, bf, rows, a.seqlen, C::T, C::CW) ||
+        !make_map(&mz, a.z ? a.z : a.u, bf, rows, a.seqlen, C::T, C::CW))
         return false;
-    const int64_t dblocks = (a.dim + CH - 1) / CH;
-    *err = launch(scan_ws_kernel<io_t, NPL, G, CH, NE>, C::kSmem, dblocks * a.batch, C::NTH,
-                  stream, a, mu, md, mz, int(dblocks));
+    const int64_t dblocks = (a.dim + C::CH - 1) / C::CH;
+    *err = launch(scan_ws_kernel<io_t, P, NPL, G, NR, NE, MINB>, C::kSmem, dblocks * a.batch,
+                  C::NTH, stream, a, mu, md, mz, int(dblocks));
     return true;
 }
 
@@ -1390,7 +1633,13 @@ cudaError_t dispatch(const ScanArgs& a, cudaStream_t stream) {
         const bool few = a.batch * a.dim < 148 * 64;
         cudaError_t err = cudaSuccess;
         if ((tile == 4 || (tile == 0 && !few)) && N == 16 && !force_reg() &&
-            try_ws<io_t, 8, 2, 32, 64>(a, stream, &err))
+            try_ws<io_t, 1, 8, 2, 64, 64, 4>(a, stream, &err))
+            return err;
+        if (tile == 5 && N == 16 && !force_reg() && try_ws<io_t, 2, 8, 2, 64, 64, 2>(a, stream, &err))
+            return err;
+        if (tile == 6 && N == 16 && !force_reg() && try_ws<io_t, 2, 4, 4, 64, 64, 4>(a, stream, &err))
+            return err;
+        if (tile == 7 && N == 16 && !force_reg() && try_ws<io_t, 1, 4, 4, 128, 64, 4>(a, stream, &err))
             return err;
         if (tile == 2 || (tile == 0 && few)) return run<io_t, 4, 4, 16, 32>(a, stream, false);
         return run<io_t, 8, 2, 32, 16>(a, stream, pair);

@@ -181,7 +181,7 @@ def test_all_tile_shapes_give_the_same_scan(cuda, io, L, dim, monkeypatch):
     x = workloads.make_scan_inputs(2, dim, L, 16, io, seed=16, d_mode="normal")
     yr, hr = oracle_scan(x)
     outs = []
-    for tile in ("0", "1", "2", "3", "4"):
+    for tile in ("0", "1", "2", "3", "4", "5", "6", "7"):
         monkeypatch.setenv("MAMBA_SCAN_TILE", tile)
         y, h = _run(x, cuda)
         _assert_close(x, y, h, yr, hr, what=f"tile {tile}")
