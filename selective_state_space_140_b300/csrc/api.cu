@@ -91,8 +91,9 @@ int mamba_selective_scan_fwd(const void* u, const void* delta, const float* A_lo
 
     mamba::ScanArgs a{u, delta, A_log, B, C, D, z, delta_bias, y, last_state,
                       batch, dim, seqlen, int(dstate), softplus_flag != 0};
-    const cudaError_t err =
-        mamba::launch_scan_fwd(a, io_dtype == MAMBA_BF16, reinterpret_cast<cudaStream_t>(stream));
+    const mamba::ScanScratch scratch{nullptr, 0, true};
+    const cudaError_t err = mamba::launch_scan_fwd(a, io_dtype == MAMBA_BF16,
+                                                   reinterpret_cast<cudaStream_t>(stream), scratch);
     return err == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
 }
 

@@ -183,6 +183,27 @@ struct ScanArgs {
     int softplus;
 };
 
+// A scan split along time into nseg segments of seg_len steps (the last may
+// be shorter): a summary pass gives each segment's end state from a zero start
+// and the sum of its dt, a carry pass chains them, and the full pass runs
+// every segment from the state that enters it.
+struct SegArgs {
+    int seg_len;    // steps per segment, a multiple of 16
+    int nseg;       // segments of the sequence (1: no split)
+    int grid_nseg;  // segments covered by one launch (nseg, or nseg - 1 for the summary)
+    float* hcarry;  // [batch * dim][nseg - 1][dstate]
+    float* sdt;     // [batch * dim][nseg - 1]
+};
+
+// Scratch memory the forward scan may use for a split: a caller buffer of
+// `bytes` (ptr != nullptr: never allocates) or, with ptr == nullptr and
+// may_alloc, stream-ordered memory taken and returned on the launch stream.
+struct ScanScratch {
+    void* ptr;
+    size_t bytes;
+    bool may_alloc;
+};
+
 struct StateUpdateArgs {
     float* state;
     const void* x;
@@ -200,7 +221,9 @@ struct StateUpdateArgs {
 };
 
 // Launchers (return the cudaError_t of the launch).
-cudaError_t launch_scan_fwd(const ScanArgs& a, bool bf16, cudaStream_t stream);
+// cudaErrorMemoryAllocation: the split needs more than a caller buffer holds.
+cudaError_t launch_scan_fwd(const ScanArgs& a, bool bf16, cudaStream_t stream,
+                            const ScanScratch& scratch);
 // Synchronise `stream`, then read and clear the scan's device error word.
 cudaError_t read_and_clear_device_error(unsigned int* word, cudaStream_t stream);
 cudaError_t launch_state_update(const StateUpdateArgs& a, bool bf16, cudaStream_t stream);

@@ -335,6 +335,27 @@ __device__ __forceinline__ void store_state(const ScanArgs& p, int64_t chain, in
     }
 }
 
+// State of NPL states per thread from / to an fp32 [N] row (segmented scan).
+template <int NPL, int G>
+__device__ __forceinline__ void load_state(const float* src, int N, int g, f32x2 (&h)[NPL / 2]) {
+#pragma unroll
+    for (int q = 0; q < NPL / 2; ++q) {
+        const int n = g * NPL + 2 * q;
+        h[q] = pack2(n < N ? src[n] : 0.f, n + 1 < N ? src[n + 1] : 0.f);
+    }
+}
+template <int NPL, int G>
+__device__ __forceinline__ void write_state(float* dst, int N, int g, const f32x2 (&h)[NPL / 2]) {
+#pragma unroll
+    for (int q = 0; q < NPL / 2; ++q) {
+        float v0, v1;
+        unpack2(h[q], v0, v1);
+        const int n = g * NPL + 2 * q;
+        if (n < N) dst[n] = v0;
+        if (n + 1 < N) dst[n + 1] = v1;
+    }
+}
+
 // =========================================================================
 // Tensor-map (TMA) path
 // =========================================================================
@@ -650,6 +671,58 @@ __device__ __forceinline__ void recurrence_multi(const float4* sdu, const float*
     }
 }
 
+// State-only recurrence over one chunk (no C, no partial sums): the summary
+// pass of a segmented scan needs only the state at the end of the segment.
+template <int NPL, int G, int CH, int T>
+__device__ __forceinline__ void recurrence_state(const float4* sdu, const float* sB,
+                                                 f32x2 (&h)[NPL / 2], const f32x2 (&A2)[NPL / 2],
+                                                 int c, int g, int tlen) {
+    constexpr int NQ = NPL / 4, NP = NPL * G;
+    const ulonglong2* du2 = reinterpret_cast<const ulonglong2*>(sdu);
+    const ulonglong2* b2 = reinterpret_cast<const ulonglong2*>(sB) + g * NQ;
+    struct Step {
+        ulonglong2 sd;
+        f32x2 a[2 * NQ];
+        ulonglong2 bq[NQ];
+    };
+    auto fetch = [&](int t, Step& st) {
+        st.sd = du2[t * CH + du_col<CH>(t, c)];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) st.bq[q] = b2[t * (NP / 4) + q];
+#pragma unroll
+        for (int q = 0; q < 2 * NQ; ++q) {
+            float x0, x1;
+            unpack2(mul2(st.sd.x, A2[q]), x0, x1);
+            st.a[q] = pack2(ex2_approx(x0), ex2_approx(x1));
+        }
+    };
+    auto update = [&](const Step& st) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            h[2 * q] = fma2(st.a[2 * q], h[2 * q], mul2(st.sd.y, st.bq[q].x));
+            h[2 * q + 1] = fma2(st.a[2 * q + 1], h[2 * q + 1], mul2(st.sd.y, st.bq[q].y));
+        }
+    };
+    Step cur;
+    fetch(0, cur);
+    if (tlen == T) {
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+            Step nxt;
+            if (t + 1 < T) fetch(t + 1, nxt);
+            update(cur);
+            if (t + 1 < T) cur = nxt;
+        }
+    } else {
+        for (int t = 0; t < tlen; ++t) {
+            Step nxt;
+            if (t + 1 < tlen) fetch(t + 1, nxt);
+            update(cur);
+            if (t + 1 < tlen) cur = nxt;
+        }
+    }
+}
+
 __device__ __forceinline__ void named_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
@@ -660,12 +733,21 @@ constexpr int kBarReady = 1;  // + (chunk & 1): prologue of the chunk written
 constexpr int kBarDone = 3;   // + (chunk & 1): recurrence of the chunk done
 constexpr int kBarElem = 5;   // element warps only
 
-template <typename io_t, int P, int NPL, int G, int NR, int NE, int MINB>
+// MODE kScanFull: the scan of a whole sequence (sg.nseg == 1) or, in a
+//   segmented scan, of segment s of every chain, starting from the state that
+//   the carry pass left in sg.hcarry.
+// MODE kScanSummary: segment s < nseg - 1 of a segmented scan from a zero
+//   state, writing only the state at its end and the sum of its dt (no y).
+constexpr int kScanFull = 0, kScanSummary = 1;
+
+template <typename io_t, int P, int NPL, int G, int NR, int NE, int MINB, int MODE>
 __global__ void __launch_bounds__(NR + NE, MINB)
     scan_ws_kernel(const ScanArgs p, const __grid_constant__ CUtensorMap tm_u,
                    const __grid_constant__ CUtensorMap tm_d,
-                   const __grid_constant__ CUtensorMap tm_z, const int dblocks) {
+                   const __grid_constant__ CUtensorMap tm_z, const int dblocks,
+                   const SegArgs sg) {
     using C = WsCfg<io_t, P, NPL, G, NR, NE>;
+    static_assert(MODE == kScanFull || P == 1, "the summary pass uses one chain per thread");
     constexpr int T = C::T, S = C::S, NTH = C::NTH, NP = C::NP, PV = C::PV, CH = C::CH;
     constexpr int SPT = C::SPT;
     using quad_t = typename C::quad_t;
@@ -681,15 +763,21 @@ __global__ void __launch_bounds__(NR + NE, MINB)
     const int L = int(p.seqlen);
     const int64_t dim = p.dim;
     const int N = p.dstate;
-    const int b = blockIdx.x / dblocks;
-    const int64_t d0 = int64_t(blockIdx.x % dblocks) * CH;
+    // blockIdx.x = (b * dblocks + channel block) * grid_nseg + time segment
+    const int tseg = blockIdx.x % sg.grid_nseg;
+    const int cblk = blockIdx.x / sg.grid_nseg;
+    const int b = cblk / dblocks;
+    const int64_t d0 = int64_t(cblk % dblocks) * CH;
+    const int t0 = tseg * sg.seg_len;
+    const int Ls = L - t0 < sg.seg_len ? L - t0 : sg.seg_len;  // steps of this segment
     const int tid = threadIdx.x;
-    const int nchunks = (L + T - 1) / T;
+    const int nchunks = (Ls + T - 1) / T;
     const int row0 = int(int64_t(b) * dim + d0);
-    const bool has_z = p.z != nullptr;
-    const io_t* Bg = static_cast<const io_t*>(p.B) + int64_t(b) * L * N;
-    const io_t* Cg = static_cast<const io_t*>(p.C) + int64_t(b) * L * N;
-    auto chunk_len = [&](int k) { return L - k * T < T ? L - k * T : T; };
+    const bool has_z = MODE == kScanFull && p.z != nullptr;
+    const io_t* Bg = static_cast<const io_t*>(p.B) + (int64_t(b) * L + t0) * N;
+    const io_t* Cg = static_cast<const io_t*>(p.C) + (int64_t(b) * L + t0) * N;
+    auto chunk_len = [&](int k) { return Ls - k * T < T ? Ls - k * T : T; };
+    const int nc = sg.nseg - 1;  // carried states per chain
 
     // Each element warp w owns chains [w * CW, (w + 1) * CW) of the CTA and
     // copies its own rows of the u / delta / z tiles; warp 0 also copies B and
@@ -703,9 +791,9 @@ __global__ void __launch_bounds__(NR + NE, MINB)
         uint64_t* br = &bar[(k & (S - 1)) * 2 + w];
         unsigned char* st = stage(k) + w * rows_bytes;
         mbar_arrive_expect_tx(br, (has_z ? 3 : 2) * rows_bytes + bc_bytes);
-        tma_load_2d(st, &tm_u, k * T, row0 + w * CW, br);
-        tma_load_2d(st + C::kTile, &tm_d, k * T, row0 + w * CW, br);
-        if (has_z) tma_load_2d(st + 2 * C::kTile, &tm_z, k * T, row0 + w * CW, br);
+        tma_load_2d(st, &tm_u, t0 + k * T, row0 + w * CW, br);
+        tma_load_2d(st + C::kTile, &tm_d, t0 + k * T, row0 + w * CW, br);
+        if (has_z) tma_load_2d(st + 2 * C::kTile, &tm_z, t0 + k * T, row0 + w * CW, br);
         bulk_g2s(raw(k, w), (w == 0 ? Bg : Cg) + int64_t(k) * T * N, bc_bytes, br);
     };
 
@@ -724,11 +812,16 @@ __global__ void __launch_bounds__(NR + NE, MINB)
         for (int q = 0; q < P; ++q) {
             cc[q] = grp + q * C::NGRP;
             init_state<NPL, G>(p, d0 + cc[q], d0 + cc[q] < dim, g, A2[q], h[q]);
+            if (MODE == kScanFull && tseg > 0 && d0 + cc[q] < dim)
+                load_state<NPL, G>(sg.hcarry + ((int64_t(b) * dim + d0 + cc[q]) * nc + tseg - 1) * N,
+                                   N, g, h[q]);
         }
         for (int k = 0; k < nchunks; ++k) {
             named_sync(kBarReady + (k & 1), NTH);
             const float* sB = bcbuf(k);
-            if constexpr (P == 1) {
+            if constexpr (MODE == kScanSummary) {
+                recurrence_state<NPL, G, CH, T>(dubuf(k), sB, h[0], A2[0], cc[0], g, chunk_len(k));
+            } else if constexpr (P == 1) {
                 recurrence<NPL, G, CH, T>(dubuf(k), sB, sB + T * NP, ybuf(k), h[0], A2[0], cc[0],
                                           g, tid, chunk_len(k));
             } else {
@@ -738,9 +831,14 @@ __global__ void __launch_bounds__(NR + NE, MINB)
             named_arrive(kBarDone + (k & 1), NTH);
         }
 #pragma unroll
-        for (int q = 0; q < P; ++q)
-            if (d0 + cc[q] < dim && p.last_state)
-                store_state<NPL, G>(p, int64_t(b) * dim + d0 + cc[q], g, h[q]);
+        for (int q = 0; q < P; ++q) {
+            if (d0 + cc[q] >= dim) continue;
+            const int64_t chain = int64_t(b) * dim + d0 + cc[q];
+            if (MODE == kScanSummary)
+                write_state<NPL, G>(sg.hcarry + (chain * nc + tseg) * N, N, g, h[q]);
+            else if (p.last_state && tseg == sg.nseg - 1)
+                store_state<NPL, G>(p, chain, g, h[q]);
+        }
         return;
     }
 
@@ -770,7 +868,7 @@ __global__ void __launch_bounds__(NR + NE, MINB)
         dub[i] = seg * PV * CH + (ec[i] ^ ((2 * seg) & (CH - 1)));  // du_col of steps 4*seg..+3
 #pragma unroll
         for (int gg = 0; gg < G; ++gg) yu[i][gg] = yunit<ROWS>(seg, ec[i] * G + gg);
-        yg[i] = static_cast<io_t*>(p.y) + (int64_t(b) * dim + dd) * L + seg * PV;
+        yg[i] = static_cast<io_t*>(p.y) + (int64_t(b) * dim + dd) * L + t0 + seg * PV;
     }
     const bool all_chains = d0 + CH <= dim;
     if (lane == 0) {
@@ -779,8 +877,12 @@ __global__ void __launch_bounds__(NR + NE, MINB)
     }
     __syncwarp();
 
+    float dtsum[SPT];  // summary pass: sum of dt over the segment
+#pragma unroll
+    for (int i = 0; i < SPT; ++i) dtsum[i] = 0.f;
     // ke: chunk to finish (or -1), kp: chunk to prepare (or -1)
     auto pass = [&](int ke, int kp) {
+        if (MODE == kScanSummary) ke = -1;
         // ---- loads ----
         ulonglong2 ps[SPT][G];
         quad_t eu[SPT], ez[SPT], pd[SPT], pu[SPT];
@@ -862,6 +964,12 @@ __global__ void __launch_bounds__(NR + NE, MINB)
                     for (int e = 0; e < PV; ++e)
                         if (!chain_ok[i] || seg * PV + e >= tl) o[i][e] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
+            if (MODE == kScanSummary) {
+#pragma unroll
+                for (int i = 0; i < SPT; ++i)
+#pragma unroll
+                    for (int e = 0; e < PV; ++e) dtsum[i] += o[i][e].x;
+            }
             float4* sdu = dubuf(kp);
 #pragma unroll
             for (int i = 0; i < SPT; ++i)
@@ -883,7 +991,7 @@ __global__ void __launch_bounds__(NR + NE, MINB)
         }
     };
 
-    if (nchunks == 0) return;
+    if (nchunks == 0) return;  // (a segment is never empty; only a whole empty sequence)
     pass(-1, 0);
     named_arrive(kBarReady + 0, NTH);
     if (nchunks > 1) {
@@ -900,6 +1008,17 @@ __global__ void __launch_bounds__(NR + NE, MINB)
         if (lane == 0 && j - 1 + S < nchunks) {
             fence_proxy_async_smem();
             issue(j - 1 + S, w);
+        }
+    }
+    if (MODE == kScanSummary) {
+        // the SEGROW lanes of a chain hold its dt sums over disjoint steps
+#pragma unroll
+        for (int i = 0; i < SPT; ++i) {
+#pragma unroll
+            for (int off = 1; off < C::SEGROW; off *= 2)
+                dtsum[i] += __shfl_xor_sync(0xffffffffu, dtsum[i], off);
+            if (seg == 0 && chain_ok[i])
+                sg.sdt[(int64_t(b) * dim + d0 + ec[i]) * nc + tseg] = dtsum[i];
         }
     }
 }
@@ -1571,25 +1690,134 @@ bool try_pair(const ScanArgs& a, cudaStream_t stream, cudaError_t* err) {
 // chain 8x2, 2: single chain 4 states x 4 threads, 3: paired chains) and
 // MAMBA_SCAN_PATH=reg forces the register-prefetch kernel; every choice
 // computes the same recurrence, and the tests check them against each other.
-template <typename io_t, int P, int NPL, int G, int NR, int NE, int MINB>
-bool try_ws(const ScanArgs& a, cudaStream_t stream, cudaError_t* err) {
+template <typename io_t, int P, int NPL, int G, int NR, int NE>
+bool ws_ok(const ScanArgs& a) {
     using C = WsCfg<io_t, P, NPL, G, NR, NE>;
     const int64_t es = sizeof(io_t);
-    const bool ok = a.dstate == C::NP && al16(a.u) && al16(a.delta) && al16(a.z) && al16(a.B) &&
-                    al16(a.C) && (reinterpret_cast<uintptr_t>(a.y) % (C::PV * es)) == 0 &&
-                    (a.seqlen * es) % 16 == 0 && a.batch * a.dim <= 0x7fffffff &&
-                    a.seqlen <= 0x7fffffff;
-    if (!ok) return false;
+    return a.dstate == C::NP && al16(a.u) && al16(a.delta) && al16(a.z) && al16(a.B) &&
+           al16(a.C) && (reinterpret_cast<uintptr_t>(a.y) % (C::PV * es)) == 0 &&
+           (a.seqlen * es) % 16 == 0 && a.batch * a.dim <= 0x7fffffff &&
+           a.seqlen <= 0x7fffffff;
+}
+
+template <typename io_t, int P, int NPL, int G, int NR, int NE, int MINB, int MODE>
+cudaError_t launch_ws(const ScanArgs& a, const SegArgs& sg, cudaStream_t stream) {
+    using C = WsCfg<io_t, P, NPL, G, NR, NE>;
     CUtensorMap mu, md, mz;
     const bool bf = sizeof(io_t) == 2;
     const int64_t rows = a.batch * a.dim;
     if (!make_map(&mu, a.u, bf, rows, a.seqlen, C::T, C::CW) ||
         !make_map(&md, a.delta, bf, rows, a.seqlen, C::T, C::CW) ||
         !make_map(&mz, a.z ? a.z : a.u, bf, rows, a.seqlen, C::T, C::CW))
-        return false;
+        return cudaErrorInvalidValue;
     const int64_t dblocks = (a.dim + C::CH - 1) / C::CH;
-    *err = launch(scan_ws_kernel<io_t, P, NPL, G, NR, NE, MINB>, C::kSmem, dblocks * a.batch,
-                  C::NTH, stream, a, mu, md, mz, int(dblocks));
+    return launch(scan_ws_kernel<io_t, P, NPL, G, NR, NE, MINB, MODE>, C::kSmem,
+                  dblocks * a.batch * sg.grid_nseg, C::NTH, stream, a, mu, md, mz, int(dblocks),
+                  sg);
+}
+
+template <typename io_t, int P, int NPL, int G, int NR, int NE, int MINB>
+bool try_ws(const ScanArgs& a, cudaStream_t stream, cudaError_t* err) {
+    if (!ws_ok<io_t, P, NPL, G, NR, NE>(a) || a.seqlen == 0) return false;
+    const SegArgs whole{int(a.seqlen), 1, 1, nullptr, nullptr};
+    *err = launch_ws<io_t, P, NPL, G, NR, NE, MINB, kScanFull>(a, whole, stream);
+    return *err != cudaErrorInvalidValue;  // tensor map refused: another path
+}
+
+// Carry pass of a segmented scan.  For chain c and state n the state entering
+// segment s + 1 is exp(A_n * sum of dt over s) times the state entering s, plus
+// the end state of s from a zero start (the product of the per-step decays
+// exp(dt_t A_n) over a segment is exp(A_n * sum dt_t)).  Overwrites hcarry[c][s]
+// with the state entering segment s + 1.
+__global__ void __launch_bounds__(256) scan_carry_kernel(const float* A_log, SegArgs sg,
+                                                         int64_t chains, int64_t dim, int N) {
+    const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= chains * N) return;
+    const int64_t chain = idx / N, d = chain % dim;
+    const int n = int(idx % N);
+    const float A2 = -expf(__ldg(A_log + d * N + n)) * kLog2e;
+    const int nc = sg.nseg - 1;
+    float h = 0.f;
+    for (int s = 0; s < nc; ++s) {
+        float* slot = sg.hcarry + (chain * nc + s) * N + n;
+        h = fmaf(ex2_approx(A2 * sg.sdt[chain * nc + s]), h, *slot);
+        *slot = h;
+    }
+}
+
+// Segments for a scan of few chains.  Splitting costs a summary pass over all
+// but the last segment, so it pays only when the unsplit grid leaves at least
+// half of the SMs idle; then about 8 CTAs of the dstate-16 tile per SM (two
+// waves), each segment at least 512 steps (32 chunks).  Measured on B300 at
+// dstate 16: 48 CTAs x L=131072 5.48 -> 1.83 ms (24 segments), 32 CTAs x
+// L=32768 1.39 -> 0.42 ms, while 128 CTAs run faster unsplit.
+// MAMBA_SCAN_SEGMENTS=n forces n segments (tests).  Returns 1 for no split.
+int plan_segments(const ScanArgs& a, int chains_per_cta, int* seg_len) {
+    const int64_t L = a.seqlen;
+    const int64_t ctas = a.batch * ((a.dim + chains_per_cta - 1) / chains_per_cta);
+    int64_t nseg = env_int("MAMBA_SCAN_SEGMENTS");
+    if (nseg <= 0) {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sms <= 0)
+            return 1;
+        if (2 * ctas > sms) return 1;
+        nseg = (8 * int64_t(sms)) / ctas;
+        const int64_t by_len = L / 512;
+        if (nseg > by_len) nseg = by_len;
+    }
+    const int64_t max_seg = (L + 15) / 16;
+    if (nseg > max_seg) nseg = max_seg;
+    if (nseg < 2) return 1;
+    const int64_t len = ((L + nseg - 1) / nseg + 15) / 16 * 16;
+    *seg_len = int(len);
+    return int((L + len - 1) / len);
+}
+
+template <typename io_t>
+bool try_ws_split(const ScanArgs& a, cudaStream_t stream, const ScanScratch& sc,
+                  cudaError_t* err) {
+    using C = WsCfg<io_t, 1, 8, 2, 64, 64>;
+    if (!ws_ok<io_t, 1, 8, 2, 64, 64>(a) || a.seqlen == 0) return false;
+    int seg_len = 0;
+    const int nseg = plan_segments(a, C::CH, &seg_len);
+    if (nseg < 2) return false;
+    const int64_t chains = a.batch * a.dim;
+    auto rnd = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t hbytes = rnd(size_t(chains) * (nseg - 1) * a.dstate * sizeof(float));
+    const size_t bytes = hbytes + rnd(size_t(chains) * (nseg - 1) * sizeof(float));
+    void* buf = sc.ptr;
+    bool owned = false;
+    if (buf) {
+        if (bytes > sc.bytes) {
+            *err = cudaErrorMemoryAllocation;
+            return true;
+        }
+    } else {
+        if (!sc.may_alloc || cudaMallocAsync(&buf, bytes, stream) != cudaSuccess) {
+            cudaGetLastError();  // clear a failed allocation; run unsplit
+            return false;
+        }
+        owned = true;
+    }
+    SegArgs sg{seg_len, nseg, nseg - 1, static_cast<float*>(buf),
+               reinterpret_cast<float*>(static_cast<char*>(buf) + hbytes)};
+    *err = launch_ws<io_t, 1, 8, 2, 64, 64, 4, kScanSummary>(a, sg, stream);
+    if (*err == cudaSuccess) {
+        const int64_t threads = chains * a.dstate;
+        scan_carry_kernel<<<unsigned((threads + 255) / 256), 256, 0, stream>>>(
+            a.A_log, sg, chains, a.dim, a.dstate);
+        *err = cudaGetLastError();
+    }
+    if (*err == cudaSuccess) {
+        sg.grid_nseg = nseg;
+        *err = launch_ws<io_t, 1, 8, 2, 64, 64, 4, kScanFull>(a, sg, stream);
+    }
+    if (owned) {
+        const cudaError_t ferr = cudaFreeAsync(buf, stream);
+        if (*err == cudaSuccess) *err = ferr;
+    }
     return true;
 }
 
@@ -1622,7 +1850,7 @@ cudaError_t run(const ScanArgs& a, cudaStream_t stream, bool pair_first) {
 }
 
 template <typename io_t>
-cudaError_t dispatch(const ScanArgs& a, cudaStream_t stream) {
+cudaError_t dispatch(const ScanArgs& a, cudaStream_t stream, const ScanScratch& sc) {
     const int N = a.dstate;
     const int tile = env_int("MAMBA_SCAN_TILE");
     const bool pair = tile == 3 || (tile == 0 && N != 16);
@@ -1632,7 +1860,11 @@ cudaError_t dispatch(const ScanArgs& a, cudaStream_t stream) {
         // Few chains (long sequences, small batch): more threads per chain.
         const bool few = a.batch * a.dim < 148 * 64;
         cudaError_t err = cudaSuccess;
-        if ((tile == 4 || (tile == 0 && !few)) && N == 16 && !force_reg() &&
+        // Few chains and a long sequence: split the sequence (see try_ws_split).
+        if ((tile == 0 || tile == 4) && N == 16 && !force_reg() &&
+            try_ws_split<io_t>(a, stream, sc, &err))
+            return err;
+        if ((tile == 4 || tile == 0) && N == 16 && !force_reg() &&
             try_ws<io_t, 1, 8, 2, 64, 64, 4>(a, stream, &err))
             return err;
         if (tile == 5 && N == 16 && !force_reg() && try_ws<io_t, 2, 8, 2, 64, 64, 2>(a, stream, &err))
@@ -1641,7 +1873,9 @@ cudaError_t dispatch(const ScanArgs& a, cudaStream_t stream) {
             return err;
         if (tile == 7 && N == 16 && !force_reg() && try_ws<io_t, 1, 4, 4, 128, 64, 4>(a, stream, &err))
             return err;
-        if (tile == 2 || (tile == 0 && few)) return run<io_t, 4, 4, 16, 32>(a, stream, false);
+        // dstate 16 falls back to the 8-state x 2-lane arrangement of the tile
+        // above, so that both sum C.h in the same order.
+        if (tile == 2 || (tile == 0 && few && N != 16)) return run<io_t, 4, 4, 16, 32>(a, stream, false);
         return run<io_t, 8, 2, 32, 16>(a, stream, pair);
     }
     if (N <= 32) return run<io_t, 4, 8, 8, 32>(a, stream, pair);
@@ -1652,8 +1886,9 @@ cudaError_t dispatch(const ScanArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_scan_fwd(const ScanArgs& a, bool bf16, cudaStream_t stream) {
-    return bf16 ? dispatch<__nv_bfloat16>(a, stream) : dispatch<float>(a, stream);
+cudaError_t launch_scan_fwd(const ScanArgs& a, bool bf16, cudaStream_t stream,
+                            const ScanScratch& sc) {
+    return bf16 ? dispatch<__nv_bfloat16>(a, stream, sc) : dispatch<float>(a, stream, sc);
 }
 
 cudaError_t read_and_clear_device_error(unsigned int* word, cudaStream_t stream) {

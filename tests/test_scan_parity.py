@@ -204,3 +204,32 @@ def test_register_path_matches_tensor_map_path(cuda, io, N, monkeypatch):
     yr, hr = oracle_scan(x)
     _assert_close(x, y0, h0, yr, hr, what="tma path")
     _assert_close(x, y1, h1, yr, hr, what="register path")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("batch,dim,L,nseg", [(2, 40, 1000, 2), (1, 70, 2048, 3), (2, 33, 1504, 7),
+                                              (1, 32, 4096, 16)])
+def test_segmented_scan_matches_oracle(cuda, io, batch, dim, L, nseg, monkeypatch):
+    """A sequence split along time (summary pass, carry pass, full pass) must
+    give the oracle's scan, ragged last segment and partial CTAs included, and
+    agree with the unsplit kernel."""
+    x = workloads.make_scan_inputs(batch, dim, L, 16, io, seed=18 + nseg, d_mode="normal")
+    yr, hr = oracle_scan(x)
+    monkeypatch.setenv("MAMBA_SCAN_SEGMENTS", "1")
+    y1, h1 = _run(x, cuda)
+    monkeypatch.setenv("MAMBA_SCAN_SEGMENTS", str(nseg))
+    ys, hs = _run(x, cuda)
+    _assert_close(x, ys, hs, yr, hr, what=f"{nseg} segments")
+    _assert_close(x, y1, h1, yr, hr, what="unsplit")
+    assert rel_err(ys, y1) <= TOL[io] and rel_err(hs, h1) <= TOL[io]
+
+
+def test_segmented_scan_without_softplus_and_optional_inputs(cuda, monkeypatch):
+    x = workloads.make_scan_inputs(1, 50, 1200, 16, "bf16", seed=23, d_mode="normal",
+                                   with_z=False, with_D=False, with_bias=False)
+    x["delta"] = (x["delta"].float().abs() * 0.05).to(x["delta"].dtype)
+    x["softplus"] = False
+    monkeypatch.setenv("MAMBA_SCAN_SEGMENTS", "5")
+    yg, hg = _run(x, cuda)
+    yr, hr = oracle_scan(x)
+    _assert_close(x, yg, hg, yr, hr, what="segmented, no z/D/bias, softplus off")
