@@ -27,7 +27,7 @@
  * Conventions shared by every entry point
  *   - All pointers are DEVICE pointers owned by the caller.  Arrays are dense
  *     row-major with the shapes given below.  The library keeps no state
- *     between calls and allocates no memory.
+ *     between calls.  Only mamba_selective_scan_fwd may allocate: see there.
  *   - io_dtype (MAMBA_F32 or MAMBA_BF16) is the element type of every
  *     "io" array (u, delta, z, B, C, y; x, dt, z, B, C, out for decode).
  *     A_log, D, the bias and the state are always fp32.  Arithmetic is fp32;
@@ -89,6 +89,15 @@ typedef enum {
  *
  * batch, dim, seqlen may be zero (nothing to compute; last_state is still
  * zeroed when seqlen == 0).  Returns MAMBA_OK or an error code as above.
+ *
+ * Long sequences of few chains (a grid that would leave at least half of the
+ * SMs idle) are split along time: a summary pass per segment, a carry pass
+ * and the full pass, the three launched on `stream`.  The carried states
+ * (batch * dim * (segments - 1) * (dstate + 1) fp32 values, at most about
+ * 256 * SMs * (dstate + 1) * 4 bytes) live in stream-ordered scratch taken
+ * with cudaMallocAsync and returned with cudaFreeAsync on `stream`, so calls
+ * on different streams never share it.  If that allocation fails the scan
+ * runs unsplit.  Results of a split and an unsplit scan agree to rounding.
  */
 int mamba_selective_scan_fwd(const void *u, const void *delta, const float *A_log,
                              const void *B, const void *C, const float *D, const void *z,
