@@ -27,7 +27,8 @@
  * Conventions shared by every entry point
  *   - All pointers are DEVICE pointers owned by the caller.  Arrays are dense
  *     row-major with the shapes given below.  The library keeps no state
- *     between calls.  Only mamba_selective_scan_fwd may allocate: see there.
+ *     between calls.  Only mamba_selective_scan_fwd may allocate: see there
+ *     and mamba_selective_scan_fwd_noalloc.
  *   - io_dtype (MAMBA_F32 or MAMBA_BF16) is the element type of every
  *     "io" array (u, delta, z, B, C, y; x, dt, z, B, C, out for decode).
  *     A_log, D, the bias and the state are always fp32.  Arithmetic is fp32;
@@ -68,7 +69,8 @@ typedef enum {
     MAMBA_ERR_DTYPE = 5,   /* io_dtype is not a mamba_dtype_t                    */
     MAMBA_ERR_LAUNCH = 6,  /* the CUDA launch failed (see cudaGetLastError)      */
     MAMBA_ERR_TIMEOUT = 7, /* reserved: a bounded device-side wait gave up       */
-    MAMBA_ERR_ALIAS = 8    /* an output overlaps an input                        */
+    MAMBA_ERR_ALIAS = 8,   /* an output overlaps an input                        */
+    MAMBA_ERR_SCRATCH = 9  /* _noalloc: the split needs more than its fixed scratch */
 } mamba_status_t;
 
 #define MAMBA_MAX_DSTATE 256
@@ -104,6 +106,35 @@ int mamba_selective_scan_fwd(const void *u, const void *delta, const float *A_lo
                              const float *delta_bias, int softplus_flag, void *y,
                              float *last_state, int64_t batch, int64_t dim, int64_t seqlen,
                              int64_t dstate, int io_dtype, mamba_stream_t stream);
+
+/*
+ * mamba_selective_scan_fwd without any allocation.  This entry point has no
+ * counterpart in the pages: it exists for callers that must not allocate
+ * (CUDA graph capture without memory nodes, no allocator at hand).
+ *
+ * Same arguments, same operation and same results as mamba_selective_scan_fwd
+ * (bit for bit: the same kernels run with the same split).  When the scan is
+ * split along time, the carried states live in a fixed device buffer of this
+ * library (4 MiB per device, a static __device__ array) instead of
+ * stream-ordered scratch:
+ *   - The buffer's address is looked up once per device (cudaGetSymbolAddress)
+ *     by the first call on that device.  Make that first call before any
+ *     stream capture; it may also be where the driver loads this library's
+ *     module on that device.  A failed look-up returns MAMBA_ERR_LAUNCH.
+ *   - A split that needs more than 4 MiB (possible only when a test forces
+ *     more segments than the planner would choose) returns MAMBA_ERR_SCRATCH
+ *     before anything is launched.
+ *   - Nothing in the buffer has to start at zero.
+ *   - Calls that overlap in time on one device (other streams, other host
+ *     threads, or graphs replayed concurrently) share the buffer and race.
+ *     Calls ordered on one stream are safe.
+ */
+int mamba_selective_scan_fwd_noalloc(const void *u, const void *delta, const float *A_log,
+                                     const void *B, const void *C, const float *D,
+                                     const void *z, const float *delta_bias, int softplus_flag,
+                                     void *y, float *last_state, int64_t batch, int64_t dim,
+                                     int64_t seqlen, int64_t dstate, int io_dtype,
+                                     mamba_stream_t stream);
 
 /*
  * Single-token decode step (recurrent inference: each new token touches only

@@ -19,12 +19,13 @@ LIB_PATH = os.path.join(PKG, "libmamba_scan.so")
 MAMBA_F32, MAMBA_BF16 = 0, 1
 STATUS = {0: "MAMBA_OK", 1: "MAMBA_ERR_NULL", 2: "MAMBA_ERR_SIZE", 3: "MAMBA_ERR_DSTATE",
           4: "MAMBA_ERR_ALIGN", 5: "MAMBA_ERR_DTYPE", 6: "MAMBA_ERR_LAUNCH",
-          7: "MAMBA_ERR_TIMEOUT", 8: "MAMBA_ERR_ALIAS"}
+          7: "MAMBA_ERR_TIMEOUT", 8: "MAMBA_ERR_ALIAS", 9: "MAMBA_ERR_SCRATCH"}
 MAX_DSTATE = 256
 
 # Every symbol include/mamba_scan.h declares.
-EXPORTED = ("mamba_selective_scan_fwd", "mamba_selective_state_update", "mamba_device_status",
-            "mamba_status_string", "mamba_abi_version")
+EXPORTED = ("mamba_selective_scan_fwd", "mamba_selective_scan_fwd_noalloc",
+            "mamba_selective_state_update", "mamba_device_status", "mamba_status_string",
+            "mamba_abi_version")
 
 _lib = None
 
@@ -37,9 +38,10 @@ class MambaError(RuntimeError):
 
 def _declare(lib):
     vp, fp, i64, ci = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
-    lib.mamba_selective_scan_fwd.restype = ci
-    lib.mamba_selective_scan_fwd.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, vp, fp,
-                                             i64, i64, i64, i64, ci, vp]
+    for name in ("mamba_selective_scan_fwd", "mamba_selective_scan_fwd_noalloc"):
+        getattr(lib, name).restype = ci
+        getattr(lib, name).argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, vp, fp,
+                                       i64, i64, i64, i64, ci, vp]
     lib.mamba_selective_state_update.restype = ci
     lib.mamba_selective_state_update.argtypes = [fp, vp, vp, fp, vp, vp, fp, vp, fp, ci, vp,
                                                  i64, i64, i64, ci, vp]
@@ -120,6 +122,24 @@ def mamba_selective_scan_fwd(u, delta, A_log, B, C, D=None, z=None, delta_bias=N
     (``last_state`` only if ``want_last_state``).  Runs on ``stream`` (default:
     the current stream) and does not synchronise.
     """
+    return _scan_fwd("mamba_selective_scan_fwd", u, delta, A_log, B, C, D, z, delta_bias,
+                     softplus, y, last_state, want_last_state, stream)
+
+
+def mamba_selective_scan_fwd_noalloc(u, delta, A_log, B, C, D=None, z=None, delta_bias=None,
+                                     softplus=True, y=None, last_state=None,
+                                     want_last_state=True, stream=None):
+    """``mamba_selective_scan_fwd`` through the C entry point that never
+    allocates (a split keeps its carried states in the library's fixed 4 MiB
+    device buffer; calls overlapping in time race on it).  ``y`` and
+    ``last_state`` are allocated here by PyTorch when not given, so pass them
+    in to keep the whole call free of allocation."""
+    return _scan_fwd("mamba_selective_scan_fwd_noalloc", u, delta, A_log, B, C, D, z, delta_bias,
+                     softplus, y, last_state, want_last_state, stream)
+
+
+def _scan_fwd(entry, u, delta, A_log, B, C, D, z, delta_bias, softplus, y, last_state,
+              want_last_state, stream):
     dev = u.device
     batch, dim, seqlen = u.shape
     dstate = A_log.shape[-1]
@@ -133,12 +153,12 @@ def mamba_selective_scan_fwd(u, delta, A_log, B, C, D=None, z=None, delta_bias=N
         y = torch.empty_like(u)
     if last_state is None and want_last_state:
         last_state = torch.empty((batch, dim, dstate), device=dev, dtype=torch.float32)
-    rc = load().mamba_selective_scan_fwd(
+    rc = getattr(load(), entry)(
         _ptr(u), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
         int(bool(softplus)), _ptr(y), _ptr(last_state), batch, dim, seqlen, dstate, io,
         _stream(stream, dev))
     if rc != 0:
-        raise MambaError(rc, "mamba_selective_scan_fwd")
+        raise MambaError(rc, entry)
     return y, last_state
 
 
@@ -179,6 +199,14 @@ def raw_scan_fwd(u, delta, A_log, B, C, D, z, delta_bias, softplus_flag, y, last
     return load().mamba_selective_scan_fwd(u, delta, A_log, B, C, D, z, delta_bias,
                                            softplus_flag, y, last_state, batch, dim, seqlen,
                                            dstate, io_dtype, stream)
+
+
+def raw_scan_fwd_noalloc(u, delta, A_log, B, C, D, z, delta_bias, softplus_flag, y, last_state,
+                         batch, dim, seqlen, dstate, io_dtype, stream) -> int:
+    """``mamba_selective_scan_fwd_noalloc`` with plain integers as pointers."""
+    return load().mamba_selective_scan_fwd_noalloc(u, delta, A_log, B, C, D, z, delta_bias,
+                                                   softplus_flag, y, last_state, batch, dim,
+                                                   seqlen, dstate, io_dtype, stream)
 
 
 def raw_state_update(state, x, dt, A_log, B, C, D, z, dt_bias, softplus_flag, out, batch, dim,

@@ -1,5 +1,7 @@
 // C entry points of libmamba_scan.so: argument validation, then one launch.
 // The declarations, layouts and error conventions are in include/mamba_scan.h.
+#include <mutex>
+
 #include "../../include/mamba_scan.h"
 #include "common.cuh"
 
@@ -34,32 +36,35 @@ bool size_ok(int64_t a, int64_t b, int64_t c) {
     return a * b <= kMaxElems / c;
 }
 
-}  // namespace
+// Scratch of mamba_selective_scan_fwd_noalloc: a fixed device buffer in this
+// library's module (one copy per device), found once per device with
+// cudaGetSymbolAddress.  A split needs at most about 256 * SMs * (dstate + 1)
+// * 4 bytes (2.6 MB at dstate 16 on 148 SMs); 4 MiB covers that.
+constexpr size_t kNoallocScratchBytes = size_t(4) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-extern "C" {
+constexpr int kMaxDevices = 64;
+std::once_flag g_scratch_once[kMaxDevices];
+void* g_scratch_addr[kMaxDevices];
+cudaError_t g_scratch_err[kMaxDevices];
 
-int mamba_abi_version(void) { return 1 * 10000 + 0 * 100 + 0; }
-
-const char* mamba_status_string(int status) {
-    switch (status) {
-        case MAMBA_OK: return "MAMBA_OK";
-        case MAMBA_ERR_NULL: return "MAMBA_ERR_NULL: a required pointer is NULL";
-        case MAMBA_ERR_SIZE: return "MAMBA_ERR_SIZE: a size is negative or too large";
-        case MAMBA_ERR_DSTATE: return "MAMBA_ERR_DSTATE: dstate must be in [1, 256]";
-        case MAMBA_ERR_ALIGN: return "MAMBA_ERR_ALIGN: a pointer is not aligned to its element size";
-        case MAMBA_ERR_DTYPE: return "MAMBA_ERR_DTYPE: io_dtype must be MAMBA_F32 or MAMBA_BF16";
-        case MAMBA_ERR_LAUNCH: return "MAMBA_ERR_LAUNCH: the CUDA launch failed";
-        case MAMBA_ERR_TIMEOUT: return "MAMBA_ERR_TIMEOUT: a bounded device-side wait gave up";
-        case MAMBA_ERR_ALIAS: return "MAMBA_ERR_ALIAS: an output overlaps an input";
-        default: return "unknown mamba_status_t";
-    }
+cudaError_t noalloc_scratch(void** out) {
+    int dev = 0;
+    const cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::call_once(g_scratch_once[dev], [dev] {
+        g_scratch_err[dev] = cudaGetSymbolAddress(&g_scratch_addr[dev], g_noalloc_scratch);
+    });
+    *out = g_scratch_addr[dev];
+    return g_scratch_err[dev];
 }
 
-int mamba_selective_scan_fwd(const void* u, const void* delta, const float* A_log, const void* B,
-                             const void* C, const float* D, const void* z,
-                             const float* delta_bias, int softplus_flag, void* y,
-                             float* last_state, int64_t batch, int64_t dim, int64_t seqlen,
-                             int64_t dstate, int io_dtype, mamba_stream_t stream) {
+// Argument checks of the forward scan: MAMBA_OK to go on, else the status.
+int check_scan_args(const void* u, const void* delta, const float* A_log, const void* B,
+                    const void* C, const float* D, const void* z, const float* delta_bias,
+                    void* y, float* last_state, int64_t batch, int64_t dim, int64_t seqlen,
+                    int64_t dstate, int io_dtype) {
     if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
     if (dstate < 1 || dstate > MAMBA_MAX_DSTATE) return MAMBA_ERR_DSTATE;
     if (!size_ok(batch, dim, seqlen) || !size_ok(batch, seqlen, dstate) ||
@@ -87,6 +92,41 @@ int mamba_selective_scan_fwd(const void* u, const void* delta, const float* A_lo
     for (const Range& r : ins)
         if (overlaps(ry, r) || overlaps(rs, r)) return MAMBA_ERR_ALIAS;
     if (overlaps(ry, rs)) return MAMBA_ERR_ALIAS;
+    return MAMBA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mamba_abi_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+const char* mamba_status_string(int status) {
+    switch (status) {
+        case MAMBA_OK: return "MAMBA_OK";
+        case MAMBA_ERR_NULL: return "MAMBA_ERR_NULL: a required pointer is NULL";
+        case MAMBA_ERR_SIZE: return "MAMBA_ERR_SIZE: a size is negative or too large";
+        case MAMBA_ERR_DSTATE: return "MAMBA_ERR_DSTATE: dstate must be in [1, 256]";
+        case MAMBA_ERR_ALIGN: return "MAMBA_ERR_ALIGN: a pointer is not aligned to its element size";
+        case MAMBA_ERR_DTYPE: return "MAMBA_ERR_DTYPE: io_dtype must be MAMBA_F32 or MAMBA_BF16";
+        case MAMBA_ERR_LAUNCH: return "MAMBA_ERR_LAUNCH: the CUDA launch failed";
+        case MAMBA_ERR_TIMEOUT: return "MAMBA_ERR_TIMEOUT: a bounded device-side wait gave up";
+        case MAMBA_ERR_ALIAS: return "MAMBA_ERR_ALIAS: an output overlaps an input";
+        case MAMBA_ERR_SCRATCH:
+            return "MAMBA_ERR_SCRATCH: the split needs more than the 4 MiB fixed scratch of "
+                   "mamba_selective_scan_fwd_noalloc";
+        default: return "unknown mamba_status_t";
+    }
+}
+
+int mamba_selective_scan_fwd(const void* u, const void* delta, const float* A_log, const void* B,
+                             const void* C, const float* D, const void* z,
+                             const float* delta_bias, int softplus_flag, void* y,
+                             float* last_state, int64_t batch, int64_t dim, int64_t seqlen,
+                             int64_t dstate, int io_dtype, mamba_stream_t stream) {
+    const int st = check_scan_args(u, delta, A_log, B, C, D, z, delta_bias, y, last_state, batch,
+                                   dim, seqlen, dstate, io_dtype);
+    if (st != MAMBA_OK) return st;
     if (batch == 0 || dim == 0) return MAMBA_OK;
 
     mamba::ScanArgs a{u, delta, A_log, B, C, D, z, delta_bias, y, last_state,
@@ -94,6 +134,30 @@ int mamba_selective_scan_fwd(const void* u, const void* delta, const float* A_lo
     const mamba::ScanScratch scratch{nullptr, 0, true};
     const cudaError_t err = mamba::launch_scan_fwd(a, io_dtype == MAMBA_BF16,
                                                    reinterpret_cast<cudaStream_t>(stream), scratch);
+    return err == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
+}
+
+int mamba_selective_scan_fwd_noalloc(const void* u, const void* delta, const float* A_log,
+                                     const void* B, const void* C, const float* D,
+                                     const void* z, const float* delta_bias, int softplus_flag,
+                                     void* y, float* last_state, int64_t batch, int64_t dim,
+                                     int64_t seqlen, int64_t dstate, int io_dtype,
+                                     mamba_stream_t stream) {
+    const int st = check_scan_args(u, delta, A_log, B, C, D, z, delta_bias, y, last_state, batch,
+                                   dim, seqlen, dstate, io_dtype);
+    if (st != MAMBA_OK) return st;
+    if (batch == 0 || dim == 0) return MAMBA_OK;
+
+    void* buf = nullptr;
+    if (noalloc_scratch(&buf) != cudaSuccess) return MAMBA_ERR_LAUNCH;
+    // Nothing in the buffer has to start at zero: the summary pass writes every
+    // carried state and dt sum before the carry pass reads it.
+    mamba::ScanArgs a{u, delta, A_log, B, C, D, z, delta_bias, y, last_state,
+                      batch, dim, seqlen, int(dstate), softplus_flag != 0};
+    const mamba::ScanScratch scratch{buf, kNoallocScratchBytes, false};
+    const cudaError_t err = mamba::launch_scan_fwd(a, io_dtype == MAMBA_BF16,
+                                                   reinterpret_cast<cudaStream_t>(stream), scratch);
+    if (err == cudaErrorMemoryAllocation) return MAMBA_ERR_SCRATCH;
     return err == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
 }
 

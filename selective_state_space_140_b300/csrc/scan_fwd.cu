@@ -731,7 +731,6 @@ __device__ __forceinline__ void named_arrive(int id, int count) {
 }
 constexpr int kBarReady = 1;  // + (chunk & 1): prologue of the chunk written
 constexpr int kBarDone = 3;   // + (chunk & 1): recurrence of the chunk done
-constexpr int kBarElem = 5;   // element warps only
 
 // MODE kScanFull: the scan of a whole sequence (sg.nseg == 1) or, in a
 //   segmented scan, of segment s of every chain, starting from the state that

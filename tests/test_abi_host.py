@@ -127,3 +127,16 @@ def test_binding_refuses_missing_library(tmp_path):
             abi.load(str(tmp_path / "nope.so"))
         finally:
             abi._lib = old
+
+
+def test_noalloc_entry_validates_like_the_allocating_one(lib):
+    """The no-allocation entry point shares the argument checks; every bad
+    call returns before any CUDA call, with the same status."""
+    cases = [dict(u=None), dict(B=None), dict(batch=-1), dict(dstate=0), dict(dstate=257),
+             dict(io_dtype=9), dict(u=P[0] + 1), dict(y=P[0]), dict(last_state=P[2]),
+             dict(batch=0), dict(dim=0)]
+    for over in cases:
+        kw = dict(GOOD)
+        kw.update(over)
+        assert abi.raw_scan_fwd_noalloc(**kw) == abi.raw_scan_fwd(**kw), over
+    assert abi.status_string(9).startswith("MAMBA_ERR_SCRATCH")
