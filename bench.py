@@ -62,6 +62,20 @@ def decode_counts(cfg) -> dict:
     }
 
 
+def launches_per_step(cfg, sms: int) -> int:
+    """Kernels one forward scan launches: 3 (summary, carry, full pass) when
+    the library splits the sequence, else 1.  Mirrors the library's planner for
+    dstate-16 inputs with 16-byte aligned rows (as every bench workload has):
+    split when the 32-chain CTAs would leave at least half of the SMs idle,
+    into min(8 * SMs / CTAs, seqlen / 512) segments, at least 2."""
+    if cfg.dstate != 16:
+        return 1
+    ctas = cfg.batch * ((cfg.dim + 31) // 32)
+    if 2 * ctas > sms:
+        return 1
+    return 3 if min(8 * sms // ctas, cfg.seqlen // 512) >= 2 else 1
+
+
 def kernel_source_hash() -> str:
     """Hash of the scan kernel sources, to match stored ncu traffic figures."""
     h = hashlib.sha256()
@@ -443,7 +457,8 @@ def run_ours(args, cfg, dcfg, rank, world, local):
         "binding_unit": "sfu" if t_sfu >= t_hbm else "hbm",
         "t_floor_us": {"hbm": round(t_hbm * 1e6, 1), "sfu": round(t_sfu * 1e6, 1)},
         "ubench": {k: (round(v / 1e9, 1) if k.endswith("_per_s") else v) for k, v in sfu.items()},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step(
+            cfg, torch.cuda.get_device_properties(device).multi_processor_count),
         "clocks": clk.summary(),
         "kernel_source_sha256_16": khash,
         "algorithmic_bytes_per_launch": cnt["bytes"],
