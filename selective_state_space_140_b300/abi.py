@@ -27,6 +27,9 @@ EXPORTED = ("mamba_selective_scan_fwd", "mamba_selective_scan_fwd_noalloc",
             "mamba_selective_state_update", "mamba_device_status", "mamba_status_string",
             "mamba_abi_version")
 
+# Test-only symbols, declared in include/mamba_scan_testing.h.
+TESTING_EXPORTED = ("mamba_test_bounded_wait",)
+
 _lib = None
 
 
@@ -51,6 +54,8 @@ def _declare(lib):
     lib.mamba_abi_version.argtypes = []
     lib.mamba_device_status.restype = ci
     lib.mamba_device_status.argtypes = [vp]
+    lib.mamba_test_bounded_wait.restype = ci
+    lib.mamba_test_bounded_wait.argtypes = [ci, vp]
     return lib
 
 
@@ -78,6 +83,16 @@ def mamba_device_status(stream=None, device=None) -> int:
     0, or MAMBA_ERR_TIMEOUT (7) if an on-device bounded wait gave up."""
     dev = device or torch.device("cuda", torch.cuda.current_device())
     return load().mamba_device_status(_stream(stream, dev))
+
+
+def mamba_test_bounded_wait(polls: int, stream=None, device=None) -> None:
+    """Test hook (include/mamba_scan_testing.h): queue a wait that nothing
+    completes, given up after ``polls`` polls; the next ``mamba_device_status``
+    reports MAMBA_ERR_TIMEOUT."""
+    dev = device or torch.device("cuda", torch.cuda.current_device())
+    rc = load().mamba_test_bounded_wait(int(polls), _stream(stream, dev))
+    if rc != 0:
+        raise MambaError(rc, "mamba_test_bounded_wait")
 
 
 def _io_dtype(t: torch.Tensor) -> int:

@@ -3,6 +3,7 @@
 #include <mutex>
 
 #include "../../include/mamba_scan.h"
+#include "../../include/mamba_scan_testing.h"
 #include "common.cuh"
 
 namespace {
@@ -158,6 +159,13 @@ int mamba_selective_scan_fwd_noalloc(const void* u, const void* delta, const flo
     const cudaError_t err = mamba::launch_scan_fwd(a, io_dtype == MAMBA_BF16,
                                                    reinterpret_cast<cudaStream_t>(stream), scratch);
     if (err == cudaErrorMemoryAllocation) return MAMBA_ERR_SCRATCH;
+    return err == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
+}
+
+int mamba_test_bounded_wait(int polls, mamba_stream_t stream) {
+    if (polls < 1 || polls > (1 << 20)) return MAMBA_ERR_SIZE;
+    const cudaError_t err =
+        mamba::launch_bounded_wait_probe(uint32_t(polls), reinterpret_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
 }
 

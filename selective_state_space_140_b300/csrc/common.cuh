@@ -95,11 +95,20 @@ __device__ __forceinline__ float softplus_accurate(float x) {
 // carry 2^-9 relative rounding already).  log1p(e) uses its Taylor series
 // e - e^2/2 + e^3/3 - e^4/4 below e = 2^-7 (truncation < e^5/5) and
 // lg2(1 + e) * ln2 above, where the lg2 result is at least 0.011.
+// Written with explicit round-to-nearest operations so that every kernel
+// (scalar or packed callers) gets bit-identical results.
 __device__ __forceinline__ float softplus_fast(float x) {
-    const float e = ex2_approx(-fabsf(x) * kLog2e);
-    const float series = e * fmaf(e, fmaf(e, fmaf(e, -0.25f, 0.333333343f), -0.5f), 1.f);
-    const float lg = lg2_approx(1.f + e) * kLn2;
-    return fmaxf(x, 0.f) + (e < 0.0078125f ? series : lg);
+    const float e = ex2_approx(__fmul_rn(-fabsf(x), kLog2e));
+    const float series =
+        __fmul_rn(e, __fmaf_rn(e, __fmaf_rn(e, __fmaf_rn(e, -0.25f, 0.333333343f), -0.5f), 1.f));
+    const float lg = __fmul_rn(lg2_approx(__fadd_rn(1.f, e)), kLn2);
+    return __fadd_rn(fmaxf(x, 0.f), e < 0.0078125f ? series : lg);
+}
+
+// y * SiLU(z) = (y * z) / (1 + e^-z), on the SFU, in a fixed operation order.
+__device__ __forceinline__ float gate_silu(float y, float z) {
+    const float den = __fadd_rn(ex2_approx(__fmul_rn(z, -kLog2e)), 1.f);
+    return __fmul_rn(__fmul_rn(y, z), rcp_approx(den));
 }
 
 // SiLU(z) = z * sigmoid(z) = z / (1 + e^-z), on the SFU.  For z << 0 the
@@ -146,14 +155,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 }
 
 // Bounded wait for phase `parity` of `bar`.  A copy that never lands must not
-// hang the GPU: after the iteration limit this returns false, the caller
+// hang the GPU: after `limit` polls (each try_wait may suspend the thread for
+// a short, implementation-defined time) this returns false; the caller
 // records the failure in its error word and carries on (its results are then
-// garbage, which the host learns from mamba_device_status()).
-constexpr uint32_t kWaitLimit = 1u << 24;
+// garbage, which the host learns from mamba_device_status()).  After a first
+// failure a thread polls only kWaitLimitAfterFailure times per later wait, so
+// a broken launch still ends in bounded time.
+constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t kWaitLimitAfterFailure = 1u << 10;
 
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_n(uint64_t* bar, uint32_t parity, uint32_t limit) {
     const uint32_t a = smem_addr(bar);
-    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    for (uint32_t i = 0; i < limit; ++i) {
         uint32_t ok;
         asm volatile(
             "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
@@ -227,5 +240,7 @@ cudaError_t launch_scan_fwd(const ScanArgs& a, bool bf16, cudaStream_t stream,
 // Synchronise `stream`, then read and clear the scan's device error word.
 cudaError_t read_and_clear_device_error(unsigned int* word, cudaStream_t stream);
 cudaError_t launch_state_update(const StateUpdateArgs& a, bool bf16, cudaStream_t stream);
+// Test hook: a wait that never completes, given up after `limit` polls.
+cudaError_t launch_bounded_wait_probe(uint32_t limit, cudaStream_t stream);
 
 }  // namespace mamba

@@ -54,6 +54,15 @@ namespace mamba {
 // Error word of this kernel family (see mbar_wait).
 __device__ unsigned int g_scan_error;
 
+// Wait for a bulk copy into shared memory; a wait that gives up sets the
+// error word and makes this thread's later waits short (see mbar_wait_n).
+__device__ __forceinline__ void wait_copy(uint64_t* bar, uint32_t parity, bool& failed) {
+    if (!mbar_wait_n(bar, parity, failed ? kWaitLimitAfterFailure : kWaitLimit)) {
+        failed = true;
+        atomicOr(&g_scan_error, kErrWaitTimeout);
+    }
+}
+
 namespace {
 
 __device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
@@ -75,38 +84,42 @@ __device__ __forceinline__ f32x2 get_pair(const V& v, int q) {
     }
 }
 
-// softplus on a pair: the bf16 path uses the SFU formulation of
+// softplus of one value: the bf16 path uses the SFU formulation of
 // softplus_fast, the fp32 path libdevice expf/log1pf.
+template <typename io_t>
+__device__ __forceinline__ float softplus_io(float x) {
+    if constexpr (sizeof(io_t) == 4) {
+        return softplus_accurate(x);
+    } else {
+        return softplus_fast(x);
+    }
+}
+
+// The same on a pair (each lane exactly as softplus_io).
 template <typename io_t>
 __device__ __forceinline__ f32x2 softplus_pair(f32x2 x) {
     float x0, x1;
     unpack2(x, x0, x1);
-    if constexpr (sizeof(io_t) == 4) {
-        return pack2(softplus_accurate(x0), softplus_accurate(x1));
-    } else {
-        const float e0 = ex2_approx(fabsf(x0) * -kLog2e), e1 = ex2_approx(fabsf(x1) * -kLog2e);
-        const f32x2 e = pack2(e0, e1);
-        f32x2 s = fma2(e, splat2(-0.25f), splat2(0.333333343f));
-        s = fma2(e, s, splat2(-0.5f));
-        s = fma2(e, s, splat2(1.f));
-        s = mul2(e, s);
-        float w0, w1;
-        unpack2(add2(e, splat2(1.f)), w0, w1);
-        float s0, s1;
-        unpack2(s, s0, s1);
-        const float l0 = e0 < 0.0078125f ? s0 : lg2_approx(w0) * kLn2;
-        const float l1 = e1 < 0.0078125f ? s1 : lg2_approx(w1) * kLn2;
-        return add2(pack2(fmaxf(x0, 0.f), fmaxf(x1, 0.f)), pack2(l0, l1));
-    }
+    return pack2(softplus_io<io_t>(x0), softplus_io<io_t>(x1));
 }
 
-// y * SiLU(z) on a pair: y * z / (1 + e^-z).
+// y * SiLU(z) on a pair (each lane exactly as gate_silu).
 __device__ __forceinline__ f32x2 gate_pair(f32x2 y, f32x2 z) {
-    float z0, z1;
-    unpack2(mul2(z, splat2(-kLog2e)), z0, z1);
-    float d0, d1;
-    unpack2(add2(pack2(ex2_approx(z0), ex2_approx(z1)), splat2(1.f)), d0, d1);
-    return mul2(mul2(y, z), pack2(rcp_approx(d0), rcp_approx(d1)));
+    float y0, y1, z0, z1;
+    unpack2(y, y0, y1);
+    unpack2(z, z0, z1);
+    return pack2(gate_silu(y0, z0), gate_silu(y1, z1));
+}
+
+// Element e of a vector of io values (bf16: the upper half-word is the odd one).
+template <typename io_t, typename V>
+__device__ __forceinline__ float io_elem(const V& v, int e) {
+    const unsigned* w = reinterpret_cast<const unsigned*>(&v);
+    if constexpr (sizeof(io_t) == 4) {
+        return __uint_as_float(w[e]);
+    } else {
+        return __uint_as_float((e & 1) ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16));
+    }
 }
 
 // Pack NQ pairs of fp32 into io values (bf16: round to nearest even).
@@ -177,16 +190,17 @@ __device__ __forceinline__ void recurrence(const float4* sdu, const float* sB, c
         }
     };
     auto update = [&](const Step& st) -> float {
-        f32x2 acc = splat2(0.f);
+        // two accumulators halve the dependent chain of C.h within a step
+        f32x2 acc0 = splat2(0.f), acc1 = splat2(0.f);
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
             h[2 * q] = fma2(st.a[2 * q], h[2 * q], mul2(st.sd.y, st.bq[q].x));
             h[2 * q + 1] = fma2(st.a[2 * q + 1], h[2 * q + 1], mul2(st.sd.y, st.bq[q].y));
-            acc = fma2(st.cq[q].x, h[2 * q], acc);
-            acc = fma2(st.cq[q].y, h[2 * q + 1], acc);
+            acc0 = fma2(st.cq[q].x, h[2 * q], acc0);
+            acc1 = fma2(st.cq[q].y, h[2 * q + 1], acc1);
         }
         float lo, hi;
-        unpack2(acc, lo, hi);
+        unpack2(add2(acc0, acc1), lo, hi);
         return lo + hi;
     };
     Step cur;
@@ -447,12 +461,13 @@ __global__ void __launch_bounds__(CH* G)
     init_state<NPL, G>(p, d, chain_ok, g, A2, h);
     __syncthreads();
 
+    bool copy_failed = false;
     io_t* yy = static_cast<io_t*>(p.y);
     for (int64_t k = 0; k < nchunks; ++k) {
         const int s = int(k % S);
         const int64_t t0 = k * T;
         const int tlen = L - t0 < T ? int(L - t0) : T;
-        if (!mbar_wait(&bar[s], uint32_t(k / S) & 1u)) atomicOr(&g_scan_error, kErrWaitTimeout);
+        wait_copy(&bar[s], uint32_t(k / S) & 1u, copy_failed);
 
         // ---- phase A ----
         widen_bc<io_t, NP, T, NTH>(raw(s, 0), raw(s, 1), sB, sC, N, tid);
@@ -853,7 +868,7 @@ __global__ void __launch_bounds__(NR + NE, MINB)
     const int seg = lane % C::SEGROW;
     constexpr int ROWS = CH * G;
     int ec[SPT], tq[SPT], dub[SPT], yu[SPT][G];
-    f32x2 bias2[SPT], Dv2[SPT];
+    float bias[SPT], Dd[SPT];
     bool chain_ok[SPT];
     io_t* yg[SPT];
 #pragma unroll
@@ -861,8 +876,8 @@ __global__ void __launch_bounds__(NR + NE, MINB)
         ec[i] = w * CW + lane / C::SEGROW + i * (32 / C::SEGROW);
         const int64_t dd = d0 + ec[i];
         chain_ok[i] = dd < dim;
-        bias2[i] = splat2((chain_ok[i] && p.delta_bias) ? __ldg(p.delta_bias + dd) : 0.f);
-        Dv2[i] = splat2((chain_ok[i] && p.D) ? __ldg(p.D + dd) : 0.f);
+        bias[i] = (chain_ok[i] && p.delta_bias) ? __ldg(p.delta_bias + dd) : 0.f;
+        Dd[i] = (chain_ok[i] && p.D) ? __ldg(p.D + dd) : 0.f;
         tq[i] = ec[i] * C::SEGROW + seg;
         dub[i] = seg * PV * CH + (ec[i] ^ ((2 * seg) & (CH - 1)));  // du_col of steps 4*seg..+3
 #pragma unroll
@@ -876,6 +891,7 @@ __global__ void __launch_bounds__(NR + NE, MINB)
     }
     __syncwarp();
 
+    bool copy_failed = false;
     float dtsum[SPT];  // summary pass: sum of dt over the segment
 #pragma unroll
     for (int i = 0; i < SPT; ++i) dtsum[i] = 0.f;
@@ -900,8 +916,7 @@ __global__ void __launch_bounds__(NR + NE, MINB)
         constexpr int BCV = T * NP * C::ES / 32 / 16;  // 16-byte pieces of B or C per lane
         uint4 rbc[BCV];
         if (kp >= 0) {
-            if (!mbar_wait(&bar[(kp & (S - 1)) * 2 + w], uint32_t(kp / S) & 1u))
-                atomicOr(&g_scan_error, kErrWaitTimeout);
+            wait_copy(&bar[(kp & (S - 1)) * 2 + w], uint32_t(kp / S) & 1u, copy_failed);
             const quad_t* td = reinterpret_cast<const quad_t*>(tile(kp, 1));
             const quad_t* tu = reinterpret_cast<const quad_t*>(tile(kp, 0));
 #pragma unroll
@@ -918,21 +933,21 @@ __global__ void __launch_bounds__(NR + NE, MINB)
             const bool seg_live = seg * PV < chunk_len(ke);
 #pragma unroll
             for (int i = 0; i < SPT; ++i) {
-                f32x2 v0 = ps[i][0].x, v1 = ps[i][0].y;
+                // scalar fp32 throughout: every value here passes through the
+                // SFU, so packed pairs would only add register moves
+                float v[PV];
 #pragma unroll
-                for (int gg = 1; gg < G; ++gg) {
-                    v0 = add2(v0, ps[i][gg].x);
-                    v1 = add2(v1, ps[i][gg].y);
+                for (int e = 0; e < PV; ++e) {
+                    float acc = reinterpret_cast<const float*>(&ps[i][0])[e];
+#pragma unroll
+                    for (int gg = 1; gg < G; ++gg)
+                        acc = __fadd_rn(acc, reinterpret_cast<const float*>(&ps[i][gg])[e]);
+                    acc = __fmaf_rn(Dd[i], io_elem<io_t>(eu[i], e), acc);
+                    v[e] = has_z ? gate_silu(acc, io_elem<io_t>(ez[i], e)) : acc;
                 }
-                v0 = fma2(Dv2[i], get_pair<io_t>(eu[i], 0), v0);
-                v1 = fma2(Dv2[i], get_pair<io_t>(eu[i], 1), v1);
-                if (has_z) {
-                    v0 = gate_pair(v0, get_pair<io_t>(ez[i], 0));
-                    v1 = gate_pair(v1, get_pair<io_t>(ez[i], 1));
-                }
-                f32x2 v[2] = {v0, v1};
+                f32x2 vp[2] = {pack2(v[0], v[1]), pack2(v[2], v[3])};
                 unsigned wd[PV * C::ES / 4];
-                pack_out<io_t, 2>(v, wd);
+                pack_out<io_t, 2>(vp, wd);
                 if (chain_ok[i] && seg_live)
                     *reinterpret_cast<quad_t*>(yg[i] + int64_t(ke) * T) =
                         *reinterpret_cast<const quad_t*>(wd);
@@ -944,15 +959,11 @@ __global__ void __launch_bounds__(NR + NE, MINB)
 #pragma unroll
             for (int i = 0; i < SPT; ++i) {
 #pragma unroll
-                for (int q = 0; q < PV / 2; ++q) {
-                    f32x2 dt = add2(get_pair<io_t>(pd[i], q), bias2[i]);
-                    if (p.softplus) dt = softplus_pair<io_t>(dt);
-                    const f32x2 du = mul2(dt, get_pair<io_t>(pu[i], q));
-                    float dt0, dt1, du0, du1;
-                    unpack2(dt, dt0, dt1);
-                    unpack2(du, du0, du1);
-                    o[i][2 * q] = make_float4(dt0, dt0, du0, du0);
-                    o[i][2 * q + 1] = make_float4(dt1, dt1, du1, du1);
+                for (int e = 0; e < PV; ++e) {
+                    float dt = __fadd_rn(io_elem<io_t>(pd[i], e), bias[i]);
+                    if (p.softplus) dt = softplus_io<io_t>(dt);
+                    const float du = __fmul_rn(dt, io_elem<io_t>(pu[i], e));
+                    o[i][e] = make_float4(dt, dt, du, du);
                 }
             }
             if (!all_chains || chunk_len(kp) < T) {  // zero steps past the end, dead chains
@@ -1127,10 +1138,8 @@ __global__ void __launch_bounds__(64)
         bulk_g2s(st + 3 * C::kTile, Bg + int64_t(k) * T * N, bc_bytes, br);
         bulk_g2s(st + 3 * C::kTile + C::kRaw, Cg + int64_t(k) * T * N, bc_bytes, br);
     };
-    auto wait_chunk = [&](int k) {
-        if (!mbar_wait(&bar[k & (S - 1)], uint32_t(k / S) & 1u))
-            atomicOr(&g_scan_error, kErrWaitTimeout);
-    };
+    bool copy_failed = false;
+    auto wait_chunk = [&](int k) { wait_copy(&bar[k & (S - 1)], uint32_t(k / S) & 1u, copy_failed); };
 
     // ---- per-element prologue of chunk k, quad item i: (dt, dt*u) ----
     auto elem_prologue = [&](int k, int i) {
@@ -1472,6 +1481,7 @@ __global__ void __launch_bounds__(CH* G)
             vz[i] = zz ? load_seg<C>(zz + row, t, L, ok) : make_uint4(0u, 0u, 0u, 0u);
         }
     };
+    bool copy_failed = false;
     prefetch(0, cur_d, cur_u, cur_z);
 
     for (int64_t k = 0; k < nchunks; ++k) {
@@ -1480,8 +1490,7 @@ __global__ void __launch_bounds__(CH* G)
 
         // ---- phase A ----
         if (chunk_by_tma(k)) {
-            if (!mbar_wait(&bar[k & 1], uint32_t(k >> 1) & 1u))
-                atomicOr(&g_scan_error, kErrWaitTimeout);
+            wait_copy(&bar[k & 1], uint32_t(k >> 1) & 1u, copy_failed);
             widen_bc<io_t, NP, T, NTH>(stageB(k), stageC(k), sB, sC, N, tid);
         } else {
             for (int idx = tid; idx < T * NP; idx += NTH) {
@@ -1888,6 +1897,23 @@ cudaError_t dispatch(const ScanArgs& a, cudaStream_t stream, const ScanScratch& 
 cudaError_t launch_scan_fwd(const ScanArgs& a, bool bf16, cudaStream_t stream,
                             const ScanScratch& sc) {
     return bf16 ? dispatch<__nv_bfloat16>(a, stream, sc) : dispatch<float>(a, stream, sc);
+}
+
+// Test hook: one thread waits, with `limit` polls, on an mbarrier that nothing
+// ever arrives on, and records the give-up in the error word exactly as the
+// scans' bounded copy waits do.  Nothing is copied, so nothing is in flight
+// when the kernel ends.
+__global__ void bounded_wait_probe_kernel(uint32_t limit) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait_n(&bar, 0u, limit)) atomicOr(&g_scan_error, kErrWaitTimeout);
+}
+
+cudaError_t launch_bounded_wait_probe(uint32_t limit, cudaStream_t stream) {
+    bounded_wait_probe_kernel<<<1, 32, 0, stream>>>(limit);
+    return cudaGetLastError();
 }
 
 cudaError_t read_and_clear_device_error(unsigned int* word, cudaStream_t stream) {

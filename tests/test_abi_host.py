@@ -140,3 +140,17 @@ def test_noalloc_entry_validates_like_the_allocating_one(lib):
         kw.update(over)
         assert abi.raw_scan_fwd_noalloc(**kw) == abi.raw_scan_fwd(**kw), over
     assert abi.status_string(9).startswith("MAMBA_ERR_SCRATCH")
+
+
+def test_testing_header_symbols_are_exported(lib):
+    text = open(os.path.join(ROOT, "include", "mamba_scan_testing.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    declared = sorted(set(re.findall(r"^\s*\w+\s*\*?\s*(mamba_\w+)\s*\(", text, flags=re.M)))
+    assert declared == sorted(abi.TESTING_EXPORTED)
+    for name in declared:
+        assert hasattr(lib, name)
+
+
+@pytest.mark.parametrize("polls", [0, -5, (1 << 20) + 1])
+def test_bounded_wait_hook_rejects_bad_poll_counts(lib, polls):
+    assert lib.mamba_test_bounded_wait(polls, None) == 2  # MAMBA_ERR_SIZE, nothing launched
