@@ -69,7 +69,9 @@ def _build_one(lib: str, force: bool, ptxas_info: bool, quiet: bool) -> str:
             if log.strip():
                 print(log, file=sys.stderr)
     tmp = lib + ".tmp"
-    cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
+    # --no-undefined: a missing definition fails here, not when the library loads
+    cmd = [NVCC, *ARCH, "-shared", "-Xlinker", "--no-undefined", "-o", tmp,
+           *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")

@@ -170,11 +170,12 @@ int mamba_test_bounded_wait(int polls, mamba_stream_t stream) {
 }
 
 int mamba_device_status(mamba_stream_t stream) {
-    unsigned int word = 0;
+    unsigned int word = 0, dword = 0;
     const cudaError_t err =
         mamba::read_and_clear_device_error(&word, reinterpret_cast<cudaStream_t>(stream));
-    if (err != cudaSuccess) return MAMBA_ERR_LAUNCH;
-    return (word & mamba::kErrWaitTimeout) ? MAMBA_ERR_TIMEOUT : MAMBA_OK;
+    if (err != cudaSuccess || mamba::read_and_clear_decode_error(&dword) != cudaSuccess)
+        return MAMBA_ERR_LAUNCH;
+    return ((word | dword) & mamba::kErrWaitTimeout) ? MAMBA_ERR_TIMEOUT : MAMBA_OK;
 }
 
 int mamba_selective_state_update(float* state, const void* x, const void* dt,

@@ -155,24 +155,27 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 }
 
 // Bounded wait for phase `parity` of `bar`.  A copy that never lands must not
-// hang the GPU: after `limit` polls (each try_wait may suspend the thread for
-// a short, implementation-defined time) this returns false; the caller
-// records the failure in its error word and carries on (its results are then
-// garbage, which the host learns from mamba_device_status()).  After a first
-// failure a thread polls only kWaitLimitAfterFailure times per later wait, so
-// a broken launch still ends in bounded time.
-constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr uint32_t kWaitLimitAfterFailure = 1u << 10;
+// hang the GPU: each poll is a try_wait that suspends the thread until the
+// phase completes or kWaitSuspendNs nanoseconds pass (a suspended warp issues
+// nothing, so waiting costs the other warps no issue slots); after `limit`
+// polls this returns false, the caller records the failure in its error word
+// and carries on (its results are then garbage, which the host learns from
+// mamba_device_status()).  kWaitLimit polls bound a wait near 1.3 s; after a
+// first failure a thread polls only kWaitLimitAfterFailure times per later
+// wait, so a broken launch still ends in bounded time.
+constexpr uint32_t kWaitSuspendNs = 20000;
+constexpr uint32_t kWaitLimit = 1u << 16;
+constexpr uint32_t kWaitLimitAfterFailure = 1u << 4;
 
 __device__ __forceinline__ bool mbar_wait_n(uint64_t* bar, uint32_t parity, uint32_t limit) {
     const uint32_t a = smem_addr(bar);
     for (uint32_t i = 0; i < limit; ++i) {
         uint32_t ok;
         asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
             " selp.u32 %0, 1, 0, p;\n}"
             : "=r"(ok)
-            : "r"(a), "r"(parity)
+            : "r"(a), "r"(parity), "r"(kWaitSuspendNs)
             : "memory");
         if (ok) return true;
     }
@@ -239,6 +242,8 @@ cudaError_t launch_scan_fwd(const ScanArgs& a, bool bf16, cudaStream_t stream,
                             const ScanScratch& scratch);
 // Synchronise `stream`, then read and clear the scan's device error word.
 cudaError_t read_and_clear_device_error(unsigned int* word, cudaStream_t stream);
+// Read and clear the decode kernels' device error word (after a synchronise).
+cudaError_t read_and_clear_decode_error(unsigned int* word);
 cudaError_t launch_state_update(const StateUpdateArgs& a, bool bf16, cudaStream_t stream);
 // Test hook: a wait that never completes, given up after `limit` polls.
 cudaError_t launch_bounded_wait_probe(uint32_t limit, cudaStream_t stream);

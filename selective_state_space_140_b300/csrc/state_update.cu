@@ -9,21 +9,31 @@
 // warp reads and writes a contiguous run of the state array (one 16-byte
 // access per lane when NPL == 4 and the state is 16-byte aligned).  The partial
 // sums of C.h are combined with warp shuffles inside the G-lane group.
+#include <cstdlib>
+
 #include "common.cuh"
 
 namespace mamba {
+
+// Device error word of the decode kernels' bounded waits; mamba_device_status
+// reads and clears it together with the scan's.
+__device__ unsigned int g_decode_error;
+
 namespace {
 
+// The grid covers each batch row with `bpr` blocks of 256 / G channels, so a
+// thread finds its (b, d) from its block with one division per block (the
+// per-thread 64-bit division by dim cost more than the whole state update).
 template <typename io_t, int NPL, int G, bool VEC>
-__global__ void __launch_bounds__(256) state_update_kernel(StateUpdateArgs p) {
-    const int64_t chains = p.batch * p.dim;
-    const int64_t gtid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t chain = gtid / G;
-    const int g = int(gtid % G);
+__global__ void __launch_bounds__(256) state_update_kernel(StateUpdateArgs p, uint32_t bpr) {
+    const uint32_t bi = blockIdx.x / bpr;  // the same for the whole block
+    const int64_t b = bi;
+    const int64_t d = int64_t(blockIdx.x - bi * bpr) * (256 / G) + threadIdx.x / G;
+    const int g = int(threadIdx.x % G);
     // Whole G-lane groups are inside or outside together (G divides 32 and the
     // block size), so the shuffles below never mix live and dead lanes.
-    if (chain >= chains) return;
-    const int64_t b = chain / p.dim, d = chain % p.dim;
+    if (d >= p.dim) return;
+    const int64_t chain = b * p.dim + d;
     const int N = p.dstate;
 
     const float raw = Io<io_t>::load(static_cast<const io_t*>(p.dt) + chain) +
@@ -85,21 +95,205 @@ __global__ void __launch_bounds__(256) state_update_kernel(StateUpdateArgs p) {
 
 template <typename io_t, int NPL, int G>
 cudaError_t launch(const StateUpdateArgs& a, cudaStream_t stream) {
-    const int64_t threads = a.batch * a.dim * G;
-    const int64_t blocks = (threads + 255) / 256;
+    const int64_t bpr = (a.dim + 256 / G - 1) / (256 / G);  // blocks per batch row
+    const int64_t blocks = a.batch * bpr;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const bool vec = (a.dstate % 4 == 0) && (a.dstate == NPL * G) &&
                      (reinterpret_cast<uintptr_t>(a.state) % 16 == 0);
     if (vec)
-        state_update_kernel<io_t, NPL, G, true><<<unsigned(blocks), 256, 0, stream>>>(a);
+        state_update_kernel<io_t, NPL, G, true><<<unsigned(blocks), 256, 0, stream>>>(a, uint32_t(bpr));
     else
-        state_update_kernel<io_t, NPL, G, false><<<unsigned(blocks), 256, 0, stream>>>(a);
+        state_update_kernel<io_t, NPL, G, false><<<unsigned(blocks), 256, 0, stream>>>(a, uint32_t(bpr));
     return cudaGetLastError();
+}
+
+// ---- bulk-copy ring path ------------------------------------------------
+// One 16-byte state access per thread keeps too few bytes in flight for the
+// HBM.  Here a persistent CTA of 256 threads walks tiles of TC = 4096 / N
+// chains of one batch row (16 KB of state); thread 0 keeps S = 2 tiles in
+// flight as bulk copies (cp.async.bulk: the state rows, the tile's A_log, bias
+// and D rows and its dt, x and z) into a shared-memory ring completed on
+// mbarriers.  B and C of the batch are loaded before a tile's copy is waited
+// for; each pass is then arithmetic on shared memory, and the new state is
+// stored straight to global memory.
+constexpr int kRingTileBytes = 16384;
+
+// Stage layout: state rows | A_log rows | dt | x | z | bias | D (each 16-byte
+// multiple).  A tile lies inside one batch row, so the A_log, bias and D rows
+// of its channels are contiguous too.
+template <typename io_t, int G>
+struct RingCfg {
+    static constexpr int NPL = 4, N = NPL * G, TC = kRingTileBytes / (N * 4), CPP = 256 / G;
+    static constexpr int PASSES = TC / CPP, ES = sizeof(io_t), S = 2;
+    static constexpr int kIoBytes = TC * ES;  // dt, x or z of one tile
+    static constexpr int kParBytes = TC * 4;  // bias or D of one tile
+    static constexpr int kA = kRingTileBytes, kDt = 2 * kRingTileBytes, kX = kDt + kIoBytes;
+    static constexpr int kZ = kX + kIoBytes, kBias = kZ + kIoBytes, kD = kBias + kParBytes;
+    static constexpr int kStage = kD + kParBytes;
+    static constexpr int kSmem = 128 + S * kStage;
+    static_assert(PASSES * CPP == TC && kIoBytes % 16 == 0, "tile shape");
+};
+
+template <typename io_t, int G>
+__global__ void __launch_bounds__(256, 4) state_update_ring_kernel(StateUpdateArgs p,
+                                                                   int64_t ntiles) {
+    using C = RingCfg<io_t, G>;
+    constexpr int N = C::N, TC = C::TC, CPP = C::CPP, PASSES = C::PASSES, S = C::S;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    auto stage = [&](int st) { return smem + 128 + st * C::kStage; };
+    const int tid = threadIdx.x, g = tid % G, cl = tid / G;
+    const bool has_z = p.z != nullptr;
+
+    const int64_t tiles_per_row = p.dim / TC;
+    auto issue = [&](int64_t tile, int st) {  // thread 0
+        const int64_t c0 = tile * TC;
+        const int64_t d0 = (tile % tiles_per_row) * TC;
+        unsigned char* sp = stage(st);
+        const uint32_t bytes = 2 * kRingTileBytes + (has_z ? 3 : 2) * C::kIoBytes +
+                               (p.dt_bias ? C::kParBytes : 0) + (p.D ? C::kParBytes : 0);
+        mbar_arrive_expect_tx(&bar[st], bytes);
+        bulk_g2s(sp, p.state + c0 * N, kRingTileBytes, &bar[st]);
+        bulk_g2s(sp + C::kA, p.A_log + d0 * N, kRingTileBytes, &bar[st]);
+        bulk_g2s(sp + C::kDt, static_cast<const io_t*>(p.dt) + c0, C::kIoBytes, &bar[st]);
+        bulk_g2s(sp + C::kX, static_cast<const io_t*>(p.x) + c0, C::kIoBytes, &bar[st]);
+        if (has_z) bulk_g2s(sp + C::kZ, static_cast<const io_t*>(p.z) + c0, C::kIoBytes, &bar[st]);
+        if (p.dt_bias) bulk_g2s(sp + C::kBias, p.dt_bias + d0, C::kParBytes, &bar[st]);
+        if (p.D) bulk_g2s(sp + C::kD, p.D + d0, C::kParBytes, &bar[st]);
+    };
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);  // (S <= 16 fit in 128 bytes)
+        fence_mbar_init();
+        for (int s = 0; s < S; ++s) {
+            const int64_t tile = blockIdx.x + int64_t(s) * gridDim.x;
+            if (tile < ntiles) issue(tile, s);
+        }
+    }
+    __syncthreads();
+
+    const unsigned lane = tid & 31u;
+    const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane / G * G));
+    bool failed = false;
+    int j = 0;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
+        const int st = j % S;
+        // ---- B and C of the batch first: they do not depend on the copy ----
+        const int64_t b = tile / tiles_per_row;
+        float Bv[4], Cv[4];
+        {
+            const io_t* Bb = static_cast<const io_t*>(p.B) + b * N + g * 4;
+            const io_t* Cb = static_cast<const io_t*>(p.C) + b * N + g * 4;
+            if constexpr (sizeof(io_t) == 2) {
+                const uint2 wb = __ldg(reinterpret_cast<const uint2*>(Bb));
+                const uint2 wc = __ldg(reinterpret_cast<const uint2*>(Cb));
+                Bv[0] = __uint_as_float(wb.x << 16); Bv[1] = __uint_as_float(wb.x & 0xffff0000u);
+                Bv[2] = __uint_as_float(wb.y << 16); Bv[3] = __uint_as_float(wb.y & 0xffff0000u);
+                Cv[0] = __uint_as_float(wc.x << 16); Cv[1] = __uint_as_float(wc.x & 0xffff0000u);
+                Cv[2] = __uint_as_float(wc.y << 16); Cv[3] = __uint_as_float(wc.y & 0xffff0000u);
+            } else {
+                const float4 vb = __ldg(reinterpret_cast<const float4*>(Bb));
+                const float4 vc = __ldg(reinterpret_cast<const float4*>(Cb));
+                Bv[0] = vb.x; Bv[1] = vb.y; Bv[2] = vb.z; Bv[3] = vb.w;
+                Cv[0] = vc.x; Cv[1] = vc.y; Cv[2] = vc.z; Cv[3] = vc.w;
+            }
+        }
+        if (!mbar_wait_n(&bar[st], uint32_t(j / S) & 1u,
+                         failed ? kWaitLimitAfterFailure : kWaitLimit)) {
+            failed = true;
+            atomicOr(&g_decode_error, kErrWaitTimeout);
+        }
+        const unsigned char* sp = stage(st);
+        const float4* sA = reinterpret_cast<const float4*>(sp + C::kA);
+        const io_t* sdt = reinterpret_cast<const io_t*>(sp + C::kDt);
+        const io_t* sx = reinterpret_cast<const io_t*>(sp + C::kX);
+        const io_t* sz = reinterpret_cast<const io_t*>(sp + C::kZ);
+        const float* sbias = reinterpret_cast<const float*>(sp + C::kBias);
+        const float* sD = reinterpret_cast<const float*>(sp + C::kD);
+#pragma unroll
+        for (int ps = 0; ps < PASSES; ++ps) {
+            const int local = ps * CPP + cl;
+            const int64_t chain = tile * TC + local;
+            const float4 hv = reinterpret_cast<const float4*>(sp)[local * G + g];
+            const float4 av = sA[local * G + g];
+            const float A[4] = {av.x, av.y, av.z, av.w};
+            const float raw = float(sdt[local]) + (p.dt_bias ? sbias[local] : 0.f);
+            const float x = float(sx[local]);
+            const float dt = !p.softplus ? raw : sizeof(io_t) == 2 ? softplus_fast(raw)
+                                                                     : softplus_accurate(raw);
+            const float dx = dt * x;
+            float h[4] = {hv.x, hv.y, hv.z, hv.w};
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                // A = -exp(A_log) = -2^(A_log * log2 e); Abar = 2^(dt * A * log2 e)
+                const float A2 = -ex2_approx(A[i] * kLog2e) * kLog2e;
+                h[i] = fmaf(ex2_approx(dt * A2), h[i], dx * Bv[i]);
+                acc = fmaf(Cv[i], h[i], acc);
+            }
+            reinterpret_cast<float4*>(p.state + chain * N)[g] = make_float4(h[0], h[1], h[2], h[3]);
+#pragma unroll
+            for (int off = G / 2; off > 0; off /= 2) acc += __shfl_xor_sync(gmask, acc, off, G);
+            if (g == 0) {
+                if (p.D) acc = fmaf(sD[local], x, acc);
+                if (has_z) acc *= silu_fast(float(sz[local]));
+                Io<io_t>::store(static_cast<io_t*>(p.out) + chain, acc);
+            }
+        }
+        __syncthreads();  // every thread is done with this stage
+        if (tid == 0 && tile + int64_t(S) * gridDim.x < ntiles) {
+            fence_proxy_async_smem();
+            issue(tile + int64_t(S) * gridDim.x, st);
+        }
+    }
+}
+
+// The ring needs whole tiles inside batch rows (dim a multiple of TC) and
+// 16-byte aligned state, A_log, dt, x, z and B/C rows of 4 elements.
+template <typename io_t, int G>
+bool try_ring(const StateUpdateArgs& a, cudaStream_t stream, cudaError_t* err) {
+    using C = RingCfg<io_t, G>;
+    auto al = [](const void* q, size_t n) {
+        return q == nullptr || reinterpret_cast<uintptr_t>(q) % n == 0;
+    };
+    if (a.dstate != C::N || a.dim % C::TC != 0 || !al(a.state, 16) || !al(a.A_log, 16) ||
+        !al(a.dt, 16) || !al(a.x, 16) || !al(a.z, 16) || !al(a.dt_bias, 16) || !al(a.D, 16) ||
+        !al(a.B, 4 * C::ES) || !al(a.C, 4 * C::ES))
+        return false;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return false;
+    const int64_t ntiles = a.batch * a.dim / C::TC;
+    int per_sm = 0;
+    if (cudaFuncSetAttribute(state_update_ring_kernel<io_t, G>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, state_update_ring_kernel<io_t, G>,
+                                                      256, C::kSmem) != cudaSuccess ||
+        per_sm < 1)
+        return false;
+    const int64_t slots = int64_t(sms) * per_sm;  // one persistent CTA per slot
+    const int64_t grid = ntiles < slots ? ntiles : slots;
+    auto kern = state_update_ring_kernel<io_t, G>;
+    *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (*err != cudaSuccess) return true;
+    kern<<<unsigned(grid), 256, C::kSmem, stream>>>(a, ntiles);
+    *err = cudaGetLastError();
+    return true;
 }
 
 template <typename io_t>
 cudaError_t dispatch(const StateUpdateArgs& a, cudaStream_t stream) {
     const int N = a.dstate;
+    cudaError_t err = cudaSuccess;
+    const char* path = getenv("MAMBA_DECODE_PATH");
+    if (!(path && path[0] == 'p')) {  // MAMBA_DECODE_PATH=plain: one access per thread
+        if (N == 4 && try_ring<io_t, 1>(a, stream, &err)) return err;
+        if (N == 8 && try_ring<io_t, 2>(a, stream, &err)) return err;
+        if (N == 16 && try_ring<io_t, 4>(a, stream, &err)) return err;
+        if (N == 32 && try_ring<io_t, 8>(a, stream, &err)) return err;
+        if (N == 64 && try_ring<io_t, 16>(a, stream, &err)) return err;
+        if (N == 128 && try_ring<io_t, 32>(a, stream, &err)) return err;
+    }
     if (N <= 4) return launch<io_t, 4, 1>(a, stream);
     if (N <= 8) return launch<io_t, 4, 2>(a, stream);
     if (N <= 16) return launch<io_t, 4, 4>(a, stream);
@@ -110,6 +304,13 @@ cudaError_t dispatch(const StateUpdateArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t read_and_clear_decode_error(unsigned int* word) {
+    const cudaError_t err = cudaMemcpyFromSymbol(word, g_decode_error, sizeof(unsigned int));
+    if (err != cudaSuccess) return err;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_decode_error, &zero, sizeof(unsigned int));
+}
 
 cudaError_t launch_state_update(const StateUpdateArgs& a, bool bf16, cudaStream_t stream) {
     return bf16 ? dispatch<__nv_bfloat16>(a, stream) : dispatch<float>(a, stream);

@@ -44,7 +44,9 @@ def test_decode_config_full(cuda):
                                             (5, 13, 5, "f32"), (4, 33, 16, "bf16"),
                                             (2, 10, 17, "f32"), (3, 6, 64, "f32"),
                                             (2, 5, 100, "bf16"), (2, 3, 256, "f32"),
-                                            (1, 4, 255, "f32")])
+                                            (1, 4, 255, "f32"), (3, 65, 16, "bf16"),
+                                            (5, 300, 16, "f32"), (2, 257, 8, "bf16"),
+                                            (3, 1000, 64, "bf16"), (70, 3, 16, "f32")])
 def test_decode_shapes(cuda, batch, dim, N, io):
     x = workloads.make_decode_inputs(batch, dim, N, io, seed=batch + dim + N)
     yg, hg = _gpu_step(to_device(x, cuda))
@@ -103,3 +105,30 @@ def test_decode_chain_reproduces_the_scan(cuda, io, N):
                                       D=f(x["D"]), z=f(x["z"]), delta_bias=f(x["delta_bias"]))
     assert rel_err(y_dec.float().cpu().numpy(), yr) <= tol
     assert rel_err(st.cpu().numpy(), hr) <= tol
+
+
+@pytest.mark.parametrize("io,N,batch,dim", [("bf16", 16, 3, 512), ("f32", 16, 2, 768),
+                                            ("bf16", 4, 2, 2048), ("f32", 8, 3, 1024),
+                                            ("bf16", 32, 2, 256), ("f32", 64, 3, 128),
+                                            ("bf16", 128, 2, 64), ("f32", 128, 1, 96),
+                                            ("bf16", 16, 2, 300)])
+def test_decode_ring_matches_the_plain_kernel(cuda, io, N, batch, dim, monkeypatch):
+    """dstate 4..128 (powers of two) with dim a multiple of the 16 KB tile and
+    16-byte aligned rows take the bulk-copy ring kernel (persistent CTAs,
+    3-stage ring); MAMBA_DECODE_PATH=plain forces one state access per thread
+    (the last shape, dim 300, always does).  Both must match the oracle and
+    each other bit for bit (same arithmetic)."""
+    x = workloads.make_decode_inputs(batch, dim, N, io, seed=41 + N)
+    for opt in ({}, dict(with_z=False, with_D=False, with_bias=False)):
+        if opt:
+            x = workloads.make_decode_inputs(batch, dim, N, io, seed=43 + N, **opt)
+        xd = to_device(x, cuda)
+        yr, hr = _oracle_step(x)
+        monkeypatch.delenv("MAMBA_DECODE_PATH", raising=False)
+        y0, h0 = _gpu_step(xd)
+        monkeypatch.setenv("MAMBA_DECODE_PATH", "plain")
+        y1, h1 = _gpu_step(xd)
+        _check(x, y0, h0, yr, hr, f"ring {opt}")
+        _check(x, y1, h1, yr, hr, f"plain {opt}")
+        assert np.array_equal(y0, y1) and np.array_equal(h0, h1)
+    assert abi.mamba_device_status() == 0
