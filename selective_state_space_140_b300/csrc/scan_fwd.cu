@@ -1887,6 +1887,14 @@ cudaError_t dispatch(const ScanArgs& a, cudaStream_t stream, const ScanScratch& 
         return run<io_t, 8, 2, 32, 16>(a, stream, pair);
     }
     if (N <= 32) return run<io_t, 4, 8, 8, 32>(a, stream, pair);
+    if (N == 64 && tile == 4 && !force_reg()) {
+        // 16 states x 4 lanes per chain, 16 chains per CTA, two CTAs per SM.
+        // Measured at 2 x 2048 x 8192 fp32: 1.85 ms against 0.97 ms for the
+        // paired tile -- under one recurrence warp per scheduler cannot hide
+        // a 16-state step's latency -- so it is a selectable variant only.
+        cudaError_t err = cudaSuccess;
+        if (try_ws<io_t, 1, 16, 4, 64, 64, 2>(a, stream, &err)) return err;
+    }
     if (N <= 64) return run<io_t, 4, 16, 4, 16>(a, stream, pair);
     if (N <= 128) return run<io_t, 4, 32, 2, 16>(a, stream, pair);
     return run<io_t, 8, 32, 2, 8>(a, stream, pair);

@@ -233,3 +233,21 @@ def test_segmented_scan_without_softplus_and_optional_inputs(cuda, monkeypatch):
     yg, hg = _run(x, cuda)
     yr, hr = oracle_scan(x)
     _assert_close(x, yg, hg, yr, hr, what="segmented, no z/D/bias, softplus off")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("batch,dim,L", [(2, 40, 1000), (1, 16, 336), (3, 33, 4096)])
+def test_dstate64_tiles_agree(cuda, io, batch, dim, L, monkeypatch):
+    """dstate 64: MAMBA_SCAN_TILE=4 selects the warp-specialised tile (16
+    states x 4 lanes per chain, 16 chains per CTA), 3 the paired-chain tile
+    (the default).  Both must match the oracle and each other (partial CTAs
+    and a ragged last chunk included)."""
+    x = workloads.make_scan_inputs(batch, dim, L, 64, io, seed=50 + L, d_mode="normal")
+    yr, hr = oracle_scan(x)
+    monkeypatch.setenv("MAMBA_SCAN_TILE", "4")
+    y0, h0 = _run(x, cuda)
+    monkeypatch.setenv("MAMBA_SCAN_TILE", "3")
+    y1, h1 = _run(x, cuda)
+    _assert_close(x, y0, h0, yr, hr, what="warp-specialised")
+    _assert_close(x, y1, h1, yr, hr, what="paired")
+    assert rel_err(y0, y1) <= TOL[io] and rel_err(h0, h1) <= TOL[io]
