@@ -45,7 +45,8 @@ def _declare(lib):
     i64 = ctypes.c_int64
     lib.oracle_selective_scan_f64.restype = ctypes.c_int
     lib.oracle_selective_scan_f64.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int,
-                                              dp, dp, dp, i64, i64, i64, i64, ctypes.c_int]
+                                              dp, ctypes.c_void_p, dp, dp, i64, i64, i64, i64,
+                                              ctypes.c_int]
     lib.oracle_selective_state_update_f64.restype = ctypes.c_int
     lib.oracle_selective_state_update_f64.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp,
                                                       ctypes.c_int, dp, i64, i64, i64]
@@ -88,11 +89,13 @@ def hw_threads(lib=None) -> int:
 
 
 def selective_scan(u, delta, A_log, B, C, D=None, z=None, delta_bias=None, softplus=True,
-                   h0=None, nthreads: int = 0, lib=None):
+                   h0=None, reset=None, nthreads: int = 0, lib=None):
     """Run the fp64 recurrence; return ``(y, last_state, threads_used)``.
 
     Shapes: u/delta/z [batch, dim, L]; B/C [batch, L, N]; A_log [dim, N];
-    D/delta_bias [dim]; h0 (optional) [batch, dim, N].
+    D/delta_bias [dim]; h0 (optional) [batch, dim, N]; reset (optional)
+    [batch, L], non-zero where a new document starts (the state restarts
+    from zero before that step).
     """
     lib = lib or load()
     u, delta, A_log, B, C = map(_f64, (u, delta, A_log, B, C))
@@ -105,11 +108,15 @@ def selective_scan(u, delta, A_log, B, C, D=None, z=None, delta_bias=None, softp
     assert D is None or D.shape == (dim,)
     assert delta_bias is None or delta_bias.shape == (dim,)
     assert h0 is None or h0.shape == (batch, dim, N)
+    if reset is not None:
+        reset = np.ascontiguousarray(np.asarray(reset) != 0, dtype=np.uint8)
+        assert reset.shape == (batch, L)
     y = np.empty((batch, dim, L), dtype=np.float64)
     hL = np.empty((batch, dim, N), dtype=np.float64)
     used = lib.oracle_selective_scan_f64(
         _ptr(u), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
-        int(bool(softplus)), _ptr(h0), _ptr(y), _ptr(hL), batch, dim, L, N, int(nthreads))
+        int(bool(softplus)), _ptr(h0), None if reset is None else reset.ctypes.data,
+        _ptr(y), _ptr(hL), batch, dim, L, N, int(nthreads))
     if used < 0:
         raise ValueError(f"oracle_selective_scan_f64 rejected its arguments ({used})")
     return y, hL, used

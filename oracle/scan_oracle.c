@@ -19,6 +19,10 @@
  *     with use_bias=True).
  *   - SiLU output gate on the z branch (highthink.cn "Mamba 整体架构" block
  *     diagram: the SiLU branch multiplies the SSM output).
+ *   - Document boundaries: Mamba isolates documents by resetting its hidden
+ *     state (codechina.net overview, section 3.2, point 2 "边界控制"), and a
+ *     given starting state lets a long sequence be processed block by block
+ *     (the same page's deployment notes on sequences beyond 1M tokens).
  *
  * Readings taken where the pages are silent or disagree:
  *   - Bbar is the Euler form dt*B (not the exact ZOH inverse form).
@@ -26,6 +30,9 @@
  *   - y_t reads the state after the update at step t.
  *   - out = (sum_n C h + D u) * SiLU(z); z, D and the bias are optional.
  *   - softplus_flag == 0 uses dt = delta + bias as given.
+ *   - reset[b][t] != 0 marks token t as the first of a new document: every
+ *     state of every channel of batch b restarts from zero before step t.
+ *     h0 (optional) is the state before step 0.
  *
  * Layouts (row-major, contiguous):
  *   u, delta, z, y : [batch][dim][seqlen]
@@ -33,7 +40,8 @@
  *   A_log          : [dim][dstate]
  *   D, delta_bias  : [dim]
  *   h0, last_state : [batch][dim][dstate]
- * Every array is double precision.  The caller widens bf16 or fp32 values.
+ *   reset          : [batch][seqlen] bytes (optional)
+ * Every other array is double precision.  The caller widens bf16 or fp32 values.
  *
  * Parallelism: the (batch, channel) chains are independent; they are split
  * over POSIX threads.  That changes no arithmetic: every chain is evaluated in
@@ -56,6 +64,7 @@ static double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
 
 typedef struct {
     const double *u, *delta, *A_log, *B, *C, *D, *z, *delta_bias, *h0;
+    const unsigned char *reset;
     double *y, *last_state;
     int64_t batch, dim, seqlen, dstate;
     int softplus_flag;
@@ -71,6 +80,7 @@ static void scan_one_chain(const scan_job *j, int64_t chain, double *h, double *
     const double *zz = j->z ? j->z + chain * L : NULL;
     const double *Bb = j->B + b * L * N;
     const double *Cb = j->C + b * L * N;
+    const unsigned char *rs = j->reset ? j->reset + b * L : NULL;
     double *y = j->y + chain * L;
     const double Dd = j->D ? j->D[d] : 0.0;
     const double bias = j->delta_bias ? j->delta_bias[d] : 0.0;
@@ -80,6 +90,8 @@ static void scan_one_chain(const scan_job *j, int64_t chain, double *h, double *
         h[n] = j->h0 ? j->h0[chain * N + n] : 0.0;  /* zero initial state */
     }
     for (int64_t t = 0; t < L; ++t) {
+        if (rs && rs[t])                                /* new document:      */
+            for (int64_t n = 0; n < N; ++n) h[n] = 0.0; /* state restarts     */
         const double raw = dl[t] + bias;
         const double dt = j->softplus_flag ? oracle_softplus(raw) : raw;
         const double ut = u[t];
@@ -116,14 +128,15 @@ int oracle_hw_threads(void) {
 
 /*
  * Full selective scan.  h0 may be NULL (zero initial state, as on the pages);
- * it exists so that splitting a sequence in two can be checked.  nthreads <= 0
- * means all hardware threads.  Returns the number of threads used, or a
- * negative value on a bad argument.
+ * reset may be NULL (one document per row).  nthreads <= 0 means all hardware
+ * threads.  Returns the number of threads used, or a negative value on a bad
+ * argument.
  */
 int oracle_selective_scan_f64(const double *u, const double *delta, const double *A_log,
                               const double *B, const double *C, const double *D,
                               const double *z, const double *delta_bias, int softplus_flag,
-                              const double *h0, double *y, double *last_state,
+                              const double *h0, const unsigned char *reset, double *y,
+                              double *last_state,
                               int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
                               int nthreads) {
     if (!u || !delta || !A_log || !B || !C || !y) return -1;
@@ -132,7 +145,7 @@ int oracle_selective_scan_f64(const double *u, const double *delta, const double
     if (nthreads <= 0) nthreads = oracle_hw_threads();
     if (nthreads > chains) nthreads = chains > 0 ? (int)chains : 1;
 
-    scan_job base = {u, delta, A_log, B, C, D, z, delta_bias, h0, y, last_state,
+    scan_job base = {u, delta, A_log, B, C, D, z, delta_bias, h0, reset, y, last_state,
                      batch, dim, seqlen, dstate, softplus_flag, 0, 0};
     scan_job *jobs = (scan_job *)malloc(sizeof(scan_job) * (size_t)nthreads);
     pthread_t *tids = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);

@@ -13,7 +13,8 @@ steps).
 
 Steps pinned (see the page sections cited in ``oracle/scan_oracle.c``):
   A = -exp(A_log), Abar = exp(dt*A), Bbar = dt*B, h_t = Abar h_{t-1} + Bbar u,
-  y = sum_n C h + D u, SiLU(z) gate, dt = softplus(delta + bias), zero h0.
+  y = sum_n C h + D u, SiLU(z) gate, dt = softplus(delta + bias), zero h0,
+  a given h0, and the state restarting at document boundaries (reset mask).
 """
 from __future__ import annotations
 
@@ -300,6 +301,70 @@ def check_optional_inputs(lib):
     _close(y2, y0 * _silu(z), rtol=1e-13, what="gate multiplies the ungated output")
 
 
+def check_reset_splits_documents(lib):
+    """A reset mask cuts each batch row into documents: the scan must equal the
+    concatenation of independent scans of the documents, the first started
+    from h0 and every later one from a zero state (codechina.net overview,
+    section 3.2: resetting the hidden state isolates documents).  The masks
+    differ between batch rows, and one boundary sits on the last step."""
+    r = _rng(10)
+    b, d, L, N = 2, 3, 30, 4
+    u, z, raw = r.normal(size=(b, d, L)), r.normal(size=(b, d, L)), r.normal(size=(b, d, L))
+    B, C = r.normal(size=(b, L, N)), r.normal(size=(b, L, N))
+    A_log, D, bias = r.normal(size=(d, N)), r.normal(size=d), r.normal(size=d)
+    h0 = r.normal(size=(b, d, N))
+    starts = {0: [7, 8, 20], 1: [13, 29]}
+    reset = np.zeros((b, L), dtype=np.uint8)
+    for bi, ss in starts.items():
+        reset[bi, ss] = 1
+    kw = dict(D=D, delta_bias=bias, softplus=True, lib=lib)
+    y, hL, _ = oracle.selective_scan(u, raw, A_log, B, C, z=z, h0=h0, reset=reset, **kw)
+    for bi, ss in starts.items():
+        edges = [0, *ss, L]
+        ys, h = [], None
+        for k, (t0, t1) in enumerate(zip(edges[:-1], edges[1:])):
+            yk, h, _ = oracle.selective_scan(u[bi:bi + 1, :, t0:t1], raw[bi:bi + 1, :, t0:t1],
+                                             A_log, B[bi:bi + 1, t0:t1], C[bi:bi + 1, t0:t1],
+                                             z=z[bi:bi + 1, :, t0:t1],
+                                             h0=h0[bi:bi + 1] if k == 0 else None, **kw)
+            ys.append(yk)
+        _close(y[bi:bi + 1], np.concatenate(ys, axis=-1), rtol=1e-12, what=f"documents b={bi}")
+        _close(hL[bi:bi + 1], h, rtol=1e-12, what=f"last document state b={bi}")
+
+
+def check_reset_every_step_is_memoryless(lib):
+    """A reset at every step leaves no memory: h_t = dt_t B_t u_t, so
+    y_t = (sum_n C_tn dt_t B_tn u_t + D u_t) SiLU(z_t), whatever h0 was."""
+    r = _rng(11)
+    b, d, L, N = 2, 2, 6, 3
+    u, z, raw = r.normal(size=(b, d, L)), r.normal(size=(b, d, L)), r.normal(size=(b, d, L))
+    B, C = r.normal(size=(b, L, N)), r.normal(size=(b, L, N))
+    A_log, D, bias = r.normal(size=(d, N)), r.normal(size=d), r.normal(size=d)
+    y, hL, _ = oracle.selective_scan(u, raw, A_log, B, C, D=D, z=z, delta_bias=bias,
+                                     h0=r.normal(size=(b, d, N)), reset=np.ones((b, L)), lib=lib)
+    dt = np.logaddexp(0.0, raw + bias[None, :, None])                     # [b, d, L]
+    h = dt[..., None] * B[:, None] * u[..., None]                         # [b, d, L, N]
+    want = (np.einsum("btn,bdtn->bdt", C, h) + D[None, :, None] * u) * _silu(z)
+    _close(y, want, rtol=1e-12, what="memoryless outputs")
+    _close(hL, h[:, :, -1], rtol=1e-12, what="memoryless final state")
+
+
+def check_reset_at_start_ignores_h0(lib):
+    """A document boundary on step 0 discards the given initial state."""
+    r = _rng(12)
+    b, d, L, N = 2, 3, 12, 4
+    u, raw = r.normal(size=(b, d, L)), r.normal(size=(b, d, L))
+    B, C = r.normal(size=(b, L, N)), r.normal(size=(b, L, N))
+    A_log = r.normal(size=(d, N))
+    reset = np.zeros((b, L), dtype=np.uint8)
+    reset[:, 0] = 1
+    y0, h0, _ = oracle.selective_scan(u, raw, A_log, B, C, lib=lib)
+    y1, h1, _ = oracle.selective_scan(u, raw, A_log, B, C, h0=r.normal(size=(b, d, N)),
+                                      reset=reset, lib=lib)
+    _close(y1, y0, rtol=0, what="outputs after a reset on step 0")
+    _close(h1, h0, rtol=0, what="state after a reset on step 0")
+
+
 ALL_CHECKS = [
     check_delta_zero_limit,
     check_single_step,
@@ -313,4 +378,7 @@ ALL_CHECKS = [
     check_decode_single_step,
     check_permutations,
     check_optional_inputs,
+    check_reset_splits_documents,
+    check_reset_every_step_is_memoryless,
+    check_reset_at_start_ignores_h0,
 ]

@@ -37,6 +37,12 @@ MUTANTS = [
     ("initial_state_ignored", "h[n] = j->h0 ? j->h0[chain * N + n] : 0.0;", "h[n] = 0.0;"),
     ("decode_without_dt", "*h = abar * *h + step * B[b * N + n] * x[e];", "*h = abar * *h + B[b * N + n] * x[e];"),
     ("decode_no_gate", "out[e] = z ? yt * oracle_silu(z[e]) : yt;", "out[e] = yt;"),
+    ("reset_ignored", "if (rs && rs[t])", "if (0)"),
+    ("reset_after_the_flagged_step", "if (rs && rs[t])", "if (rs && t > 0 && rs[t - 1])"),
+    ("reset_one_step_early", "if (rs && rs[t])", "if (rs && t + 1 < L && rs[t + 1])"),
+    ("reset_ignores_batch", "j->reset ? j->reset + b * L : NULL", "j->reset ? j->reset : NULL"),
+    ("reset_keeps_first_state", "for (int64_t n = 0; n < N; ++n) h[n] = 0.0;",
+     "for (int64_t n = 1; n < N; ++n) h[n] = 0.0;"),
 ]
 
 
