@@ -464,6 +464,8 @@ def run_ours(args, cfg, dcfg, rank, world, local):
         "algorithmic_bytes_per_launch": cnt["bytes"],
     }
 
+    if not args.no_ex:
+        result["ex"] = bench_ex(args, cnt, xd, y, h, sfu, stream)
     if not args.no_decode:
         result["decode"] = bench_decode(args, dcfg, device, peaks)
     if not args.no_e2e:
@@ -477,6 +479,46 @@ def run_ours(args, cfg, dcfg, rank, world, local):
 
         dist.destroy_process_group()
     return result
+
+
+def bench_ex(args, cnt, xd, y, h, sfu, stream) -> dict:
+    """The same workload through mamba_selective_scan_fwd_ex: a starting state
+    and a document boundary every 512 tokens (offset per batch row), timed like
+    the main step.  The extra inputs are 4*B*D*N + B*L bytes."""
+    import torch
+
+    from selective_state_space_140_b300 import abi
+
+    batch, dim, L = xd["u"].shape
+    N = xd["A_log"].shape[1]
+    h0 = torch.randn((batch, dim, N), device=y.device)
+    reset = torch.zeros((batch, L), dtype=torch.uint8, device=y.device)
+    for b in range(batch):
+        reset[b, (97 * b) % 512::512] = 1
+
+    def step():
+        abi.mamba_selective_scan_fwd_ex(xd["u"], xd["delta"], xd["A_log"], xd["B"], xd["C"],
+                                        D=xd["D"], z=xd["z"], delta_bias=xd["delta_bias"],
+                                        softplus=xd["softplus"], h0=h0, reset=reset, y=y,
+                                        last_state=h, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    steps = max(20, min(args.steps, 500))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    e1.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / steps
+    return {"what": "same workload, h0 given, a document boundary every 512 tokens",
+            "us_per_step": round(t * 1e6, 1), "state_updates_per_s": cnt["updates"] / t,
+            "roofline": {"bound": "alu", "achieved": round(cnt["exps"] / t / 1e9, 1),
+                         "peak": round(sfu["ex2_per_s"] / 1e9, 1), "unit": "Gexp/s",
+                         "frac": round(cnt["exps"] / t / sfu["ex2_per_s"], 4), "traffic": None},
+            "steps": steps, "gpu_launches": steps}
 
 
 def bench_decode(args, dcfg, device, peaks) -> dict:
@@ -613,6 +655,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-ex", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     args.steps = max(1, args.steps)

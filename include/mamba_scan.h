@@ -95,7 +95,7 @@ typedef enum {
  * Long sequences of few chains (a grid that would leave at least half of the
  * SMs idle) are split along time: a summary pass per segment, a carry pass
  * and the full pass, the three launched on `stream`.  The carried states
- * (batch * dim * (segments - 1) * (dstate + 1) fp32 values, at most about
+ * (batch * dim * segments * (dstate + 1) fp32 values, at most about
  * 256 * SMs * (dstate + 1) * 4 bytes) live in stream-ordered scratch taken
  * with cudaMallocAsync and returned with cudaFreeAsync on `stream`, so calls
  * on different streams never share it.  If that allocation fails the scan
@@ -135,6 +135,39 @@ int mamba_selective_scan_fwd_noalloc(const void *u, const void *delta, const flo
                                      void *y, float *last_state, int64_t batch, int64_t dim,
                                      int64_t seqlen, int64_t dstate, int io_dtype,
                                      mamba_stream_t stream);
+
+/*
+ * mamba_selective_scan_fwd with a starting state and document boundaries.
+ *
+ * The pages state that Mamba isolates documents by resetting its hidden state
+ * between them (codechina.net overview, section 3.2, point 2 "边界控制"), and
+ * recommend processing sequences beyond 1M tokens block by block (the same
+ * page's deployment notes), which needs the state at the end of one block as
+ * the start of the next.  For every batch b, channel d, state n:
+ *
+ *   h[n] = h0 ? h0[b,d,n] : 0                       before step 0
+ *   at each step t: if (reset && reset[b,t] != 0) h[n] = 0   (token t starts a
+ *   new document), then the step of mamba_selective_scan_fwd.
+ *
+ *   h0    : [batch, dim, dstate] fp32 or NULL (zero start).  It may be the
+ *           same buffer as last_state (continue a stream in place); any other
+ *           overlap with y or last_state is MAMBA_ERR_ALIAS.  Aligned to 4.
+ *   reset : [batch, seqlen] bytes or NULL (no boundaries); shared by all
+ *           channels of a batch row; must not overlap y or last_state.
+ *
+ * Every other argument, layout and error is as for mamba_selective_scan_fwd
+ * (including its split of long sequences of few chains and that split's
+ * stream-ordered scratch).  With h0 and reset NULL the results equal
+ * mamba_selective_scan_fwd's bit for bit.  seqlen == 0 copies h0 (or zeros)
+ * to last_state.  Fast path: dstate 16 with 16-byte aligned rows and a reset
+ * mask aligned to 4 bytes; other shapes run the register-prefetch kernel.
+ */
+int mamba_selective_scan_fwd_ex(const void *u, const void *delta, const float *A_log,
+                                const void *B, const void *C, const float *D, const void *z,
+                                const float *delta_bias, int softplus_flag, const float *h0,
+                                const unsigned char *reset, void *y, float *last_state,
+                                int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                int io_dtype, mamba_stream_t stream);
 
 /*
  * Single-token decode step (recurrent inference: each new token touches only

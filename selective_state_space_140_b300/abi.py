@@ -24,6 +24,7 @@ MAX_DSTATE = 256
 
 # Every symbol include/mamba_scan.h declares.
 EXPORTED = ("mamba_selective_scan_fwd", "mamba_selective_scan_fwd_noalloc",
+            "mamba_selective_scan_fwd_ex",
             "mamba_selective_state_update", "mamba_device_status", "mamba_status_string",
             "mamba_abi_version")
 
@@ -45,6 +46,9 @@ def _declare(lib):
         getattr(lib, name).restype = ci
         getattr(lib, name).argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, vp, fp,
                                        i64, i64, i64, i64, ci, vp]
+    lib.mamba_selective_scan_fwd_ex.restype = ci
+    lib.mamba_selective_scan_fwd_ex.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, fp, vp, vp, fp,
+                                                i64, i64, i64, i64, ci, vp]
     lib.mamba_selective_state_update.restype = ci
     lib.mamba_selective_state_update.argtypes = [fp, vp, vp, fp, vp, vp, fp, vp, fp, ci, vp,
                                                  i64, i64, i64, ci, vp]
@@ -153,8 +157,28 @@ def mamba_selective_scan_fwd_noalloc(u, delta, A_log, B, C, D=None, z=None, delt
                      softplus, y, last_state, want_last_state, stream)
 
 
+def mamba_selective_scan_fwd_ex(u, delta, A_log, B, C, D=None, z=None, delta_bias=None,
+                                softplus=True, h0=None, reset=None, y=None, last_state=None,
+                                want_last_state=True, stream=None):
+    """``mamba_selective_scan_fwd`` from a starting state ``h0`` ([batch, dim,
+    dstate] float32; may be the same tensor as ``last_state`` to continue a
+    stream in place) with document boundaries ``reset`` ([batch, seqlen]
+    uint8 or bool; non-zero at a token that starts a new document: the state
+    restarts from zero before it).  Returns ``(y, last_state)``."""
+    dev = u.device
+    _check(h0, "h0", dev, torch.float32)
+    if reset is not None:
+        _check(reset, "reset", dev)
+        if reset.dtype == torch.bool:
+            reset = reset.view(torch.uint8)
+        if reset.dtype != torch.uint8 or reset.shape != (u.shape[0], u.shape[2]):
+            raise TypeError("reset must be uint8 or bool of shape [batch, seqlen]")
+    return _scan_fwd("mamba_selective_scan_fwd_ex", u, delta, A_log, B, C, D, z, delta_bias,
+                     softplus, y, last_state, want_last_state, stream, h0=h0, reset=reset)
+
+
 def _scan_fwd(entry, u, delta, A_log, B, C, D, z, delta_bias, softplus, y, last_state,
-              want_last_state, stream):
+              want_last_state, stream, h0=None, reset=None):
     dev = u.device
     batch, dim, seqlen = u.shape
     dstate = A_log.shape[-1]
@@ -168,9 +192,10 @@ def _scan_fwd(entry, u, delta, A_log, B, C, D, z, delta_bias, softplus, y, last_
         y = torch.empty_like(u)
     if last_state is None and want_last_state:
         last_state = torch.empty((batch, dim, dstate), device=dev, dtype=torch.float32)
+    ext = (_ptr(h0), _ptr(reset)) if entry.endswith("_ex") else ()
     rc = getattr(load(), entry)(
         _ptr(u), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
-        int(bool(softplus)), _ptr(y), _ptr(last_state), batch, dim, seqlen, dstate, io,
+        int(bool(softplus)), *ext, _ptr(y), _ptr(last_state), batch, dim, seqlen, dstate, io,
         _stream(stream, dev))
     if rc != 0:
         raise MambaError(rc, entry)
@@ -222,6 +247,14 @@ def raw_scan_fwd_noalloc(u, delta, A_log, B, C, D, z, delta_bias, softplus_flag,
     return load().mamba_selective_scan_fwd_noalloc(u, delta, A_log, B, C, D, z, delta_bias,
                                                    softplus_flag, y, last_state, batch, dim,
                                                    seqlen, dstate, io_dtype, stream)
+
+
+def raw_scan_fwd_ex(u, delta, A_log, B, C, D, z, delta_bias, softplus_flag, h0, reset, y,
+                    last_state, batch, dim, seqlen, dstate, io_dtype, stream) -> int:
+    """``mamba_selective_scan_fwd_ex`` with plain integers as pointers."""
+    return load().mamba_selective_scan_fwd_ex(u, delta, A_log, B, C, D, z, delta_bias,
+                                              softplus_flag, h0, reset, y, last_state, batch, dim,
+                                              seqlen, dstate, io_dtype, stream)
 
 
 def raw_state_update(state, x, dt, A_log, B, C, D, z, dt_bias, softplus_flag, out, batch, dim,

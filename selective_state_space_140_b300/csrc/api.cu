@@ -162,6 +162,35 @@ int mamba_selective_scan_fwd_noalloc(const void* u, const void* delta, const flo
     return err == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
 }
 
+int mamba_selective_scan_fwd_ex(const void* u, const void* delta, const float* A_log,
+                                const void* B, const void* C, const float* D, const void* z,
+                                const float* delta_bias, int softplus_flag, const float* h0,
+                                const unsigned char* reset, void* y, float* last_state,
+                                int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                int io_dtype, mamba_stream_t stream) {
+    const int st = check_scan_args(u, delta, A_log, B, C, D, z, delta_bias, y, last_state, batch,
+                                   dim, seqlen, dstate, io_dtype);
+    if (st != MAMBA_OK) return st;
+    if (misaligned(h0, 4)) return MAMBA_ERR_ALIGN;
+    // h0 may be last_state itself (continue a stream in place), but must not
+    // otherwise overlap an output; the reset mask must not overlap one.
+    const Range ry = range_of(y, batch * dim * seqlen, io_size(io_dtype));
+    const Range rs = last_state ? range_of(last_state, batch * dim * dstate, 4) : Range{0, 0};
+    const Range rh = h0 ? range_of(h0, batch * dim * dstate, 4) : Range{0, 0};
+    const Range rr = reset ? range_of(reset, batch * seqlen, 1) : Range{0, 0};
+    if (overlaps(rh, ry) || overlaps(rr, ry) || overlaps(rr, rs)) return MAMBA_ERR_ALIAS;
+    if (overlaps(rh, rs) && static_cast<const void*>(h0) != static_cast<const void*>(last_state))
+        return MAMBA_ERR_ALIAS;
+    if (batch == 0 || dim == 0) return MAMBA_OK;
+
+    mamba::ScanArgs a{u, delta, A_log, B, C, D, z, delta_bias, y, last_state,
+                      batch, dim, seqlen, int(dstate), softplus_flag != 0, h0, reset};
+    const mamba::ScanScratch scratch{nullptr, 0, true};
+    const cudaError_t err = mamba::launch_scan_fwd(a, io_dtype == MAMBA_BF16,
+                                                   reinterpret_cast<cudaStream_t>(stream), scratch);
+    return err == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
+}
+
 int mamba_test_bounded_wait(int polls, mamba_stream_t stream) {
     if (polls < 1 || polls > (1 << 20)) return MAMBA_ERR_SIZE;
     const cudaError_t err =

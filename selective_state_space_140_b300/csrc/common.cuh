@@ -196,6 +196,9 @@ struct ScanArgs {
     int64_t batch, dim, seqlen;
     int dstate;
     int softplus;
+    // mamba_selective_scan_fwd_ex only (nullptr otherwise):
+    const float* h0;             // [batch, dim, dstate] state before step 0
+    const unsigned char* reset;  // [batch, seqlen]: non-zero starts a new document
 };
 
 // A scan split along time into nseg segments of seg_len steps (the last may
@@ -206,8 +209,8 @@ struct SegArgs {
     int seg_len;    // steps per segment, a multiple of 16
     int nseg;       // segments of the sequence (1: no split)
     int grid_nseg;  // segments covered by one launch (nseg, or nseg - 1 for the summary)
-    float* hcarry;  // [batch * dim][nseg - 1][dstate]
-    float* sdt;     // [batch * dim][nseg - 1]
+    float* hcarry;  // [batch * dim][nseg][dstate]: slot s = state entering segment s
+    float* sdt;     // [batch * dim][nseg - 1]: sum of dt over segment s (+inf: a reset)
 };
 
 // Scratch memory the forward scan may use for a split: a caller buffer of

@@ -315,18 +315,29 @@ __device__ __forceinline__ void widen_bc_split(const unsigned char* rawB,
     widen_bc<io_t, NP, T, NTH>(rawB, rawC, sB, sC, N, tid);
 }
 
+// A2 = min(A * log2 e, -kA2Max) so that Abar = 2^(dt * A2) and a step with
+// dt = +inf (a document boundary, see reset_dt) gives Abar = 0 exactly.  The
+// cap changes nothing for |A| >= 1e-30 (A_log >= -69); padded states get
+// A2 = -kA2Max with B = C = 0, so they stay zero.
+constexpr float kA2Max = 1e-30f;
+
+// dt written to the exponent lanes of a step that starts a new document:
+// 2^(+inf * A2) = 0 wipes the state, while dt * u keeps the real dt.
+constexpr float kResetDt = __builtin_inff();
+
 template <int NPL, int G>
 __device__ __forceinline__ void init_state(const ScanArgs& p, int64_t d, bool chain_ok, int g,
                                            f32x2 (&A2)[NPL / 2], f32x2 (&h)[NPL / 2]) {
-    // A2 = -exp(A_log) * log2(e), so that Abar = 2^(dt * A2).
 #pragma unroll
     for (int q = 0; q < NPL / 2; ++q) {
         float a[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int n = g * NPL + 2 * q + e;
-            a[e] = (chain_ok && n < p.dstate) ? -expf(__ldg(p.A_log + d * p.dstate + n)) * kLog2e
-                                               : 0.f;
+            const float v = (chain_ok && n < p.dstate)
+                                ? -expf(__ldg(p.A_log + d * p.dstate + n)) * kLog2e
+                                : 0.f;
+            a[e] = fminf(v, -kA2Max);
         }
         A2[q] = pack2(a[0], a[1]);
         h[q] = splat2(0.f);
@@ -826,9 +837,13 @@ __global__ void __launch_bounds__(NR + NE, MINB)
         for (int q = 0; q < P; ++q) {
             cc[q] = grp + q * C::NGRP;
             init_state<NPL, G>(p, d0 + cc[q], d0 + cc[q] < dim, g, A2[q], h[q]);
-            if (MODE == kScanFull && tseg > 0 && d0 + cc[q] < dim)
-                load_state<NPL, G>(sg.hcarry + ((int64_t(b) * dim + d0 + cc[q]) * nc + tseg - 1) * N,
-                                   N, g, h[q]);
+            if (MODE == kScanFull && d0 + cc[q] < dim) {
+                const int64_t chain = int64_t(b) * dim + d0 + cc[q];
+                if (sg.hcarry)  // split: the carry pass left the entering state in slot tseg
+                    load_state<NPL, G>(sg.hcarry + (chain * sg.nseg + tseg) * N, N, g, h[q]);
+                else if (p.h0)
+                    load_state<NPL, G>(p.h0 + chain * N, N, g, h[q]);
+            }
         }
         for (int k = 0; k < nchunks; ++k) {
             named_sync(kBarReady + (k & 1), NTH);
@@ -848,8 +863,8 @@ __global__ void __launch_bounds__(NR + NE, MINB)
         for (int q = 0; q < P; ++q) {
             if (d0 + cc[q] >= dim) continue;
             const int64_t chain = int64_t(b) * dim + d0 + cc[q];
-            if (MODE == kScanSummary)
-                write_state<NPL, G>(sg.hcarry + (chain * nc + tseg) * N, N, g, h[q]);
+            if (MODE == kScanSummary)  // end state of segment tseg from zero -> slot tseg + 1
+                write_state<NPL, G>(sg.hcarry + (chain * sg.nseg + tseg + 1) * N, N, g, h[q]);
             else if (p.last_state && tseg == sg.nseg - 1)
                 store_state<NPL, G>(p, chain, g, h[q]);
         }
@@ -915,6 +930,12 @@ __global__ void __launch_bounds__(NR + NE, MINB)
         }
         constexpr int BCV = T * NP * C::ES / 32 / 16;  // 16-byte pieces of B or C per lane
         uint4 rbc[BCV];
+        // document boundaries of this lane's PV steps: one byte each (4-byte
+        // aligned: the row length and every offset are multiples of 4)
+        uint32_t rsw = 0;
+        if (kp >= 0 && p.reset && seg * PV < chunk_len(kp))
+            rsw = __ldg(reinterpret_cast<const uint32_t*>(p.reset + int64_t(b) * L + t0 +
+                                                          kp * T + seg * PV));
         if (kp >= 0) {
             wait_copy(&bar[(kp & (S - 1)) * 2 + w], uint32_t(kp / S) & 1u, copy_failed);
             const quad_t* td = reinterpret_cast<const quad_t*>(tile(kp, 1));
@@ -963,7 +984,9 @@ __global__ void __launch_bounds__(NR + NE, MINB)
                     float dt = __fadd_rn(io_elem<io_t>(pd[i], e), bias[i]);
                     if (p.softplus) dt = softplus_io<io_t>(dt);
                     const float du = __fmul_rn(dt, io_elem<io_t>(pu[i], e));
-                    o[i][e] = make_float4(dt, dt, du, du);
+                    // exponent lanes of a step that starts a document: +inf
+                    const float de = ((rsw >> (8 * e)) & 0xffu) ? kResetDt : dt;
+                    o[i][e] = make_float4(de, de, du, du);
                 }
             }
             if (!all_chains || chunk_len(kp) < T) {  // zero steps past the end, dead chains
@@ -1459,6 +1482,8 @@ __global__ void __launch_bounds__(CH* G)
     }
     f32x2 A2[NPL / 2], h[NPL / 2];
     init_state<NPL, G>(p, d, chain_ok, g, A2, h);
+    if (p.h0 && chain_ok) load_state<NPL, G>(p.h0 + (int64_t(b) * dim + d) * N, N, g, h);
+    const unsigned char* rs = p.reset ? p.reset + int64_t(b) * L : nullptr;
 
     // slice s = tid + i*NTH is chain s % CH, 16-byte segment s / CH
     const io_t* dl = static_cast<const io_t*>(p.delta);
@@ -1517,10 +1542,14 @@ __global__ void __launch_bounds__(CH* G)
                 unpack2(dt, dt0, dt1);
                 unpack2(du, du0, du1);
                 const int t = seg * VEC + 2 * q;
-                if (!(live && t < tlen)) dt0 = du0 = 0.f;
-                if (!(live && t + 1 < tlen)) dt1 = du1 = 0.f;
-                sdu[t * CH + du_col<CH>(t, cc)] = make_float4(dt0, dt0, du0, du0);
-                sdu[(t + 1) * CH + du_col<CH>(t + 1, cc)] = make_float4(dt1, dt1, du1, du1);
+                // exponent lane: +inf on a document boundary (Abar = 0)
+                float de0 = dt0, de1 = dt1;
+                if (rs && live && t < tlen && rs[t0 + t]) de0 = kResetDt;
+                if (rs && live && t + 1 < tlen && rs[t0 + t + 1]) de1 = kResetDt;
+                if (!(live && t < tlen)) de0 = dt0 = du0 = 0.f;
+                if (!(live && t + 1 < tlen)) de1 = dt1 = du1 = 0.f;
+                sdu[t * CH + du_col<CH>(t, cc)] = make_float4(de0, de0, du0, du0);
+                sdu[(t + 1) * CH + du_col<CH>(t + 1, cc)] = make_float4(de1, de1, du1, du1);
             }
         }
         prefetch(k + 1, nxt_d, nxt_u, nxt_z);
@@ -1704,6 +1733,7 @@ bool ws_ok(const ScanArgs& a) {
     const int64_t es = sizeof(io_t);
     return a.dstate == C::NP && al16(a.u) && al16(a.delta) && al16(a.z) && al16(a.B) &&
            al16(a.C) && (reinterpret_cast<uintptr_t>(a.y) % (C::PV * es)) == 0 &&
+           (reinterpret_cast<uintptr_t>(a.reset) % 4) == 0 &&
            (a.seqlen * es) % 16 == 0 && a.batch * a.dim <= 0x7fffffff &&
            a.seqlen <= 0x7fffffff;
 }
@@ -1733,23 +1763,27 @@ bool try_ws(const ScanArgs& a, cudaStream_t stream, cudaError_t* err) {
 }
 
 // Carry pass of a segmented scan.  For chain c and state n the state entering
-// segment s + 1 is exp(A_n * sum of dt over s) times the state entering s, plus
-// the end state of s from a zero start (the product of the per-step decays
-// exp(dt_t A_n) over a segment is exp(A_n * sum dt_t)).  Overwrites hcarry[c][s]
-// with the state entering segment s + 1.
-__global__ void __launch_bounds__(256) scan_carry_kernel(const float* A_log, SegArgs sg,
-                                                         int64_t chains, int64_t dim, int N) {
+// segment 0 is h0 (or zero); the state entering segment s + 1 is
+// exp(A_n * sum of dt over s) times the state entering s, plus the end state
+// of s from a zero start, which the summary pass left in slot s + 1 (the
+// product of the per-step decays exp(dt_t A_n) over a segment is
+// exp(A_n * sum dt_t); a document boundary inside s makes the sum +inf and
+// the decay 0).  Leaves the state entering segment s in slot s, for every s.
+__global__ void __launch_bounds__(256) scan_carry_kernel(const float* A_log, const float* h0,
+                                                         SegArgs sg, int64_t chains, int64_t dim,
+                                                         int N) {
     const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (idx >= chains * N) return;
     const int64_t chain = idx / N, d = chain % dim;
     const int n = int(idx % N);
-    const float A2 = -expf(__ldg(A_log + d * N + n)) * kLog2e;
-    const int nc = sg.nseg - 1;
-    float h = 0.f;
-    for (int s = 0; s < nc; ++s) {
-        float* slot = sg.hcarry + (chain * nc + s) * N + n;
-        h = fmaf(ex2_approx(A2 * sg.sdt[chain * nc + s]), h, *slot);
-        *slot = h;
+    const float A2 = fminf(-expf(__ldg(A_log + d * N + n)) * kLog2e, -kA2Max);
+    float* slots = sg.hcarry + chain * sg.nseg * N + n;
+    float h = h0 ? h0[chain * N + n] : 0.f;
+    slots[0] = h;
+    for (int s = 0; s + 1 < sg.nseg; ++s) {
+        // sdt = +inf when segment s holds a document boundary: decay 0
+        h = fmaf(ex2_approx(A2 * sg.sdt[chain * (sg.nseg - 1) + s]), h, slots[(s + 1) * N]);
+        slots[(s + 1) * N] = h;
     }
 }
 
@@ -1793,7 +1827,7 @@ bool try_ws_split(const ScanArgs& a, cudaStream_t stream, const ScanScratch& sc,
     if (nseg < 2) return false;
     const int64_t chains = a.batch * a.dim;
     auto rnd = [](size_t x) { return (x + 255) / 256 * 256; };
-    const size_t hbytes = rnd(size_t(chains) * (nseg - 1) * a.dstate * sizeof(float));
+    const size_t hbytes = rnd(size_t(chains) * nseg * a.dstate * sizeof(float));
     const size_t bytes = hbytes + rnd(size_t(chains) * (nseg - 1) * sizeof(float));
     void* buf = sc.ptr;
     bool owned = false;
@@ -1815,7 +1849,7 @@ bool try_ws_split(const ScanArgs& a, cudaStream_t stream, const ScanScratch& sc,
     if (*err == cudaSuccess) {
         const int64_t threads = chains * a.dstate;
         scan_carry_kernel<<<unsigned((threads + 255) / 256), 256, 0, stream>>>(
-            a.A_log, sg, chains, a.dim, a.dstate);
+            a.A_log, a.h0, sg, chains, a.dim, a.dstate);
         *err = cudaGetLastError();
     }
     if (*err == cudaSuccess) {
@@ -1850,7 +1884,9 @@ bool try_pair_n(const ScanArgs& a, cudaStream_t stream, cudaError_t* err) {
 template <typename io_t, int NPL, int G, int CH, int TREG>
 cudaError_t run(const ScanArgs& a, cudaStream_t stream, bool pair_first) {
     cudaError_t err = cudaSuccess;
-    if (!force_reg()) {
+    // The paired and tensor-map tiles take no initial state or reset mask:
+    // those calls go to the register-prefetch kernel.
+    if (!force_reg() && !a.h0 && !a.reset) {
         if (pair_first && try_pair_n<io_t>(a, stream, &err)) return err;
         if (try_tma<io_t, NPL, G, CH>(a, stream, &err)) return err;
     }

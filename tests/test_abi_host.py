@@ -154,3 +154,22 @@ def test_testing_header_symbols_are_exported(lib):
 @pytest.mark.parametrize("polls", [0, -5, (1 << 20) + 1])
 def test_bounded_wait_hook_rejects_bad_poll_counts(lib, polls):
     assert lib.mamba_test_bounded_wait(polls, None) == 2  # MAMBA_ERR_SIZE, nothing launched
+
+
+def test_ex_entry_validates_like_the_plain_one_and_checks_h0_and_reset(lib):
+    """mamba_selective_scan_fwd_ex shares the plain entry's argument checks
+    (same status for every bad call) and adds its own: h0 aligned to 4 bytes,
+    h0 overlapping y (or part of last_state) and a reset mask overlapping an
+    output are MAMBA_ERR_ALIAS.  All return before any CUDA call."""
+    cases = [dict(u=None), dict(B=None), dict(batch=-1), dict(dstate=0), dict(io_dtype=9),
+             dict(u=P[0] + 1), dict(y=P[0]), dict(last_state=P[2]), dict(batch=0), dict(dim=0)]
+    for over in cases:
+        kw = dict(GOOD)
+        kw.update(over)
+        assert abi.raw_scan_fwd_ex(h0=None, reset=None, **kw) == abi.raw_scan_fwd(**kw), over
+    ex = lambda **o: abi.raw_scan_fwd_ex(**{**GOOD, "h0": P[10], "reset": P[11], **o})
+    assert ex(h0=P[10] + 2) == 4            # misaligned h0
+    assert ex(h0=P[8] + 64) == 8            # h0 inside y
+    assert ex(h0=P[9] + 16) == 8            # h0 straddles last_state
+    assert ex(reset=P[8] + 3) == 8          # reset mask inside y
+    assert ex(reset=P[9]) == 8              # reset mask over last_state
