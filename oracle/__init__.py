@@ -50,6 +50,10 @@ def _declare(lib):
     lib.oracle_selective_state_update_f64.restype = ctypes.c_int
     lib.oracle_selective_state_update_f64.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp,
                                                       ctypes.c_int, dp, i64, i64, i64]
+    lib.oracle_selective_scan_bwd_f64.restype = ctypes.c_int
+    lib.oracle_selective_scan_bwd_f64.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int,
+                                                  dp, dp, dp, dp, dp, dp, dp, dp, dp,
+                                                  i64, i64, i64, i64]
     lib.oracle_hw_threads.restype = ctypes.c_int
     lib.oracle_hw_threads.argtypes = []
     return lib
@@ -120,6 +124,38 @@ def selective_scan(u, delta, A_log, B, C, D=None, z=None, delta_bias=None, softp
     if used < 0:
         raise ValueError(f"oracle_selective_scan_f64 rejected its arguments ({used})")
     return y, hL, used
+
+
+def selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_bias=None,
+                       softplus=True, lib=None):
+    """Gradients of the scan for the output gradient ``dout`` [batch, dim, L]
+    (zero initial state).  Returns a dict with du, ddelta, dA_log, dB, dC and,
+    when the matching input is given, dD, dz, ddelta_bias (float64 arrays in
+    the layouts of the inputs)."""
+    lib = lib or load()
+    u, delta, A_log, B, C, dout = map(_f64, (u, delta, A_log, B, C, dout))
+    D, z, delta_bias = map(_f64, (D, z, delta_bias))
+    batch, dim, L = u.shape
+    N = A_log.shape[1]
+    assert dout.shape == u.shape and B.shape == (batch, L, N) and C.shape == (batch, L, N)
+    g = {k: np.zeros((batch, dim, L)) for k in ("du", "ddelta", "dz")}
+    g["dB"], g["dC"] = np.zeros((batch, L, N)), np.zeros((batch, L, N))
+    g["dA_log"] = np.zeros((dim, N))
+    g["dD"], g["ddelta_bias"] = np.zeros(dim), np.zeros(dim)
+    rc = lib.oracle_selective_scan_bwd_f64(
+        _ptr(u), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+        int(bool(softplus)), _ptr(dout), _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g["dA_log"]),
+        _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["dz"] if z is not None else None),
+        _ptr(g["ddelta_bias"]), batch, dim, L, N)
+    if rc != 0:
+        raise ValueError(f"oracle_selective_scan_bwd_f64 rejected its arguments ({rc})")
+    if z is None:
+        del g["dz"]
+    if D is None:
+        del g["dD"]
+    if delta_bias is None:
+        del g["ddelta_bias"]
+    return g
 
 
 def selective_state_update(state, x, dt, A_log, B, C, D=None, z=None, dt_bias=None,

@@ -167,6 +167,118 @@ int oracle_selective_scan_f64(const double *u, const double *delta, const double
 }
 
 /*
+ * Gradients of the full selective scan (training): given dout = dLoss/dy for
+ * the gated output, the gradients of every input, by the chain rule through
+ * the same recurrence (the codechina.net overview, section 2.2 point 3,
+ * trains by recomputing the forward states in the backward pass; here the
+ * forward states of a chain are simply kept in a buffer).  Per chain:
+ *   forward:  dt_t = softplus(raw_t), Abar_tn = exp(dt_t A_n),
+ *             h_tn = Abar_tn h_{t-1,n} + dt_t B_tn u_t,  y_t = C_t.h_t + D u_t
+ *   reverse:  dy_t = dout_t SiLU(z_t)   (dout_t without a gate)
+ *             dz_t = dout_t y_t SiLU'(z_t),  SiLU'(z) = s (1 + z (1 - s)), s = sigmoid(z)
+ *             g_tn = dy_t C_tn + Abar_{t+1,n} g_{t+1,n}     (adjoint of h_tn)
+ *             dC_tn += dy_t h_tn,   dB_tn += g_tn dt_t u_t,   dD += dy_t u_t
+ *             du_t = dy_t D + sum_n g_tn dt_t B_tn
+ *             ddt_t = sum_n g_tn (A_n Abar_tn h_{t-1,n} + u_t B_tn)
+ *             dA_n += g_tn dt_t Abar_tn h_{t-1,n}
+ *             ddelta_t = ddt_t sigmoid(raw_t) (softplus on) or ddt_t;  dbias += ddelta_t
+ *   dA_log = dA * A  (A = -exp(A_log)).
+ * B, C, A_log, D and the bias are shared, so their gradients are sums over
+ * chains (dB, dC over channels; dA_log, dD, dbias over batches).  Zero
+ * initial state.  Outputs: du, ddelta, dz [batch][dim][seqlen] (dz only with
+ * z), dB, dC [batch][seqlen][dstate], dA_log [dim][dstate], dD, ddelta_bias
+ * [dim]; all are overwritten.  Single-threaded: the shared sums are formed in
+ * a fixed order.  Returns 0, or a negative value on a bad argument.
+ */
+int oracle_selective_scan_bwd_f64(const double *u, const double *delta, const double *A_log,
+                                  const double *B, const double *C, const double *D,
+                                  const double *z, const double *delta_bias, int softplus_flag,
+                                  const double *dout, double *du, double *ddelta,
+                                  double *dA_log, double *dB, double *dC, double *dD,
+                                  double *dz, double *ddelta_bias, int64_t batch, int64_t dim,
+                                  int64_t seqlen, int64_t dstate) {
+    if (!u || !delta || !A_log || !B || !C || !dout || !du || !ddelta || !dA_log || !dB || !dC)
+        return -1;
+    if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 0) return -2;
+    const int64_t L = seqlen, N = dstate;
+    double *hs = (double *)malloc(sizeof(double) * (size_t)(L * N + 1));
+    double *ab = (double *)malloc(sizeof(double) * (size_t)(L * N + 1));
+    double *dts = (double *)malloc(sizeof(double) * (size_t)(L + 1));
+    double *ys = (double *)malloc(sizeof(double) * (size_t)(L + 1));
+    double *A = (double *)malloc(sizeof(double) * (size_t)(N + 1));
+    double *g = (double *)malloc(sizeof(double) * (size_t)(N + 1));
+    double *dA = (double *)malloc(sizeof(double) * (size_t)(dim * N + 1));
+    if (!hs || !ab || !dts || !ys || !A || !g || !dA) {
+        free(hs); free(ab); free(dts); free(ys); free(A); free(g); free(dA);
+        return -3;
+    }
+    for (int64_t i = 0; i < batch * L * N; ++i) dB[i] = dC[i] = 0.0;
+    for (int64_t i = 0; i < dim * N; ++i) dA[i] = 0.0;
+    for (int64_t i = 0; i < dim; ++i) {
+        if (dD) dD[i] = 0.0;
+        if (ddelta_bias) ddelta_bias[i] = 0.0;
+    }
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t d = 0; d < dim; ++d) {
+            const int64_t chain = b * dim + d;
+            const double *uc = u + chain * L, *dl = delta + chain * L, *go = dout + chain * L;
+            const double *zz = z ? z + chain * L : NULL;
+            const double *Bb = B + b * L * N, *Cb = C + b * L * N;
+            const double Dd = D ? D[d] : 0.0, bias = delta_bias ? delta_bias[d] : 0.0;
+            for (int64_t n = 0; n < N; ++n) A[n] = -exp(A_log[d * N + n]);
+            /* forward, keeping every state */
+            for (int64_t t = 0; t < L; ++t) {
+                const double xr = dl[t] + bias;
+                const double dt = softplus_flag ? oracle_softplus(xr) : xr;
+                dts[t] = dt;
+                double acc = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    const double hp = t > 0 ? hs[(t - 1) * N + n] : 0.0;
+                    const double a = exp(dt * A[n]);
+                    ab[t * N + n] = a;
+                    hs[t * N + n] = a * hp + dt * Bb[t * N + n] * uc[t];
+                    acc += Cb[t * N + n] * hs[t * N + n];
+                }
+                ys[t] = acc + Dd * uc[t];
+            }
+            /* reverse */
+            for (int64_t n = 0; n < N; ++n) g[n] = 0.0; /* Abar_{t+1} g_{t+1}, none after L-1 */
+            for (int64_t t = L - 1; t >= 0; --t) {
+                double dy = go[t];
+                if (zz) {
+                    const double s = 1.0 / (1.0 + exp(-zz[t]));
+                    dz[chain * L + t] = go[t] * ys[t] * s * (1.0 + zz[t] * (1.0 - s));
+                    dy = go[t] * zz[t] * s;
+                }
+                if (dD) dD[d] += dy * uc[t];
+                double dut = dy * Dd, ddt = 0.0;
+                const double dt = dts[t];
+                for (int64_t n = 0; n < N; ++n) {
+                    const double gn = dy * Cb[t * N + n] + g[n];
+                    const double hp = t > 0 ? hs[(t - 1) * N + n] : 0.0;
+                    const double a = ab[t * N + n];
+                    dC[(b * L + t) * N + n] += dy * hs[t * N + n];
+                    dB[(b * L + t) * N + n] += gn * dt * uc[t];
+                    dut += gn * dt * Bb[t * N + n];
+                    ddt += gn * (A[n] * a * hp + uc[t] * Bb[t * N + n]);
+                    dA[d * N + n] += gn * dt * a * hp;
+                    g[n] = a * gn;
+                }
+                du[chain * L + t] = dut;
+                const double xr = dl[t] + bias;
+                const double dr = softplus_flag ? ddt / (1.0 + exp(-xr)) : ddt;
+                ddelta[chain * L + t] = dr;
+                if (ddelta_bias) ddelta_bias[d] += dr;
+            }
+        }
+    }
+    for (int64_t d = 0; d < dim; ++d)
+        for (int64_t n = 0; n < N; ++n) dA_log[d * N + n] = dA[d * N + n] * -exp(A_log[d * N + n]);
+    free(hs); free(ab); free(dts); free(ys); free(A); free(g); free(dA);
+    return 0;
+}
+
+/*
  * One decode step ("inference stays RNN-like": each new token touches only the
  * previous state).  state [batch][dim][dstate] is updated in place; x, dt, z
  * and out are [batch][dim]; B, C are [batch][dstate].

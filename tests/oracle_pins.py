@@ -365,6 +365,57 @@ def check_reset_at_start_ignores_h0(lib):
     _close(h1, h0, rtol=0, what="state after a reset on step 0")
 
 
+def _fd_check(lib, softplus, with_opt, seed):
+    """Central differences of the forward oracle's loss sum(dout * y) with
+    respect to every element of every input must equal the gradients of the
+    backward oracle (fp64: steps of 1e-6 leave errors near 1e-9)."""
+    r = _rng(seed)
+    b, d, L, N = 2, 2, 5, 3
+    x = dict(u=r.normal(size=(b, d, L)), delta=r.normal(size=(b, d, L)),
+             A_log=r.normal(size=(d, N)) * 0.5, B=r.normal(size=(b, L, N)),
+             C=r.normal(size=(b, L, N)))
+    if not softplus:  # keep dt positive and moderate
+        x["delta"] = np.abs(x["delta"]) * 0.3 + 0.05
+    if with_opt:
+        x.update(D=r.normal(size=d), z=r.normal(size=(b, d, L)), delta_bias=r.normal(size=d))
+    dout = r.normal(size=(b, d, L))
+
+    def loss(xx):
+        y, _, _ = oracle.selective_scan(xx["u"], xx["delta"], xx["A_log"], xx["B"], xx["C"],
+                                        D=xx.get("D"), z=xx.get("z"),
+                                        delta_bias=xx.get("delta_bias"), softplus=softplus,
+                                        nthreads=1, lib=lib)
+        return float(np.sum(dout * y))
+
+    g = oracle.selective_scan_bwd(x["u"], x["delta"], x["A_log"], x["B"], x["C"], dout,
+                                  D=x.get("D"), z=x.get("z"), delta_bias=x.get("delta_bias"),
+                                  softplus=softplus, lib=lib)
+    names = {"u": "du", "delta": "ddelta", "A_log": "dA_log", "B": "dB", "C": "dC", "D": "dD",
+             "z": "dz", "delta_bias": "ddelta_bias"}
+    eps = 1e-6
+    for k, gk in names.items():
+        if k not in x:
+            assert gk not in g, f"{gk} returned without its input"
+            continue
+        fd = np.zeros_like(x[k])
+        for idx in np.ndindex(x[k].shape):
+            xp = {kk: vv.copy() for kk, vv in x.items()}
+            xm = {kk: vv.copy() for kk, vv in x.items()}
+            xp[k][idx] += eps
+            xm[k][idx] -= eps
+            fd[idx] = (loss(xp) - loss(xm)) / (2 * eps)
+        _close(g[gk], fd, rtol=1e-6, atol=1e-8, what=f"{gk} vs finite differences")
+
+
+def check_backward_finite_differences(lib):
+    _fd_check(lib, softplus=True, with_opt=True, seed=13)
+
+
+def check_backward_finite_differences_plain(lib):
+    """The other branches: softplus off, no gate, no skip, no bias."""
+    _fd_check(lib, softplus=False, with_opt=False, seed=14)
+
+
 ALL_CHECKS = [
     check_delta_zero_limit,
     check_single_step,
@@ -381,4 +432,6 @@ ALL_CHECKS = [
     check_reset_splits_documents,
     check_reset_every_step_is_memoryless,
     check_reset_at_start_ignores_h0,
+    check_backward_finite_differences,
+    check_backward_finite_differences_plain,
 ]

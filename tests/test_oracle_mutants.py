@@ -43,6 +43,19 @@ MUTANTS = [
     ("reset_ignores_batch", "j->reset ? j->reset + b * L : NULL", "j->reset ? j->reset : NULL"),
     ("reset_keeps_first_state", "for (int64_t n = 0; n < N; ++n) h[n] = 0.0;",
      "for (int64_t n = 1; n < N; ++n) h[n] = 0.0;"),
+    ("bwd_gate_derivative_without_z_term", "s * (1.0 + zz[t] * (1.0 - s))", "s"),
+    ("bwd_adjoint_carry_without_decay", "g[n] = a * gn;", "g[n] = gn;"),
+    ("bwd_dB_without_dt", "dB[(b * L + t) * N + n] += gn * dt * uc[t];",
+     "dB[(b * L + t) * N + n] += gn * uc[t];"),
+    ("bwd_dA_uses_updated_state", "dA[d * N + n] += gn * dt * a * hp;",
+     "dA[d * N + n] += gn * dt * a * hs[t * N + n];"),
+    ("bwd_dA_log_sign", "dA[d * N + n] * -exp(A_log[d * N + n])", "dA[d * N + n] * exp(A_log[d * N + n])"),
+    ("bwd_softplus_derivative_missing", "softplus_flag ? ddt / (1.0 + exp(-xr)) : ddt", "ddt"),
+    ("bwd_dC_uses_adjoint", "dC[(b * L + t) * N + n] += dy * hs[t * N + n];",
+     "dC[(b * L + t) * N + n] += gn * hs[t * N + n];"),
+    ("bwd_ddt_without_input_term", "ddt += gn * (A[n] * a * hp + uc[t] * Bb[t * N + n]);",
+     "ddt += gn * (A[n] * a * hp);"),
+    ("bwd_du_without_skip", "double dut = dy * Dd, ddt = 0.0;", "double dut = 0.0, ddt = 0.0;"),
 ]
 
 
