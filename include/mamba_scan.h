@@ -170,6 +170,43 @@ int mamba_selective_scan_fwd_ex(const void *u, const void *delta, const float *A
                                 int io_dtype, mamba_stream_t stream);
 
 /*
+ * Gradients of mamba_selective_scan_fwd (zero initial state) for a given
+ * output gradient `dout`, by recomputation: no intermediate state is kept by
+ * the forward call; this call re-runs the recurrence and takes the adjoint
+ * backwards through it (codechina.net overview, section 2.2, third point,
+ * gradient recomputation).
+ *
+ *   u, delta, A_log, B, C, D, z, delta_bias, softplus_flag, batch, dim,
+ *   seqlen, dstate, io_dtype : exactly as given to the forward call
+ *   dout        : [batch, dim, seqlen] io_dtype, gradient of y
+ *   du, ddelta  : [batch, dim, seqlen] io_dtype, written
+ *   dz          : [batch, dim, seqlen] io_dtype, written; required when z is
+ *                 given, ignored (may be NULL) when z is NULL
+ *   dA_log      : [dim, dstate] fp32, written (gradient w.r.t. A_log)
+ *   dB, dC      : [batch, seqlen, dstate] fp32, written (summed over dim)
+ *   dD          : [dim] fp32 or NULL (not wanted), written
+ *   ddelta_bias : [dim] fp32 or NULL (not wanted), written
+ *
+ * ddelta is the gradient w.r.t. delta (softplus' derivative applied).  The
+ * summed outputs (dA_log, dB, dC, dD, ddelta_bias) are zeroed on `stream`
+ * and accumulated with atomic adds, so their low bits depend on the order in
+ * which blocks finish; du, ddelta and dz are deterministic.  No output may
+ * overlap an input or another output (MAMBA_ERR_ALIAS).
+ *
+ * Scratch: per chain one fp32 state every 16 steps (batch * dim *
+ * ceil(seqlen/16) * dstate * 4 bytes), allocated and freed on `stream` in
+ * the call (stream-ordered), where the page's recomputation keeps O(1).
+ * Errors as for mamba_selective_scan_fwd.
+ */
+int mamba_selective_scan_bwd(const void *u, const void *delta, const float *A_log,
+                             const void *B, const void *C, const float *D, const void *z,
+                             const float *delta_bias, int softplus_flag, const void *dout,
+                             void *du, void *ddelta, void *dz, float *dA_log, float *dB,
+                             float *dC, float *dD, float *ddelta_bias, int64_t batch,
+                             int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
+                             mamba_stream_t stream);
+
+/*
  * Single-token decode step (recurrent inference: each new token touches only
  * the previous state -- tutorial "核心概念"; mhpn.cn article section 3).
  *

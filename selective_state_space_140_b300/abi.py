@@ -24,7 +24,7 @@ MAX_DSTATE = 256
 
 # Every symbol include/mamba_scan.h declares.
 EXPORTED = ("mamba_selective_scan_fwd", "mamba_selective_scan_fwd_noalloc",
-            "mamba_selective_scan_fwd_ex",
+            "mamba_selective_scan_fwd_ex", "mamba_selective_scan_bwd",
             "mamba_selective_state_update", "mamba_device_status", "mamba_status_string",
             "mamba_abi_version")
 
@@ -49,6 +49,9 @@ def _declare(lib):
     lib.mamba_selective_scan_fwd_ex.restype = ci
     lib.mamba_selective_scan_fwd_ex.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, fp, vp, vp, fp,
                                                 i64, i64, i64, i64, ci, vp]
+    lib.mamba_selective_scan_bwd.restype = ci
+    lib.mamba_selective_scan_bwd.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, vp, vp, vp, vp,
+                                             fp, fp, fp, fp, fp, i64, i64, i64, i64, ci, vp]
     lib.mamba_selective_state_update.restype = ci
     lib.mamba_selective_state_update.argtypes = [fp, vp, vp, fp, vp, vp, fp, vp, fp, ci, vp,
                                                  i64, i64, i64, ci, vp]
@@ -202,6 +205,53 @@ def _scan_fwd(entry, u, delta, A_log, B, C, D, z, delta_bias, softplus, y, last_
     return y, last_state
 
 
+def mamba_selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_bias=None,
+                             softplus=True, want_dD=True, want_ddelta_bias=True, grads=None,
+                             stream=None):
+    """Gradients of ``mamba_selective_scan_fwd`` (zero initial state) for the
+    output gradient ``dout``; returns a dict with ``du``, ``ddelta``,
+    ``dA_log``, ``dB``, ``dC`` and, when wanted, ``dz`` (iff ``z`` is given),
+    ``dD`` and ``ddelta_bias``.
+
+    du/ddelta/dz have the io dtype of ``u``; dA_log [dim, dstate], dB/dC
+    [batch, seqlen, dstate], dD/ddelta_bias [dim] are float32 (dB and dC sum
+    over the channels).  ``grads`` may hold preallocated outputs by the same
+    names.  Runs on ``stream`` and does not synchronise."""
+    dev = u.device
+    batch, dim, seqlen = u.shape
+    dstate = A_log.shape[-1]
+    io = _io_dtype(u)
+    for t, n in ((u, "u"), (delta, "delta"), (z, "z"), (B, "B"), (C, "C"), (dout, "dout")):
+        _check(t, n, dev, u.dtype)
+    for t, n in ((A_log, "A_log"), (D, "D"), (delta_bias, "delta_bias")):
+        _check(t, n, dev, torch.float32)
+    g = dict(grads or {})
+    f32 = torch.float32
+    shapes = {"du": (u.shape, u.dtype), "ddelta": (u.shape, u.dtype),
+              "dA_log": ((dim, dstate), f32), "dB": ((batch, seqlen, dstate), f32),
+              "dC": ((batch, seqlen, dstate), f32)}
+    if z is not None:
+        shapes["dz"] = (u.shape, u.dtype)
+    if want_dD:
+        shapes["dD"] = ((dim,), f32)
+    if want_ddelta_bias:
+        shapes["ddelta_bias"] = ((dim,), f32)
+    for k, (shape, dtype) in shapes.items():
+        if g.get(k) is None:
+            g[k] = torch.empty(shape, device=dev, dtype=dtype)
+        _check(g[k], k, dev, dtype)
+        if tuple(g[k].shape) != tuple(shape):
+            raise TypeError(f"{k} must have shape {tuple(shape)}")
+    rc = load().mamba_selective_scan_bwd(
+        _ptr(u), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+        int(bool(softplus)), _ptr(dout), _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g.get("dz")),
+        _ptr(g["dA_log"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g.get("dD")),
+        _ptr(g.get("ddelta_bias")), batch, dim, seqlen, dstate, io, _stream(stream, dev))
+    if rc != 0:
+        raise MambaError(rc, "mamba_selective_scan_bwd")
+    return {k: g[k] for k in shapes}
+
+
 def mamba_selective_state_update(state, x, dt, A_log, B, C, D=None, z=None, dt_bias=None,
                                  softplus=True, out=None, stream=None):
     """One decode step; ``state`` [batch, dim, dstate] fp32 is updated in place.
@@ -263,3 +313,13 @@ def raw_state_update(state, x, dt, A_log, B, C, D, z, dt_bias, softplus_flag, ou
     return load().mamba_selective_state_update(state, x, dt, A_log, B, C, D, z, dt_bias,
                                                softplus_flag, out, batch, dim, dstate, io_dtype,
                                                stream)
+
+
+def raw_scan_bwd(u, delta, A_log, B, C, D, z, delta_bias, softplus_flag, dout, du, ddelta, dz,
+                 dA_log, dB, dC, dD, ddelta_bias, batch, dim, seqlen, dstate, io_dtype,
+                 stream) -> int:
+    """``mamba_selective_scan_bwd`` with plain integers as pointers."""
+    return load().mamba_selective_scan_bwd(u, delta, A_log, B, C, D, z, delta_bias,
+                                           softplus_flag, dout, du, ddelta, dz, dA_log, dB, dC,
+                                           dD, ddelta_bias, batch, dim, seqlen, dstate, io_dtype,
+                                           stream)

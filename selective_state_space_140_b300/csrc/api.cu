@@ -191,6 +191,66 @@ int mamba_selective_scan_fwd_ex(const void* u, const void* delta, const float* A
     return err == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
 }
 
+int mamba_selective_scan_bwd(const void* u, const void* delta, const float* A_log, const void* B,
+                             const void* C, const float* D, const void* z,
+                             const float* delta_bias, int softplus_flag, const void* dout,
+                             void* du, void* ddelta, void* dz, float* dA_log, float* dB,
+                             float* dC, float* dD, float* ddelta_bias, int64_t batch,
+                             int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
+                             mamba_stream_t stream) {
+    if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
+    if (dstate < 1 || dstate > MAMBA_MAX_DSTATE) return MAMBA_ERR_DSTATE;
+    if (!size_ok(batch, dim, seqlen) || !size_ok(batch, seqlen, dstate) ||
+        !size_ok(batch, dim, dstate))
+        return MAMBA_ERR_SIZE;
+    const bool has_elems = batch * dim * seqlen > 0, has_bc = batch * seqlen > 0;
+    if ((has_elems && (!u || !delta || !dout || !du || !ddelta || (z && !dz))) ||
+        (has_bc && (!B || !C || !dB || !dC)) || (dim > 0 && (!A_log || !dA_log)))
+        return MAMBA_ERR_NULL;
+    const size_t es = io_size(io_dtype);
+    if (misaligned(u, es) || misaligned(delta, es) || misaligned(z, es) || misaligned(B, es) ||
+        misaligned(C, es) || misaligned(dout, es) || misaligned(du, es) ||
+        misaligned(ddelta, es) || misaligned(dz, es) || misaligned(A_log, 4) ||
+        misaligned(D, 4) || misaligned(delta_bias, 4) || misaligned(dA_log, 4) ||
+        misaligned(dB, 4) || misaligned(dC, 4) || misaligned(dD, 4) || misaligned(ddelta_bias, 4))
+        return MAMBA_ERR_ALIGN;
+    const int64_t elems = batch * dim * seqlen, nbc = batch * seqlen * dstate;
+    const Range ins[] = {range_of(u, elems, es), range_of(delta, elems, es),
+                         z ? range_of(z, elems, es) : Range{0, 0}, range_of(B, nbc, es),
+                         range_of(C, nbc, es), range_of(A_log, dim * dstate, 4),
+                         D ? range_of(D, dim, 4) : Range{0, 0},
+                         delta_bias ? range_of(delta_bias, dim, 4) : Range{0, 0},
+                         range_of(dout, elems, es)};
+    const Range outs[] = {range_of(du, elems, es), range_of(ddelta, elems, es),
+                          z ? range_of(dz, elems, es) : Range{0, 0},
+                          range_of(dA_log, dim * dstate, 4), range_of(dB, nbc, 4),
+                          range_of(dC, nbc, 4), dD ? range_of(dD, dim, 4) : Range{0, 0},
+                          ddelta_bias ? range_of(ddelta_bias, dim, 4) : Range{0, 0}};
+    for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
+        for (const Range& r : ins)
+            if (overlaps(outs[i], r)) return MAMBA_ERR_ALIAS;
+        for (size_t j = i + 1; j < sizeof(outs) / sizeof(outs[0]); ++j)
+            if (overlaps(outs[i], outs[j])) return MAMBA_ERR_ALIAS;
+    }
+    if (dim == 0) return MAMBA_OK;
+
+    mamba::ScanBwdArgs a{};
+    a.f = mamba::ScanArgs{u, delta, A_log, B, C, D, z, delta_bias, nullptr, nullptr,
+                          batch, dim, seqlen, int(dstate), softplus_flag != 0};
+    a.dout = dout;
+    a.du = du;
+    a.ddelta = ddelta;
+    a.dz = z ? dz : nullptr;
+    a.dA_log = dA_log;
+    a.dB = dB;
+    a.dC = dC;
+    a.dD = dD;
+    a.ddelta_bias = ddelta_bias;
+    const cudaError_t err =
+        mamba::launch_scan_bwd(a, io_dtype == MAMBA_BF16, reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
+}
+
 int mamba_test_bounded_wait(int polls, mamba_stream_t stream) {
     if (polls < 1 || polls > (1 << 20)) return MAMBA_ERR_SIZE;
     const cudaError_t err =

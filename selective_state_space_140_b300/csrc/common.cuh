@@ -238,6 +238,20 @@ struct StateUpdateArgs {
     int softplus;
 };
 
+// Arguments of the backward scan (gradients for dout = dLoss/dy).
+struct ScanBwdArgs {
+    ScanArgs f;          // the forward's inputs (y, last_state, h0, reset unused)
+    const void* dout;    // [batch, dim, L] io
+    void* du;            // [batch, dim, L] io
+    void* ddelta;        // [batch, dim, L] io
+    void* dz;            // [batch, dim, L] io, when z is given
+    float* dA_log;       // [dim, N]
+    float* dB;           // [batch, L, N]
+    float* dC;           // [batch, L, N]
+    float* dD;           // [dim] or nullptr
+    float* ddelta_bias;  // [dim] or nullptr
+};
+
 // Launchers (return the cudaError_t of the launch).
 // cudaErrorMemoryAllocation: the split needs more than a caller buffer holds.
 cudaError_t launch_scan_fwd(const ScanArgs& a, bool bf16, cudaStream_t stream,
@@ -247,6 +261,9 @@ cudaError_t read_and_clear_device_error(unsigned int* word, cudaStream_t stream)
 // Read and clear the decode kernels' device error word (after a synchronise).
 cudaError_t read_and_clear_decode_error(unsigned int* word);
 cudaError_t launch_state_update(const StateUpdateArgs& a, bool bf16, cudaStream_t stream);
+// Zeroes the summed gradients, takes stream-ordered checkpoint scratch, runs
+// the backward kernel and returns the scratch, all on `stream`.
+cudaError_t launch_scan_bwd(const ScanBwdArgs& a, bool bf16, cudaStream_t stream);
 // Test hook: a wait that never completes, given up after `limit` polls.
 cudaError_t launch_bounded_wait_probe(uint32_t limit, cudaStream_t stream);
 

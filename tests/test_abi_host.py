@@ -173,3 +173,38 @@ def test_ex_entry_validates_like_the_plain_one_and_checks_h0_and_reset(lib):
     assert ex(h0=P[9] + 16) == 8            # h0 straddles last_state
     assert ex(reset=P[8] + 3) == 8          # reset mask inside y
     assert ex(reset=P[9]) == 8              # reset mask over last_state
+
+
+Q = [0x7e0000000000 + i * 0x100000000 for i in range(20)]
+BGOOD = dict(u=Q[0], delta=Q[1], A_log=Q[2], B=Q[3], C=Q[4], D=Q[5], z=Q[6], delta_bias=Q[7],
+             softplus_flag=1, dout=Q[8], du=Q[9], ddelta=Q[10], dz=Q[11], dA_log=Q[12], dB=Q[13],
+             dC=Q[14], dD=Q[15], ddelta_bias=Q[16], batch=2, dim=8, seqlen=16, dstate=16,
+             io_dtype=abi.MAMBA_BF16, stream=None)
+
+
+def bwd(**over):
+    return abi.raw_scan_bwd(**{**BGOOD, **over})
+
+
+def test_bwd_entry_validation(lib):
+    """mamba_selective_scan_bwd: required pointers, dz iff z, sizes, dstate,
+    dtype, alignment, and no output overlapping an input or another output.
+    Every case returns before any CUDA call."""
+    for name in ("u", "delta", "A_log", "B", "C", "dout", "du", "ddelta", "dA_log", "dB", "dC"):
+        assert bwd(**{name: None}) == 1, name                    # MAMBA_ERR_NULL
+    assert bwd(dz=None) == 1                                     # z given, dz missing
+    assert bwd(batch=-1) == 2 and bwd(seqlen=1 << 45) == 2       # MAMBA_ERR_SIZE
+    assert bwd(dstate=0) == 3 and bwd(dstate=257) == 3           # MAMBA_ERR_DSTATE
+    assert bwd(io_dtype=4) == 5                                  # MAMBA_ERR_DTYPE
+    assert bwd(du=Q[9] + 1) == 4 and bwd(dB=Q[13] + 2) == 4      # MAMBA_ERR_ALIGN
+    assert bwd(dout=Q[8] + 2, io_dtype=abi.MAMBA_F32) == 4
+    assert bwd(du=Q[0]) == 8                                     # du over u
+    assert bwd(ddelta=Q[8] + 64) == 8                            # ddelta inside dout
+    assert bwd(dB=Q[3]) == 8                                     # dB over B
+    assert bwd(dC=Q[13] + 256) == 8                              # dC inside dB
+    assert bwd(dD=Q[12]) == 8                                    # dD over dA_log
+    assert bwd(dz=Q[9]) == 8                                     # dz over du
+    # optional outputs and a missing z
+    assert bwd(dim=0, dD=None, ddelta_bias=None) == 0
+    assert bwd(dim=0, z=None, dz=None) == 0
+    assert bwd(dim=0, z=None, dz=Q[9]) == 0                      # dz ignored without z

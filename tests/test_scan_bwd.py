@@ -1,0 +1,195 @@
+"""GPU backward scan vs the fp64 oracle's adjoint, through the C ABI.
+
+Every gradient is compared element by element with the metric of the forward
+parity tests (``parity_util.rel_err``: max |gpu - ref| / max(|ref|, 0.1 rms)).
+Tolerances: per-element gradients (du, ddelta, dz) and the sums share one
+bound per io dtype.  fp32 io: 1e-3 -- ten times the forward's bound, because
+the adjoint runs the recurrence a second time (recomputed states feed it) and
+dA_log, dD and the bias gradient add one fp32 term per step over the whole
+sequence and every batch row; measured on B300 the largest error over the
+shapes below and L=4096 was 1.4e-4.  bf16 io: 1e-2 -- du, ddelta and dz are
+rounded to bf16 (relative 2^-9, up to 2^-8 against the 0.1 rms floor), and
+the measured largest error was 3.9e-3; the fp32 sums stay near 1e-4.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import rel_err, sample_chains, to_device
+from selective_state_space_140_b300 import abi, workloads
+
+pytestmark = pytest.mark.gpu
+
+GTOL = {"f32": 1e-3, "bf16": 1e-2}
+PER_ELEMENT = ("du", "ddelta", "dz")
+
+
+def _dout(x, seed):
+    gen = torch.Generator().manual_seed(int(seed) + 99)
+    return torch.randn(x["u"].shape, generator=gen, dtype=torch.float32).to(x["u"].dtype)
+
+
+def _gpu_bwd(x, dout, device, **kw):
+    xd = to_device(x, device)
+    g = abi.mamba_selective_scan_bwd(xd["u"], xd["delta"], xd["A_log"], xd["B"], xd["C"],
+                                     dout.to(device), D=xd["D"], z=xd["z"],
+                                     delta_bias=xd["delta_bias"], softplus=xd["softplus"], **kw)
+    torch.cuda.synchronize()
+    return {k: v.float().cpu().numpy() for k, v in g.items()}
+
+
+def _oracle_bwd(x, dout):
+    f = workloads.to_f64
+    return oracle.selective_scan_bwd(f(x["u"]), f(x["delta"]), f(x["A_log"]), f(x["B"]),
+                                     f(x["C"]), f(dout), D=f(x["D"]), z=f(x["z"]),
+                                     delta_bias=f(x["delta_bias"]), softplus=x["softplus"])
+
+
+def _assert_grads(x, gg, gr, what="", tol=None):
+    tol = GTOL[x["io_dtype"]] if tol is None else tol
+    assert set(gg) == set(gr), (sorted(gg), sorted(gr))
+    errs = {k: rel_err(gg[k], gr[k]) for k in sorted(gr)}
+    bad = {k: e for k, e in errs.items() if e > tol}
+    shown = ", ".join(f"{k} {e:.2e}" for k, e in errs.items())
+    assert not bad, f"{what}: {shown} (tol {tol})"
+    return errs
+
+
+SHAPES = [
+    # batch, dim, L, N, io
+    (1, 1, 1, 16, "f32"), (1, 3, 15, 4, "f32"), (1, 5, 16, 16, "f32"), (2, 7, 17, 16, "bf16"),
+    (1, 33, 33, 16, "f32"), (2, 37, 100, 16, "bf16"), (1, 9, 63, 1, "f32"), (1, 6, 65, 3, "f32"),
+    (2, 10, 70, 8, "f32"), (1, 5, 70, 17, "f32"), (1, 6, 50, 32, "bf16"), (1, 6, 50, 64, "f32"),
+    (1, 4, 40, 100, "f32"), (1, 3, 30, 256, "f32"), (1, 130, 40, 8, "bf16"),
+    (2, 70, 1000, 16, "f32"), (2, 70, 1000, 16, "bf16"), (1, 16, 2049, 16, "f32"),
+]
+
+
+@pytest.mark.parametrize("batch,dim,L,N,io", SHAPES, ids=lambda v: str(v))
+def test_shapes_match_oracle(cuda, batch, dim, L, N, io):
+    seed = batch * 1000 + dim + L + N
+    x = workloads.make_scan_inputs(batch, dim, L, N, io, seed=seed, d_mode="normal")
+    dout = _dout(x, seed)
+    _assert_grads(x, _gpu_bwd(x, dout, cuda), _oracle_bwd(x, dout), what=str((batch, dim, L, N, io)))
+
+
+@pytest.mark.parametrize("with_z,with_D,with_bias", [(False, True, True), (True, False, True),
+                                                      (True, True, False), (False, False, False)])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_optional_inputs(cuda, with_z, with_D, with_bias, io):
+    x = workloads.make_scan_inputs(2, 21, 150, 16, io, seed=7, d_mode="normal", with_z=with_z,
+                                   with_D=with_D, with_bias=with_bias)
+    dout = _dout(x, 7)
+    gg = _gpu_bwd(x, dout, cuda)
+    gr = _oracle_bwd(x, dout)
+    assert ("dz" in gg) == with_z and ("dD" in gr) == with_D
+    # the wrapper returns dD / ddelta_bias even without D / bias: they are still
+    # gradients (of the parameter at zero), which the oracle gives only when the
+    # input exists; compare the ones it gives
+    gg = {k: v for k, v in gg.items() if k in gr}
+    _assert_grads(x, gg, gr, what=f"z={with_z} D={with_D} bias={with_bias}")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_softplus_off(cuda, io):
+    x = workloads.make_scan_inputs(1, 12, 200, 16, io, seed=8, d_mode="normal", with_bias=False)
+    x["delta"] = (x["delta"].float().abs() * 0.05).to(x["delta"].dtype)
+    x["softplus"] = False
+    dout = _dout(x, 8)
+    _assert_grads(x, _gpu_bwd(x, dout, cuda, want_ddelta_bias=False), _oracle_bwd(x, dout),
+                  what="softplus off")
+
+
+def test_large_and_very_negative_steps(cuda):
+    """Biases from -30 (dt ~ 1e-13, softplus' ~ 0) to +25 (dt ~ 25: Abar
+    underflows to zero, softplus' = 1)."""
+    x = workloads.make_scan_inputs(1, 8, 64, 16, "f32", seed=9, d_mode="normal")
+    x["delta_bias"] = torch.linspace(-30.0, 25.0, 8)
+    dout = _dout(x, 9)
+    _assert_grads(x, _gpu_bwd(x, dout, cuda), _oracle_bwd(x, dout), what="extreme steps")
+
+
+def test_zero_output_gradient_gives_zero_gradients(cuda):
+    x = workloads.make_scan_inputs(2, 40, 77, 16, "bf16", seed=10)
+    g = _gpu_bwd(x, torch.zeros_like(x["u"]), cuda)
+    for k, v in g.items():
+        assert not np.any(v), k
+
+
+def test_per_element_gradients_are_deterministic(cuda):
+    x = workloads.make_scan_inputs(2, 70, 300, 16, "bf16", seed=11, d_mode="normal")
+    dout = _dout(x, 11)
+    g1 = _gpu_bwd(x, dout, cuda)
+    g2 = _gpu_bwd(x, dout, cuda)
+    for k in PER_ELEMENT:
+        assert np.array_equal(g1[k], g2[k]), k
+    for k in ("dA_log", "dB", "dC", "dD", "ddelta_bias"):
+        assert rel_err(g2[k], g1[k]) < 1e-5, k
+
+
+def test_preallocated_outputs_are_overwritten(cuda):
+    """Outputs given by the caller start as garbage; the sums are zeroed by the call."""
+    x = workloads.make_scan_inputs(1, 20, 90, 16, "f32", seed=12, d_mode="normal")
+    dout = _dout(x, 12)
+    gr = _oracle_bwd(x, dout)
+    pre = {k: torch.full(v.shape, 7.0, device=cuda, dtype=torch.float32) for k, v in gr.items()}
+    _assert_grads(x, _gpu_bwd(x, dout, cuda, grads=pre), gr, what="preallocated")
+
+
+def test_empty_sizes(cuda):
+    x = workloads.make_scan_inputs(1, 6, 0, 16, "f32", seed=13)
+    g = _gpu_bwd(x, _dout(x, 13), cuda)
+    assert g["du"].shape == (1, 6, 0) and g["dB"].shape == (1, 0, 16)
+    assert not np.any(g["dA_log"]) and not np.any(g["dD"]) and not np.any(g["ddelta_bias"])
+
+
+def test_gradient_check_against_forward_kernel(cuda):
+    """The backward is the derivative of the CUDA forward: a central difference
+    of sum(dout * y) along a random direction, both ends through the forward
+    kernel at fp32, matches <gradient, direction> from the backward kernel."""
+    x = workloads.make_scan_inputs(1, 16, 64, 16, "f32", seed=14, d_mode="normal")
+    dout = _dout(x, 14)
+    xd = to_device(x, cuda)
+    g = abi.mamba_selective_scan_bwd(xd["u"], xd["delta"], xd["A_log"], xd["B"], xd["C"],
+                                     dout.to(cuda), D=xd["D"], z=xd["z"],
+                                     delta_bias=xd["delta_bias"])
+    gen = torch.Generator().manual_seed(15)
+    for name in ("u", "delta", "B", "C", "z", "A_log"):
+        v = torch.randn(x[name].shape, generator=gen).to(cuda)
+        eps = 1e-3
+
+        def loss(sign):
+            xs = dict(xd)
+            xs[name] = (xd[name].double() + sign * eps * v.double()).float().contiguous()
+            y, _ = abi.mamba_selective_scan_fwd(xs["u"], xs["delta"], xs["A_log"], xs["B"],
+                                                xs["C"], D=xs["D"], z=xs["z"],
+                                                delta_bias=xs["delta_bias"])
+            return float((y.double() * dout.to(cuda).double()).sum())
+
+        fd = (loss(1) - loss(-1)) / (2 * eps)
+        an = float((g["d" + name].double() * v.double()).sum())
+        assert abs(fd - an) <= 2e-3 * max(1.0, abs(an)), (name, fd, an)
+
+
+def test_full_size_layer_on_sampled_chains(cuda):
+    """Mamba-1.4B-style layer (batch 4, d_inner 4096, L=4096, N=16, bf16): the
+    per-element gradients of sampled chains, and dA_log / dD / the bias
+    gradient of sampled channels (each a sum over the 4 batch rows), against
+    the oracle run on exactly those chains."""
+    cfg = workloads.SCAN_CONFIGS["mamba1p4b_bf16"]
+    x = workloads.make_config_inputs(cfg)
+    dout = _dout(x, cfg.seed)
+    gg = _gpu_bwd(x, dout, cuda)
+    chans = sorted({d for _, d in sample_chains(cfg.batch, cfg.dim, 6, seed=cfg.seed)})
+    f = workloads.to_f64
+    for d in chans:
+        sl = lambda t: None if t is None else t[:, d:d + 1]
+        sd = lambda t: None if t is None else t[d:d + 1]
+        gr = oracle.selective_scan_bwd(f(sl(x["u"])), f(sl(x["delta"])), f(x["A_log"][d:d + 1]),
+                                       f(x["B"]), f(x["C"]), f(sl(dout)), D=f(sd(x["D"])),
+                                       z=f(sl(x["z"])), delta_bias=f(sd(x["delta_bias"])))
+        part = {k: gg[k][:, d:d + 1] for k in PER_ELEMENT}
+        part.update({"dA_log": gg["dA_log"][d:d + 1], "dD": gg["dD"][d:d + 1],
+                     "ddelta_bias": gg["ddelta_bias"][d:d + 1]})
+        _assert_grads(x, part, {k: gr[k] for k in part}, what=f"channel {d}")
