@@ -11,16 +11,23 @@
 //                     from its checkpoint into shared memory, then run the
 //                     adjoint recurrence backwards through the chunk
 //                       g_tn = dy_t C_tn + Abar_{t+1,n} g_{t+1,n}
-//                     and form every gradient of the step (see the fp64
-//                     oracle, which writes the same chain rule out).
+//                     and form every gradient of the step (the fp64 oracle
+//                     writes the same chain rule out).
+//
+// Latency: every chunk's raw inputs (delta, u, dout, z, B, C and the
+// checkpoint) are fetched into registers one chunk ahead, so the loads of
+// chunk k-1 are in flight while chunk k computes; loops have compile-time trip
+// counts (a short last chunk is padded with dt = u = dout = B = C = 0 steps,
+// which leave the state and every gradient unchanged).  The values of one
+// element (a chain and a step) stay in the registers of the thread that
+// loaded them; only what other threads read goes through shared memory.
 //
 // B, C, A_log, D and the bias are shared by many chains, so their gradients
 // are sums: dB and dC over the channels of a batch row are reduced across the
 // warp's chains with shuffles (a halving "transpose" reduction that leaves one
 // sum per lane) and across the CTA's warps in shared memory, then added to the
-// fp32 outputs with one global atomic per value and chunk; dA_log, dD and the
-// bias gradient accumulate in registers over the whole sequence and are added
-// once at the end.
+// fp32 outputs with vector atomics; dA_log, dD and the bias gradient
+// accumulate over the whole sequence and are added once at the end.
 #include <cstdlib>
 
 #include "common.cuh"
@@ -39,76 +46,85 @@ struct BwdCfg {
     static constexpr int NW = NTH / 32;       // warps
     static constexpr int NP = NPL * G;        // states per chain, padded
     static constexpr int NQ = NPL / 4;        // float4 per thread per step
+    static constexpr int kE = T * CH;         // elements (chain, step) per chunk
+    // elements per thread: EPT consecutive steps of one chain
+    static constexpr int EPT = (kE + NTH - 1) / NTH;
+    static constexpr int BPT = (T * NP + NTH - 1) / NTH;  // B (and C) values per thread
     // shared memory (floats)
-    static constexpr int kE = T * CH;                 // one per-element field
-    static constexpr int oDt = 0, oDu = kE, oU = 2 * kE, oDy = 3 * kE, oDout = 4 * kE;
-    static constexpr int oSilu = 5 * kE, oDsilu = 6 * kE, oSp = 7 * kE;
-    static constexpr int oGu = 8 * kE, oGdt = 9 * kE;  // reduced sum_n g B, sum_n g (...)
-    static constexpr int oB = 10 * kE, oC = oB + T * NP;
-    static constexpr int oH = oC + T * NP;              // [T][NQ][NTH] float4 states
-    static constexpr int oYs = oH + T * NQ * NTH * 4;  // [T][NTH] partial C.h
-    static constexpr int oRed = oYs + T * NTH;         // [NW][T][2][NP] per-warp dB/dC sums
-    static constexpr int kFloats = oRed + NW * T * 2 * NP;
+    static constexpr int oDt = 0, oU = kE, oDy = 2 * kE;
+    static constexpr int oGu = 3 * kE, oGdt = 4 * kE;   // reduced sum_n g B, sum_n g (...)
+    static constexpr int oB = 5 * kE, oC = oB + T * NP;
+    static constexpr int oH = oC + T * NP;               // [T][NQ][NTH] float4 states
+    static constexpr int oX = oH + T * NQ * NTH * 4;     // [T][NTH] C.h partials, then
+    static constexpr int kRed = NW * T * 2 * NP;         // [NW][T][2][NP] per-warp dB/dC sums
+    static constexpr int kX = T * NTH > kRed ? T * NTH : kRed;
+    static constexpr int kFloats = oX + kX;
     static constexpr size_t kSmem = size_t(kFloats) * 4;
     static_assert(NPL % 4 == 0, "states per lane in whole float4");
+    static_assert(T % EPT == 0, "a thread's elements stay within one chain");
+    static_assert(oH % 4 == 0, "float4 state tiles");
 };
 
 struct BwdArgs : ScanBwdArgs {
     float* ckpt;  // [batch * dim][nchunks][N] scratch: state at each chunk start
 };
 
-// Per-element inputs of chunk k into shared memory: dt (and, for the reverse
-// phase, u, dout and the gate values).  Chains past dim and steps past L get
-// dt = 0, u = 0, dout = 0, so they leave every gradient untouched.
-template <typename io_t, int NPL, int G, bool REVERSE>
-__device__ __forceinline__ void load_chunk(const BwdArgs& a, float* sm, int b, int64_t d0,
-                                           int64_t k, int tid) {
+// One chunk's raw inputs as fetched (converted to float only when staged, so
+// that no instruction waits on the loads before the chunk is used).
+template <typename io_t, int NPL, int G>
+struct Raw {
+    using C = BwdCfg<io_t, NPL, G>;
+    io_t dl[C::EPT], u[C::EPT], go[C::EPT], z[C::EPT];
+    io_t B[C::BPT], Cc[C::BPT];
+    float hs[NPL];  // checkpoint: the state at the chunk's start
+};
+
+template <typename io_t>
+__device__ __forceinline__ float to_f(io_t v);
+template <>
+__device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// Issue the loads of chunk k (REV: everything the reverse phase needs; else
+// only delta, u and B).  Out-of-range elements read as zero.
+template <typename io_t, int NPL, int G, bool REV>
+__device__ __forceinline__ void fetch(const BwdArgs& a, Raw<io_t, NPL, G>& r, int b, int64_t d0,
+                                      int64_t k, int tid, const float* ck, bool chain_ok, int g) {
     using C = BwdCfg<io_t, NPL, G>;
     const ScanArgs& p = a.f;
     const int64_t L = p.seqlen, dim = p.dim;
     const int N = p.dstate;
     const int64_t t0 = k * C::T;
-    for (int e = tid; e < C::kE; e += C::NTH) {
-        const int c = e / C::T, t = e % C::T;   // consecutive threads walk time
-        const int64_t d = d0 + c;
-        const bool ok = d < dim && t0 + t < L;
-        const int64_t idx = (int64_t(b) * dim + (ok ? d : 0)) * L + (ok ? t0 + t : 0);
-        float dt = 0.f, u = 0.f, sp = 0.f;
-        if (ok) {
-            const float raw = Io<io_t>::load(static_cast<const io_t*>(p.delta) + idx) +
-                              (p.delta_bias ? __ldg(p.delta_bias + d) : 0.f);
-            dt = p.softplus ? (sizeof(io_t) == 2 ? softplus_fast(raw) : softplus_accurate(raw))
-                            : raw;
-            sp = p.softplus ? rcp_approx(1.f + ex2_approx(-raw * kLog2e)) : 1.f;  // softplus'
-            u = Io<io_t>::load(static_cast<const io_t*>(p.u) + idx);
-        }
-        const int s = t * C::CH + c;  // [t][c]
-        sm[C::oDt + s] = dt;
-        sm[C::oDu + s] = dt * u;
-        if constexpr (REVERSE) {
-            sm[C::oU + s] = u;
-            sm[C::oSp + s] = sp;
-            const float go = ok ? Io<io_t>::load(static_cast<const io_t*>(a.dout) + idx) : 0.f;
-            sm[C::oDout + s] = go;
-            float silu = 1.f, dsilu = 0.f;
-            if (p.z && ok) {
-                const float z = Io<io_t>::load(static_cast<const io_t*>(p.z) + idx);
-                const float sg = rcp_approx(1.f + ex2_approx(-z * kLog2e));
-                silu = z * sg;
-                dsilu = sg * (1.f + z * (1.f - sg));
-            }
-            sm[C::oSilu + s] = silu;
-            sm[C::oDsilu + s] = dsilu;
+    const io_t zero = io_t(0.f);
+#pragma unroll
+    for (int j = 0; j < C::EPT; ++j) {
+        const int e = tid * C::EPT + j;
+        const int c = e / C::T, t = e % C::T;
+        const bool ok = e < C::kE && d0 + c < dim && t0 + t < L;
+        const int64_t idx = ok ? (int64_t(b) * dim + d0 + c) * L + t0 + t : 0;
+        r.dl[j] = ok ? __ldg(static_cast<const io_t*>(p.delta) + idx) : zero;
+        r.u[j] = ok ? __ldg(static_cast<const io_t*>(p.u) + idx) : zero;
+        if constexpr (REV) {
+            r.go[j] = ok ? __ldg(static_cast<const io_t*>(a.dout) + idx) : zero;
+            r.z[j] = (ok && p.z) ? __ldg(static_cast<const io_t*>(p.z) + idx) : zero;
         }
     }
-    // B (and C) of the chunk, fp32 [t][n], zero past L and past N
     const io_t* Bg = static_cast<const io_t*>(p.B) + int64_t(b) * L * N;
     const io_t* Cg = static_cast<const io_t*>(p.C) + int64_t(b) * L * N;
-    for (int e = tid; e < C::T * C::NP; e += C::NTH) {
+#pragma unroll
+    for (int j = 0; j < C::BPT; ++j) {
+        const int e = tid + j * C::NTH;
         const int t = e / C::NP, n = e % C::NP;
-        const bool ok = n < N && t0 + t < L;
-        sm[C::oB + e] = ok ? Io<io_t>::load(Bg + (t0 + t) * N + n) : 0.f;
-        if constexpr (REVERSE) sm[C::oC + e] = ok ? Io<io_t>::load(Cg + (t0 + t) * N + n) : 0.f;
+        const bool ok = e < C::T * C::NP && n < N && t0 + t < L;
+        const int64_t off = ok ? (t0 + t) * N + n : 0;
+        r.B[j] = ok ? __ldg(Bg + off) : zero;
+        if constexpr (REV) r.Cc[j] = ok ? __ldg(Cg + off) : zero;
+    }
+    if constexpr (REV) {
+#pragma unroll
+        for (int i = 0; i < NPL; ++i)
+            r.hs[i] = (chain_ok && g * NPL + i < N) ? ck[k * N + g * NPL + i] : 0.f;
     }
 }
 
@@ -143,13 +159,13 @@ struct ChainSum {
 };
 
 template <typename io_t, int NPL, int G>
-__global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const int dblocks) {
+__global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const int dblocks,
+                                                         const bool vec_red) {
     using C = BwdCfg<io_t, NPL, G>;
     constexpr int T = C::T, NTH = C::NTH, CH = C::CH, NP = C::NP, NQ = C::NQ, CPW = C::CPW;
+    constexpr int EPT = C::EPT;
     constexpr int V = 2 * NPL;  // dB and dC values per lane and step
     extern __shared__ __align__(16) float sm[];
-    float* sDacc = sm + C::kFloats;       // [CH] per-chain sum of dy * u
-    float* sBacc = sDacc + CH;            // [CH] per-chain sum of ddelta
     float4* sH = reinterpret_cast<float4*>(sm + C::oH);
 
     const ScanArgs& p = a.f;
@@ -157,8 +173,14 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
     const int N = p.dstate;
     const int b = blockIdx.x / dblocks;
     const int64_t d0 = int64_t(blockIdx.x % dblocks) * CH;
+    // recurrence role: chain c, states g * NPL ..; element role: chain ce, steps te0 ..
     const int tid = threadIdx.x, c = tid / G, g = tid % G;
     const int warp = tid / 32, cw = (tid % 32) / G;
+    const int e0 = tid * EPT, ce = e0 / T, te0 = e0 % T;
+    const bool e_live = e0 < C::kE && d0 + ce < dim;  // this thread owns real elements
+    const int64_t de = e_live ? d0 + ce : 0;
+    const float e_bias = (e_live && p.delta_bias) ? __ldg(p.delta_bias + de) : 0.f;
+    const float e_D = (e_live && p.D) ? __ldg(p.D + de) : 0.f;
     const int64_t d = d0 + c;
     const bool chain_ok = d < dim;
     const int64_t chain = int64_t(b) * dim + (chain_ok ? d : 0);
@@ -173,21 +195,51 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
         A2[i] = A[i] * kLog2e;
         h[i] = 0.f;
     }
-    for (int e = tid; e < 2 * CH; e += NTH) sDacc[e] = 0.f;
 
+    // dt (and softplus') of element j of this thread in chunk k; zero past the data
+    auto step_of = [&](float raw_delta, int64_t k, int j, float& sp) {
+        const bool ok = e_live && k * T + te0 + j < L;
+        const float raw = raw_delta + e_bias;
+        float dt = raw;
+        sp = 1.f;
+        if (p.softplus) {
+            dt = sizeof(io_t) == 2 ? softplus_fast(raw) : softplus_accurate(raw);
+            sp = rcp_approx(1.f + ex2_approx(-raw * kLog2e));
+        }
+        if (!ok) dt = sp = 0.f;
+        return dt;
+    };
+
+    Raw<io_t, NPL, G> r;
     // ---------------- forward phase: checkpoints ----------------
+    fetch<io_t, NPL, G, false>(a, r, b, d0, 0, tid, ck, chain_ok, g);
     for (int64_t k = 0; k < nchunks; ++k) {
         __syncthreads();
-        load_chunk<io_t, NPL, G, false>(a, sm, b, d0, k, tid);
-        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) {
+            float sp;
+            const float dt = step_of(to_f(r.dl[j]), k, j, sp);
+            if (e0 + j < C::kE) {
+                sm[C::oDt + (te0 + j) * CH + ce] = dt;
+                sm[C::oU + (te0 + j) * CH + ce] = dt * to_f(r.u[j]);  // dt u
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < C::BPT; ++j)
+            if (tid + j * NTH < T * NP) sm[C::oB + tid + j * NTH] = to_f(r.B[j]);
         if (chain_ok) {
 #pragma unroll
             for (int i = 0; i < NPL; ++i)
                 if (g * NPL + i < N) ck[k * N + g * NPL + i] = h[i];
         }
-        const int tlen = L - k * T < T ? int(L - k * T) : T;
-        for (int t = 0; t < tlen; ++t) {
-            const float dt = sm[C::oDt + t * CH + c], du = sm[C::oDu + t * CH + c];
+        __syncthreads();
+        if (k + 1 < nchunks)
+            fetch<io_t, NPL, G, false>(a, r, b, d0, k + 1, tid, ck, chain_ok, g);
+        else
+            fetch<io_t, NPL, G, true>(a, r, b, d0, k, tid, ck, chain_ok, g);
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+            const float dt = sm[C::oDt + t * CH + c], du = sm[C::oU + t * CH + c];
 #pragma unroll
             for (int i = 0; i < NPL; ++i)
                 h[i] = fmaf(ex2_approx(dt * A2[i]), h[i], du * sm[C::oB + t * NP + g * NPL + i]);
@@ -198,24 +250,43 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
     float gc[NPL], dA[NPL];  // Abar_{t+1} g_{t+1}; sum of g dt Abar h_{t-1}
 #pragma unroll
     for (int i = 0; i < NPL; ++i) gc[i] = dA[i] = 0.f;
+    float accD = 0.f, accB = 0.f;  // this thread's elements: sums of dy u and ddelta
     for (int64_t k = nchunks - 1; k >= 0; --k) {
-        __syncthreads();
-        load_chunk<io_t, NPL, G, true>(a, sm, b, d0, k, tid);
-        float hs[NPL];  // state at the start of the chunk
-#pragma unroll
-        for (int i = 0; i < NPL; ++i)
-            hs[i] = (chain_ok && g * NPL + i < N) ? ck[k * N + g * NPL + i] : 0.f;
-        __syncthreads();
-        const int tlen = L - k * T < T ? int(L - k * T) : T;
         const int64_t t0 = k * T;
+        const int tlen = L - t0 < T ? int(L - t0) : T;
+        __syncthreads();
+        // stage chunk k: dt and u for every thread, the rest stays in registers
+        float e_sp[EPT], e_go[EPT], e_z[EPT], hs[NPL];
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) {
+            const float dt = step_of(to_f(r.dl[j]), k, j, e_sp[j]);
+            e_go[j] = to_f(r.go[j]);
+            e_z[j] = to_f(r.z[j]);
+            if (e0 + j < C::kE) {
+                sm[C::oDt + (te0 + j) * CH + ce] = dt;
+                sm[C::oU + (te0 + j) * CH + ce] = to_f(r.u[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < C::BPT; ++j)
+            if (tid + j * NTH < T * NP) {
+                sm[C::oB + tid + j * NTH] = to_f(r.B[j]);
+                sm[C::oC + tid + j * NTH] = to_f(r.Cc[j]);
+            }
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) hs[i] = r.hs[i];
+        __syncthreads();
+        if (k > 0) fetch<io_t, NPL, G, true>(a, r, b, d0, k - 1, tid, ck, chain_ok, g);
 
         // recompute the chunk's states (kept in shared memory) and C.h partials
         {
             float hh[NPL];
 #pragma unroll
             for (int i = 0; i < NPL; ++i) hh[i] = hs[i];
-            for (int t = 0; t < tlen; ++t) {
-                const float dt = sm[C::oDt + t * CH + c], du = sm[C::oDu + t * CH + c];
+#pragma unroll
+            for (int t = 0; t < T; ++t) {
+                const float dt = sm[C::oDt + t * CH + c];
+                const float du = dt * sm[C::oU + t * CH + c];
                 float acc = 0.f;
 #pragma unroll
                 for (int i = 0; i < NPL; ++i) {
@@ -227,35 +298,37 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
                 for (int q = 0; q < NQ; ++q)
                     sH[(t * NQ + q) * NTH + tid] =
                         make_float4(hh[4 * q], hh[4 * q + 1], hh[4 * q + 2], hh[4 * q + 3]);
-                sm[C::oYs + t * NTH + tid] = acc;
+                sm[C::oX + t * NTH + tid] = acc;
             }
         }
         __syncthreads();
 
-        // per element: y = C.h + D u, the gate's gradient, dy
-        for (int e = tid; e < C::kE; e += NTH) {
-            const int ce = e / T, t = e % T;
-            const int64_t de = d0 + ce;
-            if (t >= tlen) continue;
-            const int s = t * CH + ce;
+        // this thread's elements: y = C.h + D u, the gate's gradient, dy
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) {
+            if (e0 + j >= C::kE) continue;
+            const int t = te0 + j, s = t * CH + ce;
             float ys = 0.f;
 #pragma unroll
-            for (int gg = 0; gg < G; ++gg) ys += sm[C::oYs + t * NTH + ce * G + gg];
-            const float u = sm[C::oU + s], go = sm[C::oDout + s];
-            const float y = p.D && de < dim ? fmaf(__ldg(p.D + de), u, ys) : ys;
+            for (int gg = 0; gg < G; ++gg) ys += sm[C::oX + t * NTH + ce * G + gg];
+            const float y = fmaf(e_D, sm[C::oU + s], ys);
+            const float go = e_go[j];
+            float dy = go;
             if (p.z) {
-                if (de < dim)
+                const float z = e_z[j];
+                const float sg = rcp_approx(1.f + ex2_approx(-z * kLog2e));
+                if (e_live && t < tlen)
                     Io<io_t>::store(static_cast<io_t*>(a.dz) + (int64_t(b) * dim + de) * L + t0 + t,
-                                    go * y * sm[C::oDsilu + s]);
-                sm[C::oDy + s] = go * sm[C::oSilu + s];
-            } else {
-                sm[C::oDy + s] = go;
+                                    go * y * (sg * (1.f + z * (1.f - sg))));
+                dy = go * (z * sg);
             }
+            sm[C::oDy + s] = dy;
         }
         __syncthreads();
 
         // adjoint, backwards through the chunk
-        for (int t = tlen - 1; t >= 0; --t) {
+#pragma unroll
+        for (int t = T - 1; t >= 0; --t) {
             const int s = t * CH + c;
             const float dy = sm[C::oDy + s], dt = sm[C::oDt + s], u = sm[C::oU + s];
             const float dtu = dt * u;
@@ -280,14 +353,15 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
                 const float Bn = sm[C::oB + t * NP + n], Cn = sm[C::oC + t * NP + n];
                 const float ab = ex2_approx(dt * A2[i]);
                 const float gn = fmaf(dy, Cn, gc[i]);
-                const float ahp = ab * hp[i];
-                v[i] = gn * dtu;        // dB
+                const float w = gn * (ab * hp[i]);
+                v[i] = gn * dtu;          // dB
                 v[NPL + i] = dy * hc[i];  // dC
                 gu = fmaf(gn, Bn, gu);
-                gd = fmaf(gn, fmaf(A[i], ahp, u * Bn), gd);
-                dA[i] = fmaf(gn * dt, ahp, dA[i]);
+                gd = fmaf(A[i], w, gd);
+                dA[i] = fmaf(dt, w, dA[i]);
                 gc[i] = ab * gn;
             }
+            gd = fmaf(u, gu, gd);  // sum_n g (A Abar h_{t-1} + u B)
 #pragma unroll
             for (int off = G / 2; off > 0; off /= 2) {
                 gu += __shfl_xor_sync(0xffffffffu, gu, off);
@@ -298,7 +372,7 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
                 sm[C::oGdt + s] = gd;
             }
             ChainSum<V, CPW / 2, G>::run(v, cw);
-            float* red = sm + C::oRed + (warp * T + t) * 2 * NP;  // [q][n]
+            float* red = sm + C::oX + (warp * T + t) * 2 * NP;  // [q][n]
             if constexpr (V >= CPW) {
                 constexpr int K = V / CPW;
 #pragma unroll
@@ -316,69 +390,93 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
         }
         __syncthreads();
 
-        // per element: du, ddelta; per chain: sums for dD and the bias gradient
-        for (int e = tid; e < C::kE; e += NTH) {
-            const int ce = e / T, t = e % T;
-            const int64_t de = d0 + ce;
-            if (t >= tlen || de >= dim) continue;
+        // this thread's elements: du, ddelta, and the sums for dD and the bias
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) {
+            const int t = te0 + j;
+            if (!(e_live && t < tlen)) continue;
             const int s = t * CH + ce;
             const int64_t idx = (int64_t(b) * dim + de) * L + t0 + t;
-            const float dy = sm[C::oDy + s], u = sm[C::oU + s];
-            const float du = fmaf(sm[C::oDt + s], sm[C::oGu + s],
-                                  p.D ? dy * __ldg(p.D + de) : 0.f);
-            const float dr = sm[C::oGdt + s] * sm[C::oSp + s];
+            const float dy = sm[C::oDy + s];
+            const float du = fmaf(sm[C::oDt + s], sm[C::oGu + s], dy * e_D);
+            const float dr = sm[C::oGdt + s] * e_sp[j];
             Io<io_t>::store(static_cast<io_t*>(a.du) + idx, du);
             Io<io_t>::store(static_cast<io_t*>(a.ddelta) + idx, dr);
-            atomicAdd(&sDacc[ce], dy * u);
-            atomicAdd(&sBacc[ce], dr);
+            accD = fmaf(dy, sm[C::oU + s], accD);
+            accB += dr;
         }
-        // dB, dC of the chunk: sum over the warps, then one atomic per value
-        for (int e = tid; e < T * 2 * NP; e += NTH) {
-            const int t = e / (2 * NP), q = (e / NP) % 2, n = e % NP;
-            if (t >= tlen || n >= N) continue;
-            float sum = 0.f;
+        // dB, dC of the chunk: sum over the warps, then one atomic per value (or 4)
+        const float* red = sm + C::oX;
+        float* dBg = a.dB + (int64_t(b) * L + t0) * N;
+        float* dCg = a.dC + (int64_t(b) * L + t0) * N;
+        if (vec_red) {
+            constexpr int NP4 = NP / 4;
+            for (int e = tid; e < T * 2 * NP4; e += NTH) {
+                const int t = e / (2 * NP4), q = (e / NP4) % 2, n = (e % NP4) * 4;
+                if (t >= tlen || n >= N) continue;
+                float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int w = 0; w < C::NW; ++w) sum += sm[C::oRed + (w * T + t) * 2 * NP + q * NP + n];
-            atomicAdd((q ? a.dC : a.dB) + (int64_t(b) * L + t0 + t) * N + n, sum);
+                for (int w = 0; w < C::NW; ++w) {
+                    const float4 x =
+                        *reinterpret_cast<const float4*>(red + (w * T + t) * 2 * NP + q * NP + n);
+                    sum.x += x.x; sum.y += x.y; sum.z += x.z; sum.w += x.w;
+                }
+                atomicAdd(reinterpret_cast<float4*>((q ? dCg : dBg) + t * N + n), sum);
+            }
+        } else {
+            for (int e = tid; e < T * 2 * NP; e += NTH) {
+                const int t = e / (2 * NP), q = (e / NP) % 2, n = e % NP;
+                if (t >= tlen || n >= N) continue;
+                float sum = 0.f;
+#pragma unroll
+                for (int w = 0; w < C::NW; ++w) sum += red[(w * T + t) * 2 * NP + q * NP + n];
+                atomicAdd((q ? dCg : dBg) + t * N + n, sum);
+            }
         }
     }
 
-    // dA_log = dA * A (A = -exp(A_log)); dD, the bias gradient: per chain sums
+    // dA_log = dA * A (A = -exp(A_log)); dD and the bias gradient per chain
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
         const int n = g * NPL + i;
         if (chain_ok && n < N) atomicAdd(a.dA_log + d * N + n, dA[i] * A[i]);
     }
-    __syncthreads();
-    if (g == 0 && chain_ok) {
-        if (a.dD) atomicAdd(a.dD + d, sDacc[c]);
-        if (a.ddelta_bias) atomicAdd(a.ddelta_bias + d, sBacc[c]);
+    constexpr int R = T / EPT;  // threads that share a chain's elements
+#pragma unroll
+    for (int off = R / 2; off > 0; off /= 2) {
+        accD += __shfl_xor_sync(0xffffffffu, accD, off);
+        accB += __shfl_xor_sync(0xffffffffu, accB, off);
+    }
+    if (e_live && tid % R == 0) {
+        if (a.dD) atomicAdd(a.dD + de, accD);
+        if (a.ddelta_bias) atomicAdd(a.ddelta_bias + de, accB);
     }
 }
 
 template <typename io_t, int NPL, int G>
-cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
+cudaError_t launch_bwd(const BwdArgs& a, bool vec_red, cudaStream_t stream) {
     using C = BwdCfg<io_t, NPL, G>;
     const int64_t dblocks = (a.f.dim + C::CH - 1) / C::CH;
     const int64_t blocks = dblocks * a.f.batch;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    const size_t smem = C::kSmem + 2 * C::CH * sizeof(float);
     cudaError_t err = cudaFuncSetAttribute(scan_bwd_kernel<io_t, NPL, G>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           int(C::kSmem));
     if (err != cudaSuccess) return err;
-    scan_bwd_kernel<io_t, NPL, G><<<unsigned(blocks), C::NTH, smem, stream>>>(a, int(dblocks));
+    scan_bwd_kernel<io_t, NPL, G>
+        <<<unsigned(blocks), C::NTH, C::kSmem, stream>>>(a, int(dblocks), vec_red);
     return cudaGetLastError();
 }
 
 template <typename io_t>
-cudaError_t dispatch_bwd(const BwdArgs& a, cudaStream_t stream) {
+cudaError_t dispatch_bwd(const BwdArgs& a, bool vec_red, cudaStream_t stream) {
     const int N = a.f.dstate;
-    if (N <= 8) return launch_bwd<io_t, 4, 2>(a, stream);
-    if (N <= 16) return launch_bwd<io_t, 8, 2>(a, stream);
-    if (N <= 32) return launch_bwd<io_t, 8, 4>(a, stream);
-    if (N <= 64) return launch_bwd<io_t, 8, 8>(a, stream);
-    if (N <= 128) return launch_bwd<io_t, 8, 16>(a, stream);
-    return launch_bwd<io_t, 8, 32>(a, stream);
+    if (N <= 8) return launch_bwd<io_t, 4, 2>(a, vec_red, stream);
+    if (N <= 16) return launch_bwd<io_t, 8, 2>(a, vec_red, stream);
+    if (N <= 32) return launch_bwd<io_t, 8, 4>(a, vec_red, stream);
+    if (N <= 64) return launch_bwd<io_t, 8, 8>(a, vec_red, stream);
+    if (N <= 128) return launch_bwd<io_t, 8, 16>(a, vec_red, stream);
+    return launch_bwd<io_t, 8, 32>(a, vec_red, stream);
 }
 
 }  // namespace
@@ -407,7 +505,11 @@ cudaError_t launch_scan_bwd(const ScanBwdArgs& s, bool bf16, cudaStream_t stream
     BwdArgs a;
     static_cast<ScanBwdArgs&>(a) = s;
     a.ckpt = static_cast<float*>(ck);
-    err = bf16 ? dispatch_bwd<__nv_bfloat16>(a, stream) : dispatch_bwd<float>(a, stream);
+    // 16-byte atomics on dB / dC need rows of whole float4 and aligned bases
+    const bool vec_red = s.f.dstate % 4 == 0 && (reinterpret_cast<uintptr_t>(s.dB) & 15) == 0 &&
+                         (reinterpret_cast<uintptr_t>(s.dC) & 15) == 0;
+    err = bf16 ? dispatch_bwd<__nv_bfloat16>(a, vec_red, stream)
+               : dispatch_bwd<float>(a, vec_red, stream);
     const cudaError_t ferr = cudaFreeAsync(ck, stream);
     return err != cudaSuccess ? err : ferr;
 }
