@@ -53,6 +53,23 @@ def scan_counts(cfg) -> dict:
     }
 
 
+def bwd_counts(cfg) -> dict:
+    """Algorithmic counts of one backward launch (mamba_selective_scan_bwd)."""
+    s = 2 if cfg.io_dtype == "bf16" else 4
+    B, D, L, N = cfg.batch, cfg.dim, cfg.seqlen, cfg.dstate
+    elems = B * D * L
+    return {
+        "updates": elems * N,
+        # u, delta, z, dout read and du, ddelta, dz written; B, C read; dB, dC
+        # (fp32) written; A_log, D, bias read and their gradients written.
+        "bytes": elems * 7 * s + 2 * B * L * N * s + 2 * B * L * N * 4 + 8 * D * N + 16 * D,
+        # three exponentials per update (the forward pass to the checkpoints,
+        # the recomputation of each chunk and the adjoint's Abar), plus per
+        # element softplus, its derivative and the gate's sigmoid
+        "exps": elems * (3 * N + 3),
+    }
+
+
 def decode_counts(cfg) -> dict:
     s = 2 if cfg.io_dtype == "bf16" else 4
     B, D, N = cfg.batch, cfg.dim, cfg.dstate
@@ -466,6 +483,8 @@ def run_ours(args, cfg, dcfg, rank, world, local):
 
     if not args.no_ex:
         result["ex"] = bench_ex(args, cnt, xd, y, h, sfu, stream)
+    if not args.no_bwd:
+        result["bwd"] = bench_bwd(args, cfg, xd, sfu, peaks, stream)
     if not args.no_decode:
         result["decode"] = bench_decode(args, dcfg, device, peaks)
     if not args.no_e2e:
@@ -518,6 +537,53 @@ def bench_ex(args, cnt, xd, y, h, sfu, stream) -> dict:
             "roofline": {"bound": "alu", "achieved": round(cnt["exps"] / t / 1e9, 1),
                          "peak": round(sfu["ex2_per_s"] / 1e9, 1), "unit": "Gexp/s",
                          "frac": round(cnt["exps"] / t / sfu["ex2_per_s"], 4), "traffic": None},
+            "steps": steps, "gpu_launches": steps}
+
+
+def bench_bwd(args, cfg, xd, sfu, peaks, stream) -> dict:
+    """The backward (gradients of every input for a given output gradient) on
+    the same workload, timed on the launching stream like the main step.  Its
+    inputs and outputs (about 7 bytes per element in bf16) exceed L2 at the
+    bench sizes."""
+    import torch
+
+    from selective_state_space_140_b300 import abi
+
+    cnt = bwd_counts(cfg)
+    gen = torch.Generator(device=xd["u"].device).manual_seed(17)
+    dout = torch.randn(xd["u"].shape, generator=gen, device=xd["u"].device).to(xd["u"].dtype)
+    grads = None
+
+    def step():
+        nonlocal grads
+        grads = abi.mamba_selective_scan_bwd(xd["u"], xd["delta"], xd["A_log"], xd["B"], xd["C"],
+                                             dout, D=xd["D"], z=xd["z"],
+                                             delta_bias=xd["delta_bias"], softplus=xd["softplus"],
+                                             grads=grads, stream=stream)
+
+    for _ in range(max(3, min(args.warmup, 5))):
+        step()
+    steps = max(5, min(args.steps // 20, 50))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    e1.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / steps
+    gbs = cnt["bytes"] / t / 1e9
+    hbm_peak = float(peaks["hbm_gbs"])
+    return {"what": "backward with recomputation, same workload, bf16 gradients of u/delta/z, "
+                    "fp32 gradients of A_log/B/C/D/bias",
+            "us_per_step": round(t * 1e6, 1), "state_updates_per_s": cnt["updates"] / t,
+            "roofline": {"bound": "alu", "achieved": round(cnt["exps"] / t / 1e9, 1),
+                         "peak": round(sfu["ex2_per_s"] / 1e9, 1), "unit": "Gexp/s",
+                         "frac": round(cnt["exps"] / t / sfu["ex2_per_s"], 4), "traffic": None,
+                         "exps_per_launch": cnt["exps"]},
+            "roofline_hbm": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
+                             "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
+                             "bytes_per_launch": cnt["bytes"]},
             "steps": steps, "gpu_launches": steps}
 
 
@@ -656,6 +722,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-ex", action="store_true")
+    ap.add_argument("--no-bwd", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     args.steps = max(1, args.steps)

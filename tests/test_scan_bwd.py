@@ -193,3 +193,14 @@ def test_full_size_layer_on_sampled_chains(cuda):
         part.update({"dA_log": gg["dA_log"][d:d + 1], "dD": gg["dD"][d:d + 1],
                      "ddelta_bias": gg["ddelta_bias"][d:d + 1]})
         _assert_grads(x, part, {k: gr[k] for k in part}, what=f"channel {d}")
+
+
+@pytest.mark.parametrize("tile", ["0", "1"])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_selectable_dstate16_tiles(cuda, monkeypatch, tile, io):
+    """Every tile the dstate <= 16 dispatch can take (MAMBA_BWD_TILE) matches
+    the oracle on a ragged shape with a partial CTA."""
+    monkeypatch.setenv("MAMBA_BWD_TILE", tile)
+    x = workloads.make_scan_inputs(2, 37, 201, 16, io, seed=16, d_mode="normal")
+    dout = _dout(x, 16)
+    _assert_grads(x, _gpu_bwd(x, dout, cuda), _oracle_bwd(x, dout), what=f"tile {tile}")
