@@ -54,6 +54,9 @@ def _declare(lib):
     lib.oracle_selective_scan_bwd_f64.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int,
                                                   dp, dp, dp, dp, dp, dp, dp, dp, dp,
                                                   i64, i64, i64, i64]
+    lib.oracle_causal_conv1d_f64.restype = ctypes.c_int
+    lib.oracle_causal_conv1d_f64.argtypes = [dp, dp, dp, dp, ctypes.c_int, dp, dp,
+                                             i64, i64, i64, i64]
     lib.oracle_hw_threads.restype = ctypes.c_int
     lib.oracle_hw_threads.argtypes = []
     return lib
@@ -156,6 +159,29 @@ def selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_bias=N
     if delta_bias is None:
         del g["ddelta_bias"]
     return g
+
+
+def causal_conv1d(x, weight, bias=None, initial_state=None, silu=True, lib=None):
+    """Causal depthwise conv1d (one filter per channel), then SiLU if ``silu``.
+
+    x [batch, dim, L]; weight [dim, width]; bias [dim]; initial_state
+    [batch, dim, width-1] (the inputs before step 0, oldest first; zeros if
+    None).  Returns ``(out [batch, dim, L], final_state [batch, dim, width-1])``
+    where final_state holds the last width-1 inputs."""
+    lib = lib or load()
+    x, weight, bias, initial_state = map(_f64, (x, weight, bias, initial_state))
+    batch, dim, L = x.shape
+    width = weight.shape[1]
+    assert weight.shape == (dim, width) and width >= 1
+    assert bias is None or bias.shape == (dim,)
+    assert initial_state is None or initial_state.shape == (batch, dim, width - 1)
+    out = np.empty((batch, dim, L), dtype=np.float64)
+    fin = np.empty((batch, dim, width - 1), dtype=np.float64)
+    rc = lib.oracle_causal_conv1d_f64(_ptr(x), _ptr(weight), _ptr(bias), _ptr(initial_state),
+                                      int(bool(silu)), _ptr(out), _ptr(fin), batch, dim, L, width)
+    if rc != 0:
+        raise ValueError(f"oracle_causal_conv1d_f64 rejected its arguments ({rc})")
+    return out, fin
 
 
 def selective_state_update(state, x, dt, A_log, B, C, D=None, z=None, dt_bias=None,

@@ -19,6 +19,10 @@
  *     with use_bias=True).
  *   - SiLU output gate on the z branch (highthink.cn "Mamba 整体架构" block
  *     diagram: the SiLU branch multiplies the SSM output).
+ *   - The causal depthwise convolution (+ SiLU) in front of the scan
+ *     (luzhipeng.com tutorial, step 2 nn.Conv1d with groups = d_model;
+ *     highthink.cn "Mamba 整体架构": causal Conv1D then SiLU), at the end of
+ *     this file.
  *   - Document boundaries: Mamba isolates documents by resetting its hidden
  *     state (codechina.net overview, section 3.2, point 2 "边界控制"), and a
  *     given starting state lets a long sequence be processed block by block
@@ -306,6 +310,61 @@ int oracle_selective_state_update_f64(double *state, const double *x, const doub
             }
             const double yt = acc + (D ? D[d] : 0.0) * x[e];
             out[e] = z ? yt * oracle_silu(z[e]) : yt;
+        }
+    }
+    return 0;
+}
+
+/*
+ * Causal depthwise convolution, optionally followed by SiLU: the short
+ * convolution the Mamba block applies to its x branch before the scan
+ * (luzhipeng.com tutorial, step 2: nn.Conv1d with kernel_size = d_conv,
+ * padding = d_conv - 1, groups = d_model -- one filter per channel;
+ * highthink.cn "Mamba 整体架构": Conv1D (causal) followed by SiLU).
+ *
+ * Readings: "causal" keeps the first seqlen outputs of the padded
+ * convolution, so output t sees inputs t-width+1 .. t.  The convolution is a
+ * cross-correlation as in PyTorch: weight[d][width-1] multiplies the current
+ * input.  Inputs before the sequence come from init_state (the last width-1
+ * inputs of a previous block, oldest first) or are zero when it is NULL;
+ * final_state (optional) receives the last width-1 inputs, for the next block.
+ *
+ *   xin(s)  = x[b][d][s] for s >= 0;  init_state[b][d][width-1+s] (or 0) for s < 0
+ *   pre     = bias[d] + sum_{k=0}^{width-1} weight[d][k] * xin(t - (width-1) + k)
+ *   out[b][d][t] = silu_flag ? SiLU(pre) : pre
+ *   final_state[b][d][j] = xin(seqlen - (width-1) + j),  j = 0 .. width-2
+ *
+ * Layouts: x, out [batch][dim][seqlen]; weight [dim][width]; bias [dim]
+ * (optional); init_state, final_state [batch][dim][width-1].
+ */
+static double conv_input(const double *xr, const double *st, int64_t width, int64_t s) {
+    if (s >= 0) return xr[s];
+    return st ? st[width - 1 + s] : 0.0;
+}
+
+int oracle_causal_conv1d_f64(const double *x, const double *weight, const double *bias,
+                             const double *init_state, int silu_flag, double *out,
+                             double *final_state, int64_t batch, int64_t dim, int64_t seqlen,
+                             int64_t width) {
+    if ((!x && batch * dim * seqlen > 0) || !weight || (!out && batch * dim * seqlen > 0))
+        return -1;
+    if (batch < 0 || dim < 0 || seqlen < 0 || width < 1) return -2;
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t d = 0; d < dim; ++d) {
+            const int64_t row = b * dim + d;
+            const double *xr = x ? x + row * seqlen : NULL;
+            const double *st = init_state ? init_state + row * (width - 1) : NULL;
+            const double *w = weight + d * width;
+            for (int64_t t = 0; t < seqlen; ++t) {
+                double pre = bias ? bias[d] : 0.0;
+                for (int64_t k = 0; k < width; ++k)
+                    pre += w[k] * conv_input(xr, st, width, t - (width - 1) + k);
+                out[row * seqlen + t] = silu_flag ? oracle_silu(pre) : pre;
+            }
+            if (final_state)
+                for (int64_t j = 0; j < width - 1; ++j)
+                    final_state[row * (width - 1) + j] =
+                        conv_input(xr, st, width, seqlen - (width - 1) + j);
         }
     }
     return 0;

@@ -14,7 +14,10 @@ steps).
 Steps pinned (see the page sections cited in ``oracle/scan_oracle.c``):
   A = -exp(A_log), Abar = exp(dt*A), Bbar = dt*B, h_t = Abar h_{t-1} + Bbar u,
   y = sum_n C h + D u, SiLU(z) gate, dt = softplus(delta + bias), zero h0,
-  a given h0, and the state restarting at document boundaries (reset mask).
+  a given h0, the state restarting at document boundaries (reset mask), the
+  gradients (finite differences), and the causal depthwise conv1d + SiLU in
+  front of the scan (numpy.convolve, impulse response, SiLU values, state
+  chaining).
 """
 from __future__ import annotations
 
@@ -416,6 +419,106 @@ def check_backward_finite_differences_plain(lib):
     _fd_check(lib, softplus=False, with_opt=False, seed=14)
 
 
+# --------------------------------------------------------------------------
+# causal depthwise conv1d (+ SiLU) in front of the scan
+def check_conv_against_numpy_convolve(lib):
+    """Without the activation, each channel is numpy's full convolution of the
+    zero-padded input with the channel's filter (PyTorch's Conv1d is a
+    cross-correlation, so the filter is reversed for np.convolve), keeping the
+    first L outputs; widths 1 to 6, with and without a bias."""
+    r = _rng(40)
+    for width in (1, 2, 3, 4, 6):
+        b, d, L = 2, 3, 17
+        x, w = r.normal(size=(b, d, L)), r.normal(size=(d, width))
+        bias = r.normal(size=d) if width % 2 == 0 else None
+        out, _ = oracle.causal_conv1d(x, w, bias=bias, silu=False, lib=lib)
+        want = np.empty_like(x)
+        for bi in range(b):
+            for di in range(d):
+                full = np.convolve(x[bi, di], w[di][::-1], mode="full")[:L]
+                want[bi, di] = full + (bias[di] if bias is not None else 0.0)
+        _close(out, want, rtol=1e-13, what=f"conv width {width}")
+
+
+def check_conv_impulse_response(lib):
+    """A unit impulse at step t0 (no bias, no activation) comes out as the
+    filter read backwards: out[t0 + j] = w[width-1-j] for j < width, zero
+    elsewhere -- the current input meets the last tap, and nothing leaks
+    before t0 (causality)."""
+    L, t0, width = 12, 5, 4
+    w = np.array([[0.5, -1.25, 2.0, 3.5]])
+    x = np.zeros((1, 1, L))
+    x[0, 0, t0] = 1.0
+    out, _ = oracle.causal_conv1d(x, w, silu=False, lib=lib)
+    want = np.zeros(L)
+    for j in range(width):
+        want[t0 + j] = w[0, width - 1 - j]
+    assert np.array_equal(out[0, 0], want), (out[0, 0], want)
+
+
+def check_conv_silu_closed_forms(lib):
+    """A pass-through filter (last tap 1, bias 0) leaves SiLU(x) = x/(1+e^-x):
+    SiLU(0) = 0, SiLU(1) = 1/(1+e^-1) = 0.7310585786300049, SiLU(-1) =
+    -0.2689414213699951, SiLU(40) = 40 to double precision; the bias enters
+    before the activation (SiLU(0 + 1) for a zero input)."""
+    x = np.array([[[0.0, 1.0, -1.0, 40.0]]])
+    w = np.array([[0.0, 0.0, 0.0, 1.0]])
+    out, _ = oracle.causal_conv1d(x, w, silu=True, lib=lib)
+    _close(out[0, 0], [0.0, 0.7310585786300049, -0.2689414213699951, 40.0], rtol=1e-15,
+           what="SiLU values")
+    out, _ = oracle.causal_conv1d(np.zeros((1, 1, 3)), w, bias=np.array([1.0]), silu=True, lib=lib)
+    _close(out[0, 0], [0.7310585786300049] * 3, rtol=1e-15, what="bias before SiLU")
+
+
+def check_conv_state_chaining(lib):
+    """Cutting a sequence into blocks and passing each block's final state as
+    the next block's initial state gives the unsplit result, outputs and final
+    state; the final state is the last width-1 inputs (also when a block is
+    shorter than width-1)."""
+    r = _rng(41)
+    b, d, L, width = 2, 4, 23, 4
+    x, w, bias = r.normal(size=(b, d, L)), r.normal(size=(d, width)), r.normal(size=d)
+    st0 = r.normal(size=(b, d, width - 1))
+    ref, fin = oracle.causal_conv1d(x, w, bias=bias, initial_state=st0, lib=lib)
+    _close(fin, x[:, :, L - (width - 1):], rtol=0.0, what="final state = last inputs")
+    outs, st = [], st0
+    for lo, hi in ((0, 2), (2, 3), (3, 11), (11, 23)):
+        o, st = oracle.causal_conv1d(x[:, :, lo:hi], w, bias=bias, initial_state=st, lib=lib)
+        outs.append(o)
+    _close(np.concatenate(outs, axis=2), ref, rtol=0.0, what="chained blocks")
+    _close(st, fin, rtol=0.0, what="chained final state")
+
+
+def check_conv_initial_state_reaches_first_outputs_only(lib):
+    """The initial state is the input before step 0: with zero x it alone
+    drives out[t] for t < width-1 (out[t] = sum_k w[k] st[t+k] over the taps
+    that reach back before the sequence), and outputs from step width-1 on
+    equal the bias."""
+    width = 4
+    w = np.array([[1.0, 10.0, 100.0, 1000.0]])
+    st = np.array([[[2.0, 3.0, 5.0]]])
+    out, _ = oracle.causal_conv1d(np.zeros((1, 1, 6)), w, bias=np.array([0.25]),
+                                  initial_state=st, silu=False, lib=lib)
+    want = [1 * 2 + 10 * 3 + 100 * 5, 1 * 3 + 10 * 5, 1 * 5, 0.0, 0.0, 0.0]
+    _close(out[0, 0], np.array(want) + 0.25, rtol=1e-15, what="initial state")
+
+
+def check_conv_channels_and_batches_are_independent(lib):
+    """Each (batch, channel) row uses only its own input and its channel's
+    filter: permuting channels (with their filters and biases) or batch rows
+    permutes the output the same way."""
+    r = _rng(42)
+    b, d, L, width = 3, 5, 9, 4
+    x, w, bias = r.normal(size=(b, d, L)), r.normal(size=(d, width)), r.normal(size=d)
+    st = r.normal(size=(b, d, width - 1))
+    ref, fin = oracle.causal_conv1d(x, w, bias=bias, initial_state=st, lib=lib)
+    pd, pb = r.permutation(d), r.permutation(b)
+    out, f2 = oracle.causal_conv1d(x[pb][:, pd], w[pd], bias=bias[pd],
+                                   initial_state=st[pb][:, pd], lib=lib)
+    _close(out, ref[pb][:, pd], rtol=0.0, what="permuted rows")
+    _close(f2, fin[pb][:, pd], rtol=0.0, what="permuted final state")
+
+
 ALL_CHECKS = [
     check_delta_zero_limit,
     check_single_step,
@@ -434,4 +537,10 @@ ALL_CHECKS = [
     check_reset_at_start_ignores_h0,
     check_backward_finite_differences,
     check_backward_finite_differences_plain,
+    check_conv_against_numpy_convolve,
+    check_conv_impulse_response,
+    check_conv_silu_closed_forms,
+    check_conv_state_chaining,
+    check_conv_initial_state_reaches_first_outputs_only,
+    check_conv_channels_and_batches_are_independent,
 ]

@@ -56,6 +56,18 @@ MUTANTS = [
     ("bwd_ddt_without_input_term", "ddt += gn * (A[n] * a * hp + uc[t] * Bb[t * N + n]);",
      "ddt += gn * (A[n] * a * hp);"),
     ("bwd_du_without_skip", "double dut = dy * Dd, ddt = 0.0;", "double dut = 0.0, ddt = 0.0;"),
+    ("conv_window_one_step_late", "pre += w[k] * conv_input(xr, st, width, t - (width - 1) + k);",
+     "pre += w[k] * conv_input(xr, st, width, t - width + k);"),
+    ("conv_taps_reversed", "pre += w[k] * conv_input(xr, st, width, t - (width - 1) + k);",
+     "pre += w[width - 1 - k] * conv_input(xr, st, width, t - (width - 1) + k);"),
+    ("conv_bias_dropped", "double pre = bias ? bias[d] : 0.0;", "double pre = 0.0;"),
+    ("conv_sigmoid_instead_of_silu", "out[row * seqlen + t] = silu_flag ? oracle_silu(pre) : pre;",
+     "out[row * seqlen + t] = silu_flag ? 1.0 / (1.0 + exp(-pre)) : pre;"),
+    ("conv_state_newest_first", "return st ? st[width - 1 + s] : 0.0;", "return st ? st[-1 - s] : 0.0;"),
+    ("conv_state_ignored", "return st ? st[width - 1 + s] : 0.0;", "return 0.0;"),
+    ("conv_final_state_shifted", "conv_input(xr, st, width, seqlen - (width - 1) + j);",
+     "conv_input(xr, st, width, seqlen - width + j);"),
+    ("conv_filter_ignores_channel", "const double *w = weight + d * width;", "const double *w = weight;"),
 ]
 
 
