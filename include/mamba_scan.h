@@ -1,6 +1,7 @@
 /*
  * mamba_scan.h -- C ABI of libmamba_scan.so, a B300 (sm_103a) implementation
- * of the Mamba selective scan and its single-token decode step.
+ * of the Mamba selective scan (forward, backward, single-token decode) and of
+ * the causal depthwise conv1d + SiLU that feeds it.
  *
  * Operation (definitions restated from the pages this library follows):
  *   - Discrete state-space recurrence h_t = Abar_t h_{t-1} + Bbar_t u_t,
@@ -27,8 +28,9 @@
  * Conventions shared by every entry point
  *   - All pointers are DEVICE pointers owned by the caller.  Arrays are dense
  *     row-major with the shapes given below.  The library keeps no state
- *     between calls.  Only mamba_selective_scan_fwd may allocate: see there
- *     and mamba_selective_scan_fwd_noalloc.
+ *     between calls.  Only mamba_selective_scan_fwd (see there and
+ *     mamba_selective_scan_fwd_noalloc) and mamba_selective_scan_bwd take
+ *     scratch memory, stream-ordered on the call's stream.
  *   - io_dtype (MAMBA_F32 or MAMBA_BF16) is the element type of every
  *     "io" array (u, delta, z, B, C, y; x, dt, z, B, C, out for decode).
  *     A_log, D, the bias and the state are always fp32.  Arithmetic is fp32;
@@ -74,6 +76,8 @@ typedef enum {
 } mamba_status_t;
 
 #define MAMBA_MAX_DSTATE 256
+/* Largest conv1d width (taps per channel) of mamba_causal_conv1d_*. */
+#define MAMBA_MAX_CONV_WIDTH 8
 
 /*
  * Selective scan, forward.
@@ -224,6 +228,51 @@ int mamba_selective_state_update(float *state, const void *x, const void *dt,
                                  const float *D, const void *z, const float *dt_bias,
                                  int softplus_flag, void *out, int64_t batch, int64_t dim,
                                  int64_t dstate, int io_dtype, mamba_stream_t stream);
+
+/*
+ * Causal depthwise conv1d, optionally followed by SiLU: the short per-channel
+ * convolution the Mamba block applies to its x branch before the scan
+ * (luzhipeng.com tutorial, step 2: Conv1d with kernel_size = d_conv,
+ * padding = d_conv - 1, groups = d_model; highthink.cn "Mamba 整体架构":
+ * causal Conv1D, then SiLU).  "Causal" keeps the first seqlen outputs of the
+ * padded convolution: for every row (b, d) and step t
+ *
+ *   out[b,d,t] = act(bias[d] + sum_{k<width} weight[d,k] * xin(t - (width-1) + k))
+ *   xin(s) = x[b,d,s] for s >= 0, initial_state[b,d,width-1+s] (or 0) for s < 0
+ *
+ * with act = SiLU if silu_flag, else identity (a cross-correlation, as in
+ * PyTorch: weight[d,width-1] multiplies the current input).
+ *
+ *   x, out        : [batch, dim, seqlen] io_dtype (out must not overlap x)
+ *   weight        : [dim, width] fp32;  bias : [dim] fp32 or NULL
+ *   initial_state : [batch, dim, width-1] io_dtype or NULL (zeros): the last
+ *                   width-1 inputs of the previous block, oldest first
+ *   final_state   : [batch, dim, width-1] io_dtype or NULL (not written): the
+ *                   last width-1 inputs of xin, for the next block; must not
+ *                   overlap initial_state (MAMBA_ERR_ALIAS) -- use two buffers
+ *   width         : 1 .. MAMBA_MAX_CONV_WIDTH (Mamba uses 4), else MAMBA_ERR_SIZE
+ *
+ * Fast path: seqlen a multiple of 8 (bf16) or 4 (fp32), x and out 16-byte
+ * aligned and width-1 at most that vector length; other inputs take a scalar
+ * path with the same arithmetic.  Errors as for mamba_selective_scan_fwd.
+ */
+int mamba_causal_conv1d_fwd(const void *x, const float *weight, const float *bias,
+                            const void *initial_state, int silu_flag, void *out,
+                            void *final_state, int64_t batch, int64_t dim, int64_t seqlen,
+                            int64_t width, int io_dtype, mamba_stream_t stream);
+
+/*
+ * Decode step of the conv1d: one new token per row.  out[b,d] is
+ * mamba_causal_conv1d_fwd of x[b,d] with seqlen 1 and initial state
+ * conv_state[b,d,:]; conv_state is then shifted IN PLACE to hold the last
+ * width-1 inputs (the oldest drops out, x[b,d] enters at the end).
+ *
+ *   conv_state : [batch, dim, width-1] io_dtype (may be NULL when width == 1)
+ *   x, out     : [batch, dim] io_dtype;  weight [dim, width], bias [dim] as above
+ */
+int mamba_causal_conv1d_update(void *conv_state, const void *x, const float *weight,
+                               const float *bias, int silu_flag, void *out, int64_t batch,
+                               int64_t dim, int64_t width, int io_dtype, mamba_stream_t stream);
 
 /*
  * Wait for the work queued on `stream`, then report and clear the device-side

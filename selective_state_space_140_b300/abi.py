@@ -25,6 +25,7 @@ MAX_DSTATE = 256
 # Every symbol include/mamba_scan.h declares.
 EXPORTED = ("mamba_selective_scan_fwd", "mamba_selective_scan_fwd_noalloc",
             "mamba_selective_scan_fwd_ex", "mamba_selective_scan_bwd",
+            "mamba_causal_conv1d_fwd", "mamba_causal_conv1d_update",
             "mamba_selective_state_update", "mamba_device_status", "mamba_status_string",
             "mamba_abi_version")
 
@@ -52,6 +53,10 @@ def _declare(lib):
     lib.mamba_selective_scan_bwd.restype = ci
     lib.mamba_selective_scan_bwd.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, vp, vp, vp, vp,
                                              fp, fp, fp, fp, fp, i64, i64, i64, i64, ci, vp]
+    lib.mamba_causal_conv1d_fwd.restype = ci
+    lib.mamba_causal_conv1d_fwd.argtypes = [vp, fp, fp, vp, ci, vp, vp, i64, i64, i64, i64, ci, vp]
+    lib.mamba_causal_conv1d_update.restype = ci
+    lib.mamba_causal_conv1d_update.argtypes = [vp, vp, fp, fp, ci, vp, i64, i64, i64, ci, vp]
     lib.mamba_selective_state_update.restype = ci
     lib.mamba_selective_state_update.argtypes = [fp, vp, vp, fp, vp, vp, fp, vp, fp, ci, vp,
                                                  i64, i64, i64, ci, vp]
@@ -252,6 +257,55 @@ def mamba_selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_
     return {k: g[k] for k in shapes}
 
 
+def mamba_causal_conv1d_fwd(x, weight, bias=None, initial_state=None, silu=True, out=None,
+                            final_state=None, want_final_state=False, stream=None):
+    """Causal depthwise conv1d (+ SiLU) of ``x`` [batch, dim, L] with
+    ``weight`` [dim, width] (float32) and ``bias`` [dim]; ``initial_state`` /
+    ``final_state`` [batch, dim, width-1] hold the last width-1 inputs before /
+    after the block (io dtype).  Returns ``(out, final_state)``."""
+    dev = x.device
+    batch, dim, L = x.shape
+    width = weight.shape[-1]
+    io = _io_dtype(x)
+    for t, n in ((x, "x"), (initial_state, "initial_state"), (out, "out"),
+                 (final_state, "final_state")):
+        _check(t, n, dev, x.dtype)
+    for t, n in ((weight, "weight"), (bias, "bias")):
+        _check(t, n, dev, torch.float32)
+    if out is None:
+        out = torch.empty_like(x)
+    if final_state is None and want_final_state:
+        final_state = torch.empty((batch, dim, width - 1), device=dev, dtype=x.dtype)
+    rc = load().mamba_causal_conv1d_fwd(_ptr(x), _ptr(weight), _ptr(bias), _ptr(initial_state),
+                                        int(bool(silu)), _ptr(out), _ptr(final_state), batch, dim,
+                                        L, width, io, _stream(stream, dev))
+    if rc != 0:
+        raise MambaError(rc, "mamba_causal_conv1d_fwd")
+    return out, final_state
+
+
+def mamba_causal_conv1d_update(conv_state, x, weight, bias=None, silu=True, out=None,
+                               stream=None):
+    """One decode token per row: ``x`` [batch, dim]; ``conv_state`` [batch, dim,
+    width-1] (io dtype) is shifted in place.  Returns ``out`` [batch, dim]."""
+    dev = x.device
+    batch, dim = x.shape
+    width = weight.shape[-1]
+    io = _io_dtype(x)
+    for t, n in ((x, "x"), (conv_state, "conv_state"), (out, "out")):
+        _check(t, n, dev, x.dtype)
+    for t, n in ((weight, "weight"), (bias, "bias")):
+        _check(t, n, dev, torch.float32)
+    if out is None:
+        out = torch.empty_like(x)
+    rc = load().mamba_causal_conv1d_update(_ptr(conv_state), _ptr(x), _ptr(weight), _ptr(bias),
+                                           int(bool(silu)), _ptr(out), batch, dim, width, io,
+                                           _stream(stream, dev))
+    if rc != 0:
+        raise MambaError(rc, "mamba_causal_conv1d_update")
+    return out
+
+
 def mamba_selective_state_update(state, x, dt, A_log, B, C, D=None, z=None, dt_bias=None,
                                  softplus=True, out=None, stream=None):
     """One decode step; ``state`` [batch, dim, dstate] fp32 is updated in place.
@@ -323,3 +377,17 @@ def raw_scan_bwd(u, delta, A_log, B, C, D, z, delta_bias, softplus_flag, dout, d
                                            softplus_flag, dout, du, ddelta, dz, dA_log, dB, dC,
                                            dD, ddelta_bias, batch, dim, seqlen, dstate, io_dtype,
                                            stream)
+
+
+def raw_conv1d_fwd(x, weight, bias, initial_state, silu_flag, out, final_state, batch, dim,
+                   seqlen, width, io_dtype, stream) -> int:
+    """``mamba_causal_conv1d_fwd`` with plain integers as pointers."""
+    return load().mamba_causal_conv1d_fwd(x, weight, bias, initial_state, silu_flag, out,
+                                          final_state, batch, dim, seqlen, width, io_dtype, stream)
+
+
+def raw_conv1d_update(conv_state, x, weight, bias, silu_flag, out, batch, dim, width, io_dtype,
+                      stream) -> int:
+    """``mamba_causal_conv1d_update`` with plain integers as pointers."""
+    return load().mamba_causal_conv1d_update(conv_state, x, weight, bias, silu_flag, out, batch,
+                                             dim, width, io_dtype, stream)

@@ -302,4 +302,59 @@ int mamba_selective_state_update(float* state, const void* x, const void* dt,
     return err == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
 }
 
+int mamba_causal_conv1d_fwd(const void* x, const float* weight, const float* bias,
+                            const void* initial_state, int silu_flag, void* out,
+                            void* final_state, int64_t batch, int64_t dim, int64_t seqlen,
+                            int64_t width, int io_dtype, mamba_stream_t stream) {
+    if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
+    if (width < 1 || width > MAMBA_MAX_CONV_WIDTH) return MAMBA_ERR_SIZE;
+    if (!size_ok(batch, dim, seqlen) || !size_ok(batch, dim, width)) return MAMBA_ERR_SIZE;
+    const int64_t elems = batch * dim * seqlen, nst = batch * dim * (width - 1);
+    if ((elems > 0 && (!x || !out)) || (dim > 0 && !weight)) return MAMBA_ERR_NULL;
+    const size_t es = io_size(io_dtype);
+    if (misaligned(x, es) || misaligned(out, es) || misaligned(initial_state, es) ||
+        misaligned(final_state, es) || misaligned(weight, 4) || misaligned(bias, 4))
+        return MAMBA_ERR_ALIGN;
+    const Range ro = range_of(out, elems, es);
+    const Range rf = final_state ? range_of(final_state, nst, es) : Range{0, 0};
+    const Range ins[] = {range_of(x, elems, es), range_of(weight, dim * width, 4),
+                         bias ? range_of(bias, dim, 4) : Range{0, 0},
+                         initial_state ? range_of(initial_state, nst, es) : Range{0, 0}};
+    for (const Range& r : ins)
+        if (overlaps(ro, r) || overlaps(rf, r)) return MAMBA_ERR_ALIAS;
+    if (overlaps(ro, rf)) return MAMBA_ERR_ALIAS;
+    if (batch == 0 || dim == 0) return MAMBA_OK;
+    const cudaError_t err = mamba::launch_causal_conv1d(
+        x, weight, bias, initial_state, out, final_state, batch, dim, seqlen, int(width),
+        silu_flag != 0, io_dtype == MAMBA_BF16, reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
+}
+
+int mamba_causal_conv1d_update(void* conv_state, const void* x, const float* weight,
+                               const float* bias, int silu_flag, void* out, int64_t batch,
+                               int64_t dim, int64_t width, int io_dtype, mamba_stream_t stream) {
+    if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
+    if (width < 1 || width > MAMBA_MAX_CONV_WIDTH) return MAMBA_ERR_SIZE;
+    if (!size_ok(batch, dim, width)) return MAMBA_ERR_SIZE;
+    const int64_t rows = batch * dim, nst = rows * (width - 1);
+    if ((rows > 0 && (!x || !out || (width > 1 && !conv_state))) || (dim > 0 && !weight))
+        return MAMBA_ERR_NULL;
+    const size_t es = io_size(io_dtype);
+    if (misaligned(conv_state, es) || misaligned(x, es) || misaligned(out, es) ||
+        misaligned(weight, 4) || misaligned(bias, 4))
+        return MAMBA_ERR_ALIGN;
+    const Range ro = range_of(out, rows, es);
+    const Range rs = width > 1 ? range_of(conv_state, nst, es) : Range{0, 0};
+    const Range ins[] = {range_of(x, rows, es), range_of(weight, dim * width, 4),
+                         bias ? range_of(bias, dim, 4) : Range{0, 0}};
+    for (const Range& r : ins)
+        if (overlaps(ro, r) || overlaps(rs, r)) return MAMBA_ERR_ALIAS;
+    if (overlaps(ro, rs)) return MAMBA_ERR_ALIAS;
+    if (rows == 0) return MAMBA_OK;
+    const cudaError_t err = mamba::launch_conv1d_update(
+        conv_state, x, weight, bias, out, batch, dim, int(width), silu_flag != 0,
+        io_dtype == MAMBA_BF16, reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
+}
+
 }  // extern "C"

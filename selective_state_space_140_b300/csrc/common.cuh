@@ -264,6 +264,16 @@ cudaError_t launch_state_update(const StateUpdateArgs& a, bool bf16, cudaStream_
 // Zeroes the summed gradients, takes stream-ordered checkpoint scratch, runs
 // the backward kernel and returns the scratch, all on `stream`.
 cudaError_t launch_scan_bwd(const ScanBwdArgs& a, bool bf16, cudaStream_t stream);
+
+// Causal depthwise conv1d (+ SiLU) over [batch][dim][L] rows; states [batch][dim][width-1].
+cudaError_t launch_causal_conv1d(const void* x, const float* w, const float* bias,
+                                 const void* st_in, void* out, void* st_out, int64_t batch,
+                                 int64_t dim, int64_t L, int width, bool silu, bool bf16,
+                                 cudaStream_t stream);
+// One token per row; the conv state shifts in place.
+cudaError_t launch_conv1d_update(void* state, const void* x, const float* w, const float* bias,
+                                 void* out, int64_t batch, int64_t dim, int width, bool silu,
+                                 bool bf16, cudaStream_t stream);
 // Test hook: a wait that never completes, given up after `limit` polls.
 cudaError_t launch_bounded_wait_probe(uint32_t limit, cudaStream_t stream);
 

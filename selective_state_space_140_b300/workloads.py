@@ -22,6 +22,7 @@ values the GPU reads.
 from __future__ import annotations
 
 import dataclasses
+import math
 
 import numpy as np
 import torch
@@ -136,6 +137,24 @@ def make_decode_inputs(batch: int, dim: int, dstate: int, io_dtype: str = "bf16"
         "A_log": A_log, "D": D if with_D else None, "dt_bias": bias if with_bias else None,
         "softplus": True, "io_dtype": io_dtype,
     }
+
+
+def make_conv_inputs(batch: int, dim: int, seqlen: int, width: int = 4, io_dtype: str = "bf16",
+                     seed: int = 20, with_bias: bool = True, with_state: bool = False) -> dict:
+    """Draw inputs of the causal depthwise conv1d as CPU tensors: x [batch,
+    dim, seqlen] ~ N(0, 1) in the io dtype; weight [dim, width] and bias [dim]
+    fp32 ~ U(-1/sqrt(width), 1/sqrt(width)) (the default initialisation of a
+    depthwise Conv1d, fan-in = width); initial_state [batch, dim, width-1]
+    ~ N(0, 1) in the io dtype when ``with_state``."""
+    gen = torch.Generator().manual_seed(int(seed))
+    tdt = TORCH_DTYPES[io_dtype]
+    bound = 1.0 / math.sqrt(width)
+    x = torch.randn((batch, dim, seqlen), generator=gen, dtype=torch.float32).to(tdt)
+    w = (torch.rand((dim, width), generator=gen, dtype=torch.float32) * 2 - 1) * bound
+    bias = (torch.rand(dim, generator=gen, dtype=torch.float32) * 2 - 1) * bound
+    st = torch.randn((batch, dim, width - 1), generator=gen, dtype=torch.float32).to(tdt)
+    return {"x": x, "weight": w.contiguous(), "bias": bias if with_bias else None,
+            "initial_state": st if with_state else None, "io_dtype": io_dtype}
 
 
 def to_f64(t):

@@ -208,3 +208,31 @@ def test_bwd_entry_validation(lib):
     assert bwd(dim=0, dD=None, ddelta_bias=None) == 0
     assert bwd(dim=0, z=None, dz=None) == 0
     assert bwd(dim=0, z=None, dz=Q[9]) == 0                      # dz ignored without z
+
+
+CGOOD = dict(x=Q[0], weight=Q[1], bias=Q[2], initial_state=Q[3], silu_flag=1, out=Q[4],
+             final_state=Q[5], batch=2, dim=8, seqlen=16, width=4, io_dtype=abi.MAMBA_BF16,
+             stream=None)
+
+
+def test_conv1d_entry_validation(lib):
+    """mamba_causal_conv1d_fwd / _update: every bad call returns before any CUDA call."""
+    conv = lambda **o: abi.raw_conv1d_fwd(**{**CGOOD, **o})
+    for name in ("x", "weight", "out"):
+        assert conv(**{name: None}) == 1, name                       # MAMBA_ERR_NULL
+    assert conv(width=0) == 2 and conv(width=9) == 2                 # MAMBA_ERR_SIZE
+    assert conv(batch=-1) == 2 and conv(seqlen=1 << 50) == 2
+    assert conv(io_dtype=3) == 5                                     # MAMBA_ERR_DTYPE
+    assert conv(x=Q[0] + 1) == 4 and conv(weight=Q[1] + 2) == 4      # MAMBA_ERR_ALIGN
+    assert conv(out=Q[0]) == 8                                       # out over x
+    assert conv(final_state=Q[3]) == 8                               # final over initial state
+    assert conv(final_state=Q[4] + 8) == 8                           # final state inside out
+    assert conv(dim=0) == 0 and conv(batch=0) == 0                   # nothing to do
+    upd_ = lambda **o: abi.raw_conv1d_update(**{**dict(conv_state=Q[6], x=Q[0], weight=Q[1],
+                                                       bias=Q[2], silu_flag=1, out=Q[4], batch=2,
+                                                       dim=8, width=4, io_dtype=abi.MAMBA_BF16,
+                                                       stream=None), **o})
+    assert upd_(conv_state=None) == 1 and upd_(x=None) == 1
+    assert upd_(width=9) == 2 and upd_(io_dtype=7) == 5
+    assert upd_(out=Q[6]) == 8 and upd_(conv_state=Q[0]) == 8
+    assert upd_(batch=0) == 0
