@@ -57,6 +57,9 @@ def _declare(lib):
     lib.oracle_causal_conv1d_f64.restype = ctypes.c_int
     lib.oracle_causal_conv1d_f64.argtypes = [dp, dp, dp, dp, ctypes.c_int, dp, dp,
                                              i64, i64, i64, i64]
+    lib.oracle_selective_scan_complex_f64.restype = ctypes.c_int
+    lib.oracle_selective_scan_complex_f64.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp,
+                                                      ctypes.c_int, dp, dp, i64, i64, i64, i64]
     lib.oracle_hw_threads.restype = ctypes.c_int
     lib.oracle_hw_threads.argtypes = []
     return lib
@@ -159,6 +162,36 @@ def selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_bias=N
     if delta_bias is None:
         del g["ddelta_bias"]
     return g
+
+
+def selective_scan_complex(u, delta, A_log_re, A_im, B, C, D=None, z=None, delta_bias=None,
+                           softplus=True, lib=None):
+    """Complex-state scan: A = -exp(A_log_re) + i*A_im [dim, N]; B, C complex
+    [batch, L, N] (numpy complex arrays, or real arrays [batch, L, N, 2] of
+    (re, im) pairs).  Returns ``(y [batch, dim, L] real, last_state [batch,
+    dim, N] complex)``."""
+    lib = lib or load()
+
+    def pairs(a):
+        a = np.asarray(a)
+        if np.iscomplexobj(a):
+            a = np.stack([a.real, a.imag], axis=-1)
+        return _f64(a)
+
+    u, delta, A_log_re, A_im = map(_f64, (u, delta, A_log_re, A_im))
+    B, C = pairs(B), pairs(C)
+    D, z, delta_bias = map(_f64, (D, z, delta_bias))
+    batch, dim, L = u.shape
+    N = A_log_re.shape[1]
+    assert A_im.shape == (dim, N) and B.shape == (batch, L, N, 2) and C.shape == B.shape
+    y = np.empty((batch, dim, L), dtype=np.float64)
+    hL = np.empty((batch, dim, N, 2), dtype=np.float64)
+    rc = lib.oracle_selective_scan_complex_f64(
+        _ptr(u), _ptr(delta), _ptr(A_log_re), _ptr(A_im), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+        _ptr(delta_bias), int(bool(softplus)), _ptr(y), _ptr(hL), batch, dim, L, N)
+    if rc != 0:
+        raise ValueError(f"oracle_selective_scan_complex_f64 rejected its arguments ({rc})")
+    return y, hL[..., 0] + 1j * hL[..., 1]
 
 
 def causal_conv1d(x, weight, bias=None, initial_state=None, silu=True, lib=None):

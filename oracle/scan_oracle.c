@@ -23,6 +23,9 @@
  *     (luzhipeng.com tutorial, step 2 nn.Conv1d with groups = d_model;
  *     highthink.cn "Mamba 整体架构": causal Conv1D then SiLU), at the end of
  *     this file.
+ *   - The complex-state variant: S4D-Lin initialisation A = -0.5 + i*n and a
+ *     complex state that keeps phase (codechina.net overview, section 4.1 and
+ *     section 5.3), at the end of this file.
  *   - Document boundaries: Mamba isolates documents by resetting its hidden
  *     state (codechina.net overview, section 3.2, point 2 "边界控制"), and a
  *     given starting state lets a long sequence be processed block by block
@@ -51,6 +54,7 @@
  * over POSIX threads.  That changes no arithmetic: every chain is evaluated in
  * exactly the order written below.
  */
+#include <complex.h>
 #include <math.h>
 #include <pthread.h>
 #include <stdint.h>
@@ -369,3 +373,70 @@ int oracle_causal_conv1d_f64(const double *x, const double *weight, const double
     }
     return 0;
 }
+
+/*
+ * Complex-state selective scan (codechina.net overview, section 4.1: the
+ * complex version initialises A = -0.5 + i*n (S4D-Lin); section 5.3: a
+ * complex state keeps phase information).  The pages give nothing else, so:
+ *
+ *   A[d][n]  = -exp(A_log_re[d][n]) + i * A_im[d][n]        (Re A < 0)
+ *   dt       = softplus(delta + bias) (or delta + bias), real
+ *   h[n]     = exp(dt * A[d][n]) * h[n] + dt * B[b][t][n] * u      (complex)
+ *   out      = (Re(sum_n C[b][t][n] * h[n]) + D[d] * u) * SiLU(z)
+ *
+ * B and C are complex, input-dependent, stored as interleaved (re, im)
+ * pairs: [batch][seqlen][dstate][2]; the state starts at zero and
+ * last_state is [batch][dim][dstate][2].  Everything else is laid out as for
+ * oracle_selective_scan_f64.  Chains run one after another (no threads).
+ */
+int oracle_selective_scan_complex_f64(const double *u, const double *delta,
+                                      const double *A_log_re, const double *A_im,
+                                      const double *B, const double *C, const double *D,
+                                      const double *z, const double *delta_bias,
+                                      int softplus_flag, double *y, double *last_state,
+                                      int64_t batch, int64_t dim, int64_t seqlen,
+                                      int64_t dstate) {
+    if (!u || !delta || !A_log_re || !A_im || !B || !C || !y) return -1;
+    if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1) return -2;
+    const int64_t L = seqlen, N = dstate;
+    double complex *h = malloc((size_t)N * sizeof(double complex));
+    double complex *A = malloc((size_t)N * sizeof(double complex));
+    if (!h || !A) {
+        free(h);
+        free(A);
+        return -3;
+    }
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t d = 0; d < dim; ++d) {
+            const int64_t chain = b * dim + d;
+            for (int64_t n = 0; n < N; ++n) {
+                A[n] = -exp(A_log_re[d * N + n]) + I * A_im[d * N + n];
+                h[n] = 0.0;
+            }
+            for (int64_t t = 0; t < L; ++t) {
+                const double ut = u[chain * L + t];
+                const double raw = delta[chain * L + t] + (delta_bias ? delta_bias[d] : 0.0);
+                const double dt = softplus_flag ? oracle_softplus(raw) : raw;
+                double complex acc = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    const int64_t k = ((b * L + t) * N + n) * 2;
+                    const double complex Bn = B[k] + I * B[k + 1];
+                    const double complex Cn = C[k] + I * C[k + 1];
+                    h[n] = cexp(dt * A[n]) * h[n] + dt * Bn * ut;
+                    acc += Cn * h[n];
+                }
+                const double yt = creal(acc) + (D ? D[d] : 0.0) * ut;
+                y[chain * L + t] = z ? yt * oracle_silu(z[chain * L + t]) : yt;
+            }
+            if (last_state)
+                for (int64_t n = 0; n < N; ++n) {
+                    last_state[(chain * N + n) * 2] = creal(h[n]);
+                    last_state[(chain * N + n) * 2 + 1] = cimag(h[n]);
+                }
+        }
+    }
+    free(h);
+    free(A);
+    return 0;
+}
+

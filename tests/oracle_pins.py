@@ -30,8 +30,9 @@ RTOL = 1e-12
 
 
 def _close(got, want, rtol=RTOL, atol=0.0, what=""):
-    got = np.asarray(got, dtype=np.float64)
-    want = np.asarray(want, dtype=np.float64)
+    cplx = np.iscomplexobj(got) or np.iscomplexobj(want)
+    got = np.asarray(got, dtype=np.complex128 if cplx else np.float64)
+    want = np.asarray(want, dtype=np.complex128 if cplx else np.float64)
     assert got.shape == want.shape, f"{what}: shape {got.shape} != {want.shape}"
     scale = max(float(np.max(np.abs(want))) if want.size else 0.0, 1e-300)
     err = float(np.max(np.abs(got - want))) if want.size else 0.0
@@ -519,6 +520,94 @@ def check_conv_channels_and_batches_are_independent(lib):
     _close(f2, fin[pb][:, pd], rtol=0.0, what="permuted final state")
 
 
+# --------------------------------------------------------------------------
+# complex-state (S4D-Lin) scan
+def _cplx(r, shape):
+    return r.normal(size=shape) + 1j * r.normal(size=shape)
+
+
+def check_complex_with_real_parameters_is_the_real_scan(lib):
+    """A_im = 0 and real B, C: every state stays real and the complex scan is
+    the real scan (same dt, D, gate), output and final state."""
+    r = _rng(50)
+    b, d, L, N = 2, 3, 21, 4
+    u, delta, z = r.normal(size=(b, d, L)), r.normal(size=(b, d, L)), r.normal(size=(b, d, L))
+    A_log = np.log(r.uniform(0.5, 4, size=(d, N)))
+    B, C = r.normal(size=(b, L, N)), r.normal(size=(b, L, N))
+    D, bias = r.normal(size=d), r.normal(size=d)
+    yc, hc = oracle.selective_scan_complex(u, delta, A_log, np.zeros((d, N)), B + 0j, C + 0j,
+                                           D=D, z=z, delta_bias=bias, lib=lib)
+    yr, hr, _ = oracle.selective_scan(u, delta, A_log, B, C, D=D, z=z, delta_bias=bias)
+    _close(yc, yr, rtol=1e-13, what="complex vs real output")
+    _close(hc.real, hr, rtol=1e-13, what="complex vs real state")
+    assert np.all(hc.imag == 0.0)
+
+
+def check_complex_impulse_response_closed_form(lib):
+    """S4D-Lin A = -0.5 + i*n (and one channel with Re A ~ 0: a pure
+    rotation), a unit impulse at t = 0, constant dt, B and C: h_t = dt B a^t
+    with a = exp(dt A), so y_t = Re(sum_n C_n dt B_n a_n^t) + D [t == 0], from
+    complex powers (no recurrence); for the rotation, |h_t| stays |dt B| and
+    the phase advances by dt * Im A per step."""
+    r = _rng(51)
+    b, d, L, N = 1, 2, 30, 5
+    dt = 0.3
+    A_log = np.stack([np.full(N, np.log(0.5)), np.full(N, -60.0)])  # Re A = -0.5 and ~ -1e-26
+    A_im = np.tile(np.arange(N, dtype=float), (d, 1))
+    B0, C0 = _cplx(r, N), _cplx(r, N)
+    B = np.broadcast_to(B0, (b, L, N)).copy()
+    C = np.broadcast_to(C0, (b, L, N)).copy()
+    u = np.zeros((b, d, L))
+    u[:, :, 0] = 1.0
+    D = np.array([0.7, -1.1])
+    y, hL = oracle.selective_scan_complex(u, np.full((b, d, L), dt), A_log, A_im, B, C, D=D,
+                                          softplus=False, lib=lib)
+    t = np.arange(L)
+    for di in range(d):
+        a = np.exp(dt * (-np.exp(A_log[di]) + 1j * A_im[di]))
+        ht = dt * B0[None, :] * a[None, :] ** t[:, None]           # [L, N]
+        want = (ht * C0[None, :]).sum(axis=1).real + D[di] * u[0, di]
+        _close(y[0, di], want, rtol=1e-12, what=f"impulse response, channel {di}")
+        _close(hL[0, di], ht[-1], rtol=1e-12, what=f"final state, channel {di}")
+    rot = hL[0, 1]
+    _close(np.abs(rot), np.abs(dt * B0), rtol=1e-12, what="rotation keeps the modulus")
+    _close(np.exp(1j * (np.angle(rot) - np.angle(dt * B0))),
+           np.exp(1j * dt * A_im[1] * (L - 1)), rtol=1e-11, what="rotation phase")
+
+
+def check_complex_geometric_series(lib):
+    """Constant u, dt and B: h_L = dt B u (1 - a^L) / (1 - a), a = exp(dt A)."""
+    r = _rng(52)
+    b, d, L, N = 1, 3, 40, 4
+    dt, uval = 0.2, 1.5
+    A_log = np.log(r.uniform(0.2, 2.0, size=(d, N)))
+    A_im = r.uniform(-6, 6, size=(d, N))
+    B0 = _cplx(r, N)
+    B = np.broadcast_to(B0, (b, L, N)).copy()
+    y, hL = oracle.selective_scan_complex(np.full((b, d, L), uval), np.full((b, d, L), dt),
+                                          A_log, A_im, B, _cplx(r, (b, L, N)), softplus=False,
+                                          lib=lib)
+    a = np.exp(dt * (-np.exp(A_log) + 1j * A_im))
+    want = dt * B0[None, :] * uval * (1 - a ** L) / (1 - a)
+    _close(hL[0], want, rtol=1e-12, what="geometric series")
+
+
+def check_complex_conjugation_symmetry(lib):
+    """Conjugating A, B and C conjugates every state and leaves the real
+    output unchanged."""
+    r = _rng(53)
+    b, d, L, N = 2, 2, 17, 3
+    args = dict(u=r.normal(size=(b, d, L)), delta=r.normal(size=(b, d, L)),
+                A_log_re=np.log(r.uniform(0.3, 3, size=(d, N))))
+    A_im, B, C = r.normal(size=(d, N)) * 3, _cplx(r, (b, L, N)), _cplx(r, (b, L, N))
+    z = r.normal(size=(b, d, L))
+    y1, h1 = oracle.selective_scan_complex(A_im=A_im, B=B, C=C, z=z, lib=lib, **args)
+    y2, h2 = oracle.selective_scan_complex(A_im=-A_im, B=B.conj(), C=C.conj(), z=z, lib=lib,
+                                           **args)
+    _close(y2, y1, rtol=1e-12, what="conjugated output")
+    _close(h2, h1.conj(), rtol=1e-12, what="conjugated state")
+
+
 ALL_CHECKS = [
     check_delta_zero_limit,
     check_single_step,
@@ -543,4 +632,8 @@ ALL_CHECKS = [
     check_conv_state_chaining,
     check_conv_initial_state_reaches_first_outputs_only,
     check_conv_channels_and_batches_are_independent,
+    check_complex_with_real_parameters_is_the_real_scan,
+    check_complex_impulse_response_closed_form,
+    check_complex_geometric_series,
+    check_complex_conjugation_symmetry,
 ]

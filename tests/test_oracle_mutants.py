@@ -68,6 +68,20 @@ MUTANTS = [
     ("conv_final_state_shifted", "conv_input(xr, st, width, seqlen - (width - 1) + j);",
      "conv_input(xr, st, width, seqlen - width + j);"),
     ("conv_filter_ignores_channel", "const double *w = weight + d * width;", "const double *w = weight;"),
+    ("complex_A_conjugated", "A[n] = -exp(A_log_re[d * N + n]) + I * A_im[d * N + n];",
+     "A[n] = -exp(A_log_re[d * N + n]) - I * A_im[d * N + n];"),
+    ("complex_A_im_ignored", "A[n] = -exp(A_log_re[d * N + n]) + I * A_im[d * N + n];",
+     "A[n] = -exp(A_log_re[d * N + n]);"),
+    ("complex_output_imag_part", "const double yt = creal(acc) + (D ? D[d] : 0.0) * ut;",
+     "const double yt = cimag(acc) + (D ? D[d] : 0.0) * ut;"),
+    ("complex_B_conjugated", "const double complex Bn = B[k] + I * B[k + 1];",
+     "const double complex Bn = B[k] - I * B[k + 1];"),
+    ("complex_C_pair_swapped", "const double complex Cn = C[k] + I * C[k + 1];",
+     "const double complex Cn = C[k + 1] + I * C[k];"),
+    ("complex_Bbar_without_dt", "h[n] = cexp(dt * A[n]) * h[n] + dt * Bn * ut;",
+     "h[n] = cexp(dt * A[n]) * h[n] + Bn * ut;"),
+    ("complex_state_written_conjugated", "last_state[(chain * N + n) * 2 + 1] = cimag(h[n]);",
+     "last_state[(chain * N + n) * 2 + 1] = -cimag(h[n]);"),
 ]
 
 
