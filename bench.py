@@ -368,7 +368,7 @@ def measure_ex2_rate(ub, device) -> dict:
     out = torch.empty(blocks * threads, device=device)
     s = torch.cuda.current_stream(device)
     best = None
-    for fn_name in ("mamba_ubench_ex2", "mamba_ubench_ffma2"):
+    for fn_name in ("mamba_ubench_ex2", "mamba_ubench_ffma2", "mamba_ubench_sincos"):
         fn = getattr(ub, fn_name)
         fn.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
         times = []
@@ -384,8 +384,10 @@ def measure_ex2_rate(ub, device) -> dict:
         rate = ops / min(times[1:])
         if fn_name == "mamba_ubench_ex2":
             best = {"ex2_per_s": rate}
-        else:
+        elif fn_name == "mamba_ubench_ffma2":
             best["ffma2_per_s"] = rate
+        else:
+            best["sincos_pairs_per_s"] = rate
     best["sms"] = sms
     return best
 
@@ -485,6 +487,10 @@ def run_ours(args, cfg, dcfg, rank, world, local):
         result["ex"] = bench_ex(args, cnt, xd, y, h, sfu, stream)
     if not args.no_bwd:
         result["bwd"] = bench_bwd(args, cfg, xd, sfu, peaks, stream)
+    if not args.no_complex:
+        result["complex"] = bench_complex(args, device, sfu, stream)
+    if not args.no_conv:
+        result["conv"] = bench_conv(args, cfg, device, peaks, stream)
     if not args.no_decode:
         result["decode"] = bench_decode(args, dcfg, device, peaks)
     if not args.no_e2e:
@@ -584,6 +590,93 @@ def bench_bwd(args, cfg, xd, sfu, peaks, stream) -> dict:
             "roofline_hbm": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
                              "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
                              "bytes_per_launch": cnt["bytes"]},
+            "steps": steps, "gpu_launches": steps}
+
+
+def bench_complex(args, device, sfu, stream) -> dict:
+    """The complex-state (S4D-Lin) scan on the Mamba-130M-style shape (batch 8,
+    d_inner 1536, L 2048, N 16, bf16): per update one SFU exponential and one
+    SFU sine/cosine pair (bf16 io), so its floor is the larger of the two
+    SFU times at their measured rates."""
+    import torch
+
+    from selective_state_space_140_b300 import abi, workloads
+
+    batch, dim, L, N = 8, 1536, 2048, 16
+    x = workloads.make_complex_inputs(batch, dim, L, N, "bf16", seed=37)
+    xd = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    y = torch.empty_like(xd["u"])
+    h = torch.empty((batch, dim, N, 2), device=device, dtype=torch.float32)
+    updates = batch * dim * L * N
+
+    def step():
+        abi.mamba_selective_scan_complex_fwd(xd["u"], xd["delta"], xd["A_log_re"], xd["A_im"],
+                                             xd["B"], xd["C"], D=xd["D"], z=xd["z"],
+                                             delta_bias=xd["delta_bias"], y=y, last_state=h,
+                                             stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    steps = max(10, min(args.steps // 4, 200))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    e1.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / steps
+    t_floor = updates / sfu["ex2_per_s"] + updates / sfu["sincos_pairs_per_s"]
+    return {"what": "complex-state scan, S4D-Lin A = -0.5 + i n, batch 8, d_inner 1536, "
+                    "L 2048, N 16, bf16 io, fp32 complex state",
+            "us_per_step": round(t * 1e6, 1), "state_updates_per_s": updates / t,
+            "roofline": {"bound": "alu", "achieved": round(updates / t / 1e9, 1),
+                         "peak": round(updates / t_floor / 1e9, 1), "unit": "Gupdates/s",
+                         "frac": round(t_floor / t, 4), "traffic": None,
+                         "peak_source": "SFU floor: one ex2 and one sin/cos pair per update at "
+                                        "the micro-benchmarked rates of this run"},
+            "steps": steps, "gpu_launches": steps}
+
+
+def bench_conv(args, cfg, device, peaks, stream) -> dict:
+    """The causal depthwise conv1d + SiLU (width 4) that produces the scan's u,
+    on the x branch of the same workload ([batch, dim, seqlen] io dtype): one
+    read of x and one write of out per element; inputs exceed L2."""
+    import torch
+
+    from selective_state_space_140_b300 import abi, workloads
+
+    width = 4
+    x = workloads.make_conv_inputs(cfg.batch, cfg.dim, cfg.seqlen, width, cfg.io_dtype, seed=20)
+    xd = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    out = torch.empty_like(xd["x"])
+    s = 2 if cfg.io_dtype == "bf16" else 4
+    elems = cfg.batch * cfg.dim * cfg.seqlen
+    nbytes = 2 * elems * s + cfg.dim * (width + 1) * 4
+
+    def step():
+        abi.mamba_causal_conv1d_fwd(xd["x"], xd["weight"], bias=xd["bias"], silu=True, out=out,
+                                    stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    steps = max(20, min(args.steps, 500))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    e1.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / steps
+    gbs = nbytes / t / 1e9
+    hbm = float(peaks["hbm_gbs"])
+    return {"what": f"causal depthwise conv1d (width {width}) + SiLU over x [{cfg.batch}, "
+                    f"{cfg.dim}, {cfg.seqlen}] {cfg.io_dtype}",
+            "us_per_step": round(t * 1e6, 2), "elements_per_s": elems / t, "gbs": round(gbs, 1),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(gbs / hbm, 4), "traffic": None,
+                         "bytes_per_launch": nbytes},
             "steps": steps, "gpu_launches": steps}
 
 
@@ -723,6 +816,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-ex", action="store_true")
     ap.add_argument("--no-bwd", action="store_true")
+    ap.add_argument("--no-conv", action="store_true")
+    ap.add_argument("--no-complex", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     args.steps = max(1, args.steps)

@@ -230,6 +230,37 @@ int mamba_selective_state_update(float *state, const void *x, const void *dt,
                                  int64_t dstate, int io_dtype, mamba_stream_t stream);
 
 /*
+ * Complex-state selective scan, forward (codechina.net overview, section 4.1:
+ * the complex version initialises A = -0.5 + i*n, S4D-Lin; section 5.3: a
+ * complex state keeps phase information).  For every b, d, t, n:
+ *
+ *   A[d,n]   = -exp(A_log_re[d,n]) + i * A_im[d,n]
+ *   dt       = as for mamba_selective_scan_fwd (softplus of delta + bias)
+ *   h[n]     = exp(dt * A[d,n]) * h[n] + dt * B[b,t,n] * u[b,d,t]   (complex)
+ *   y[b,d,t] = (Re(sum_n C[b,t,n] * h[n]) + D[d] * u[b,d,t]) * SiLU(z[b,d,t])
+ *
+ * The pages give only A and the complex state; B and C are read as complex
+ * and input-dependent, and the output as the real part (a caller that keeps
+ * one state of each conjugate pair scales C by 2).  The state starts at zero.
+ *
+ *   u, delta, z, y   : [batch, dim, seqlen] io_dtype
+ *   B, C             : [batch, seqlen, dstate, 2] io_dtype, (re, im) pairs
+ *   A_log_re, A_im   : [dim, dstate] fp32 (S4D-Lin: log 0.5 and n)
+ *   D, delta_bias    : [dim] fp32 or NULL
+ *   last_state       : [batch, dim, dstate, 2] fp32 (re, im) or NULL, aligned
+ *                      to 8 bytes
+ *
+ * Errors as for mamba_selective_scan_fwd.  Arithmetic is fp32: exp(dt*A) is
+ * 2^(dt*Re A*log2 e) times (cos, sin) of dt*Im A reduced to [-pi, pi].
+ */
+int mamba_selective_scan_complex_fwd(const void *u, const void *delta, const float *A_log_re,
+                                     const float *A_im, const void *B, const void *C,
+                                     const float *D, const void *z, const float *delta_bias,
+                                     int softplus_flag, void *y, float *last_state,
+                                     int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                     int io_dtype, mamba_stream_t stream);
+
+/*
  * Causal depthwise conv1d, optionally followed by SiLU: the short per-channel
  * convolution the Mamba block applies to its x branch before the scan
  * (luzhipeng.com tutorial, step 2: Conv1d with kernel_size = d_conv,

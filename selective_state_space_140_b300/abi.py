@@ -25,6 +25,7 @@ MAX_DSTATE = 256
 # Every symbol include/mamba_scan.h declares.
 EXPORTED = ("mamba_selective_scan_fwd", "mamba_selective_scan_fwd_noalloc",
             "mamba_selective_scan_fwd_ex", "mamba_selective_scan_bwd",
+            "mamba_selective_scan_complex_fwd",
             "mamba_causal_conv1d_fwd", "mamba_causal_conv1d_update",
             "mamba_selective_state_update", "mamba_device_status", "mamba_status_string",
             "mamba_abi_version")
@@ -53,6 +54,9 @@ def _declare(lib):
     lib.mamba_selective_scan_bwd.restype = ci
     lib.mamba_selective_scan_bwd.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, vp, vp, vp, vp,
                                              fp, fp, fp, fp, fp, i64, i64, i64, i64, ci, vp]
+    lib.mamba_selective_scan_complex_fwd.restype = ci
+    lib.mamba_selective_scan_complex_fwd.argtypes = [vp, vp, fp, fp, vp, vp, fp, vp, fp, ci, vp,
+                                                     fp, i64, i64, i64, i64, ci, vp]
     lib.mamba_causal_conv1d_fwd.restype = ci
     lib.mamba_causal_conv1d_fwd.argtypes = [vp, fp, fp, vp, ci, vp, vp, i64, i64, i64, i64, ci, vp]
     lib.mamba_causal_conv1d_update.restype = ci
@@ -257,6 +261,36 @@ def mamba_selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_
     return {k: g[k] for k in shapes}
 
 
+def mamba_selective_scan_complex_fwd(u, delta, A_log_re, A_im, B, C, D=None, z=None,
+                                     delta_bias=None, softplus=True, y=None, last_state=None,
+                                     want_last_state=True, stream=None):
+    """Complex-state scan.  B, C: [batch, seqlen, dstate, 2] (re, im) pairs in
+    the io dtype of ``u``; A_log_re, A_im [dim, dstate] float32.  Returns
+    ``(y, last_state)`` with last_state [batch, dim, dstate, 2] float32."""
+    dev = u.device
+    batch, dim, seqlen = u.shape
+    dstate = A_log_re.shape[-1]
+    io = _io_dtype(u)
+    for t, n in ((u, "u"), (delta, "delta"), (z, "z"), (B, "B"), (C, "C"), (y, "y")):
+        _check(t, n, dev, u.dtype)
+    for t, n in ((A_log_re, "A_log_re"), (A_im, "A_im"), (D, "D"), (delta_bias, "delta_bias"),
+                 (last_state, "last_state")):
+        _check(t, n, dev, torch.float32)
+    if B.shape != (batch, seqlen, dstate, 2) or C.shape != B.shape:
+        raise TypeError("B and C must be [batch, seqlen, dstate, 2]")
+    if y is None:
+        y = torch.empty_like(u)
+    if last_state is None and want_last_state:
+        last_state = torch.empty((batch, dim, dstate, 2), device=dev, dtype=torch.float32)
+    rc = load().mamba_selective_scan_complex_fwd(
+        _ptr(u), _ptr(delta), _ptr(A_log_re), _ptr(A_im), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+        _ptr(delta_bias), int(bool(softplus)), _ptr(y), _ptr(last_state), batch, dim, seqlen,
+        dstate, io, _stream(stream, dev))
+    if rc != 0:
+        raise MambaError(rc, "mamba_selective_scan_complex_fwd")
+    return y, last_state
+
+
 def mamba_causal_conv1d_fwd(x, weight, bias=None, initial_state=None, silu=True, out=None,
                             final_state=None, want_final_state=False, stream=None):
     """Causal depthwise conv1d (+ SiLU) of ``x`` [batch, dim, L] with
@@ -391,3 +425,11 @@ def raw_conv1d_update(conv_state, x, weight, bias, silu_flag, out, batch, dim, w
     """``mamba_causal_conv1d_update`` with plain integers as pointers."""
     return load().mamba_causal_conv1d_update(conv_state, x, weight, bias, silu_flag, out, batch,
                                              dim, width, io_dtype, stream)
+
+
+def raw_scan_complex_fwd(u, delta, A_log_re, A_im, B, C, D, z, delta_bias, softplus_flag, y,
+                         last_state, batch, dim, seqlen, dstate, io_dtype, stream) -> int:
+    """``mamba_selective_scan_complex_fwd`` with plain integers as pointers."""
+    return load().mamba_selective_scan_complex_fwd(u, delta, A_log_re, A_im, B, C, D, z,
+                                                   delta_bias, softplus_flag, y, last_state, batch,
+                                                   dim, seqlen, dstate, io_dtype, stream)

@@ -302,6 +302,46 @@ int mamba_selective_state_update(float* state, const void* x, const void* dt,
     return err == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
 }
 
+int mamba_selective_scan_complex_fwd(const void* u, const void* delta, const float* A_log_re,
+                                     const float* A_im, const void* B, const void* C,
+                                     const float* D, const void* z, const float* delta_bias,
+                                     int softplus_flag, void* y, float* last_state, int64_t batch,
+                                     int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
+                                     mamba_stream_t stream) {
+    if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
+    if (dstate < 1 || dstate > MAMBA_MAX_DSTATE) return MAMBA_ERR_DSTATE;
+    if (!size_ok(batch, dim, seqlen) || !size_ok(batch, seqlen, 2 * dstate) ||
+        !size_ok(batch, dim, 2 * dstate))
+        return MAMBA_ERR_SIZE;
+    const int64_t elems = batch * dim * seqlen, nbc = batch * seqlen * dstate * 2;
+    const int64_t nst = batch * dim * dstate * 2;
+    if ((elems > 0 && (!u || !delta || !y)) || (nbc > 0 && (!B || !C)) ||
+        (dim > 0 && (!A_log_re || !A_im)))
+        return MAMBA_ERR_NULL;
+    const size_t es = io_size(io_dtype);
+    if (misaligned(u, es) || misaligned(delta, es) || misaligned(z, es) || misaligned(B, es) ||
+        misaligned(C, es) || misaligned(y, es) || misaligned(A_log_re, 4) ||
+        misaligned(A_im, 4) || misaligned(D, 4) || misaligned(delta_bias, 4) ||
+        misaligned(last_state, 8))
+        return MAMBA_ERR_ALIGN;
+    const Range ry = range_of(y, elems, es);
+    const Range rh = last_state ? range_of(last_state, nst, 4) : Range{0, 0};
+    const Range ins[] = {range_of(u, elems, es), range_of(delta, elems, es),
+                         z ? range_of(z, elems, es) : Range{0, 0}, range_of(B, nbc, es),
+                         range_of(C, nbc, es), range_of(A_log_re, dim * dstate, 4),
+                         range_of(A_im, dim * dstate, 4), D ? range_of(D, dim, 4) : Range{0, 0},
+                         delta_bias ? range_of(delta_bias, dim, 4) : Range{0, 0}};
+    for (const Range& r : ins)
+        if (overlaps(ry, r) || overlaps(rh, r)) return MAMBA_ERR_ALIAS;
+    if (overlaps(ry, rh)) return MAMBA_ERR_ALIAS;
+    if (batch == 0 || dim == 0) return MAMBA_OK;
+    const cudaError_t err = mamba::launch_scan_complex(
+        u, delta, A_log_re, A_im, B, C, D, z, delta_bias, softplus_flag != 0, y, last_state,
+        batch, dim, seqlen, int(dstate), io_dtype == MAMBA_BF16,
+        reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
+}
+
 int mamba_causal_conv1d_fwd(const void* x, const float* weight, const float* bias,
                             const void* initial_state, int silu_flag, void* out,
                             void* final_state, int64_t batch, int64_t dim, int64_t seqlen,

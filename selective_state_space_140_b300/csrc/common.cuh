@@ -265,6 +265,13 @@ cudaError_t launch_state_update(const StateUpdateArgs& a, bool bf16, cudaStream_
 // the backward kernel and returns the scratch, all on `stream`.
 cudaError_t launch_scan_bwd(const ScanBwdArgs& a, bool bf16, cudaStream_t stream);
 
+// Complex-state scan: B, C [batch][L][N][2] (re, im); last_state [batch][dim][N][2].
+cudaError_t launch_scan_complex(const void* u, const void* delta, const float* A_log_re,
+                                const float* A_im, const void* B, const void* C, const float* D,
+                                const void* z, const float* delta_bias, bool softplus, void* y,
+                                float* last_state, int64_t batch, int64_t dim, int64_t seqlen,
+                                int dstate, bool bf16, cudaStream_t stream);
+
 // Causal depthwise conv1d (+ SiLU) over [batch][dim][L] rows; states [batch][dim][width-1].
 cudaError_t launch_causal_conv1d(const void* x, const float* w, const float* bias,
                                  const void* st_in, void* out, void* st_out, int64_t batch,

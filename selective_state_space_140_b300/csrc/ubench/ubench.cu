@@ -1,4 +1,4 @@
-// Throughput micro-benchmarks: SFU ex2, fp32 FMA and packed f32x2 FMA.
+// Throughput micro-benchmarks: SFU ex2, SFU sin/cos, fp32 FMA and packed f32x2 FMA.
 // Each thread keeps 8 independent chains so that latency is hidden and the
 // pipe's issue rate is what the launch time measures.
 #include <cuda_runtime.h>
@@ -66,6 +66,24 @@ __global__ void ffma2_kernel(float* out, int iters) {
     out[blockIdx.x * blockDim.x + threadIdx.x] = s;
 }
 
+// SFU sine and cosine: 8 chains of each per thread (16 operations per step).
+__global__ void sincos_kernel(float* out, int iters) {
+    float v[8], w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = w[i] = 0.001f * float(threadIdx.x + i);
+    for (int k = 0; k < iters; ++k) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            asm volatile("sin.approx.ftz.f32 %0, %0;" : "+f"(v[i]));  // stays in [-1, 1]
+            asm volatile("cos.approx.ftz.f32 %0, %0;" : "+f"(w[i]));
+        }
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += v[i] + w[i];
+    out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+
 template <typename K>
 int launch(K kern, float* out, int blocks, int threads, int iters, cudaStream_t s) {
     if (!out || blocks <= 0 || threads <= 0 || iters <= 0) return 2;
@@ -84,5 +102,8 @@ int mamba_ubench_ffma(float* out, int blocks, int threads, int iters, CUstream_s
 }
 int mamba_ubench_ffma2(float* out, int blocks, int threads, int iters, CUstream_st* s) {
     return launch(ffma2_kernel, out, blocks, threads, iters, s);
+}
+int mamba_ubench_sincos(float* out, int blocks, int threads, int iters, CUstream_st* s) {
+    return launch(sincos_kernel, out, blocks, threads, iters, s);
 }
 }

@@ -139,6 +139,32 @@ def make_decode_inputs(batch: int, dim: int, dstate: int, io_dtype: str = "bf16"
     }
 
 
+def make_complex_inputs(batch: int, dim: int, seqlen: int, dstate: int, io_dtype: str = "bf16",
+                        seed: int = 30, with_z: bool = True, with_D: bool = True,
+                        with_bias: bool = True) -> dict:
+    """Inputs of the complex-state scan as CPU tensors: u, delta, z [batch,
+    dim, seqlen] ~ N(0, 1); B, C [batch, seqlen, dstate, 2] (re, im) ~ N(0, 1/2)
+    each part (unit complex variance) in the io dtype; S4D-Lin A = -0.5 + i*n:
+    A_log_re = log 0.5 and A_im = n; D ~ N(0, 1); the step bias as for the
+    real scan (dt in [1e-3, 1e-1])."""
+    gen = torch.Generator().manual_seed(int(seed))
+    tdt = TORCH_DTYPES[io_dtype]
+    shape = (batch, dim, seqlen)
+    u = torch.randn(shape, generator=gen, dtype=torch.float32).to(tdt)
+    delta = torch.randn(shape, generator=gen, dtype=torch.float32).to(tdt)
+    z = torch.randn(shape, generator=gen, dtype=torch.float32).to(tdt)
+    s = math.sqrt(0.5)
+    B = (torch.randn((batch, seqlen, dstate, 2), generator=gen, dtype=torch.float32) * s).to(tdt)
+    C = (torch.randn((batch, seqlen, dstate, 2), generator=gen, dtype=torch.float32) * s).to(tdt)
+    bias = _dt_bias(gen, dim)
+    D = torch.randn(dim, generator=gen, dtype=torch.float32)
+    A_log_re = torch.full((dim, dstate), math.log(0.5), dtype=torch.float32)
+    A_im = torch.arange(dstate, dtype=torch.float32).repeat(dim, 1).contiguous()
+    return {"u": u, "delta": delta, "z": z if with_z else None, "B": B, "C": C,
+            "A_log_re": A_log_re, "A_im": A_im, "D": D if with_D else None,
+            "delta_bias": bias if with_bias else None, "softplus": True, "io_dtype": io_dtype}
+
+
 def make_conv_inputs(batch: int, dim: int, seqlen: int, width: int = 4, io_dtype: str = "bf16",
                      seed: int = 20, with_bias: bool = True, with_state: bool = False) -> dict:
     """Draw inputs of the causal depthwise conv1d as CPU tensors: x [batch,

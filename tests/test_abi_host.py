@@ -236,3 +236,17 @@ def test_conv1d_entry_validation(lib):
     assert upd_(width=9) == 2 and upd_(io_dtype=7) == 5
     assert upd_(out=Q[6]) == 8 and upd_(conv_state=Q[0]) == 8
     assert upd_(batch=0) == 0
+
+
+def test_complex_scan_entry_validation(lib):
+    kw = dict(u=Q[0], delta=Q[1], A_log_re=Q[2], A_im=Q[3], B=Q[4], C=Q[5], D=Q[6], z=Q[7],
+              delta_bias=Q[8], softplus_flag=1, y=Q[9], last_state=Q[10], batch=2, dim=8,
+              seqlen=16, dstate=16, io_dtype=abi.MAMBA_BF16, stream=None)
+    cx = lambda **o: abi.raw_scan_complex_fwd(**{**kw, **o})
+    for name in ("u", "delta", "A_log_re", "A_im", "B", "C", "y"):
+        assert cx(**{name: None}) == 1, name                         # MAMBA_ERR_NULL
+    assert cx(batch=-1) == 2 and cx(dstate=0) == 3 and cx(dstate=300) == 3
+    assert cx(io_dtype=2) == 5
+    assert cx(u=Q[0] + 1) == 4 and cx(last_state=Q[10] + 4) == 4    # state needs 8 bytes
+    assert cx(y=Q[0]) == 8 and cx(last_state=Q[4] + 64) == 8         # y over u, state in B
+    assert cx(dim=0) == 0 and cx(batch=0) == 0
