@@ -93,21 +93,29 @@ def launches_per_step(cfg, sms: int) -> int:
     return 3 if min(8 * sms // ctas, cfg.seqlen // 512) >= 2 else 1
 
 
-def kernel_source_hash() -> str:
-    """Hash of the scan kernel sources, to match stored ncu traffic figures."""
+# kernel sources behind each stored ncu summary (profiles/<prefix>_<workload>.md)
+PROFILED_SOURCES = {
+    "scan_fwd": ("scan_fwd.cu", "common.cuh"),
+    "scan_bwd": ("scan_bwd.cu", "common.cuh"),
+    "conv1d": ("conv1d.cu", "common.cuh"),
+    "scan_complex": ("scan_complex.cu", "common.cuh"),
+}
+
+
+def kernel_source_hash(prefix: str = "scan_fwd") -> str:
+    """Hash of the sources of one kernel family, to match stored ncu figures."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "selective_state_space_140_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as fh:
-                h.update(name.encode() + fh.read())
+    for name in PROFILED_SOURCES[prefix]:
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
-def stored_traffic(workload: str, kernel_hash: str):
+def stored_traffic(workload: str, kernel_hash: str, prefix: str = "scan_fwd"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", f"scan_fwd_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"{prefix}_{workload}.md")
     if not os.path.exists(path):
         return None
     fields = {}
@@ -585,7 +593,9 @@ def bench_bwd(args, cfg, xd, sfu, peaks, stream) -> dict:
             "us_per_step": round(t * 1e6, 1), "state_updates_per_s": cnt["updates"] / t,
             "roofline": {"bound": "alu", "achieved": round(cnt["exps"] / t / 1e9, 1),
                          "peak": round(sfu["ex2_per_s"] / 1e9, 1), "unit": "Gexp/s",
-                         "frac": round(cnt["exps"] / t / sfu["ex2_per_s"], 4), "traffic": None,
+                         "frac": round(cnt["exps"] / t / sfu["ex2_per_s"], 4),
+                         "traffic": stored_traffic(cfg.name, kernel_source_hash("scan_bwd"),
+                                                   "scan_bwd"),
                          "exps_per_launch": cnt["exps"]},
             "roofline_hbm": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
                              "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
@@ -632,7 +642,10 @@ def bench_complex(args, device, sfu, stream) -> dict:
             "us_per_step": round(t * 1e6, 1), "state_updates_per_s": updates / t,
             "roofline": {"bound": "alu", "achieved": round(updates / t / 1e9, 1),
                          "peak": round(updates / t_floor / 1e9, 1), "unit": "Gupdates/s",
-                         "frac": round(t_floor / t, 4), "traffic": None,
+                         "frac": round(t_floor / t, 4),
+                         "traffic": stored_traffic("mamba130m_bf16",
+                                                   kernel_source_hash("scan_complex"),
+                                                   "scan_complex"),
                          "peak_source": "SFU floor: one ex2 and one sin/cos pair per update at "
                                         "the micro-benchmarked rates of this run"},
             "steps": steps, "gpu_launches": steps}
@@ -675,7 +688,9 @@ def bench_conv(args, cfg, device, peaks, stream) -> dict:
                     f"{cfg.dim}, {cfg.seqlen}] {cfg.io_dtype}",
             "us_per_step": round(t * 1e6, 2), "elements_per_s": elems / t, "gbs": round(gbs, 1),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
-                         "frac": round(gbs / hbm, 4), "traffic": None,
+                         "frac": round(gbs / hbm, 4),
+                         "traffic": stored_traffic(cfg.name, kernel_source_hash("conv1d"),
+                                                   "conv1d"),
                          "bytes_per_launch": nbytes},
             "steps": steps, "gpu_launches": steps}
 

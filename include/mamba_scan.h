@@ -317,7 +317,8 @@ int mamba_device_status(mamba_stream_t stream);
 /* Human-readable name of a mamba_status_t; never NULL. */
 const char *mamba_status_string(int status);
 
-/* Version of this ABI (major * 10000 + minor * 100 + patch). */
+/* Version of this ABI (major * 10000 + minor * 100 + patch): 1.1.0 adds the
+ * backward, the complex-state scan and the causal conv1d entry points. */
 int mamba_abi_version(void);
 
 #ifdef __cplusplus

@@ -100,7 +100,7 @@ int check_scan_args(const void* u, const void* delta, const float* A_log, const 
 
 extern "C" {
 
-int mamba_abi_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+int mamba_abi_version(void) { return 1 * 10000 + 1 * 100 + 0; }
 
 const char* mamba_status_string(int status) {
     switch (status) {

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert abi.abi_version() == 10000
+    assert abi.abi_version() == 10100
     for code, name in abi.STATUS.items():
         assert abi.status_string(code).startswith(name)
     assert abi.status_string(12345) == "unknown mamba_status_t"
