@@ -77,65 +77,84 @@ __device__ __forceinline__ uint4 ldg16(const void* p) {
     return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
-// One thread per V-element vector of a row (rows padded to nothing: L % V == 0,
-// 16-byte aligned rows, K - 1 <= V).  Consecutive lanes hold consecutive
-// vectors, so lane l's previous inputs are lane l-1's vector.
-template <typename io_t, int K>
+// One thread per V-element vector of a row (L % V == 0, 16-byte aligned rows,
+// K - 1 <= V).  Each warp takes segments of 32 * U consecutive vectors of one
+// row (one division per segment, the channel's taps loaded once per segment)
+// and issues all U loads of a segment before using any.  Within a group of 32
+// lane l's previous inputs are lane l-1's vector; lane 0 takes lane 31's
+// vector of the previous group, and in the first group it reloads its
+// predecessor (an L1/L2 hit) unless the segment starts the row.
+template <typename io_t, int K, int U>
 __global__ void __launch_bounds__(256) conv_vec_kernel(const ConvArgs a) {
-    constexpr int V = Vec<io_t>::V, H = K - 1, HP = H > 0 ? H : 1;
+    constexpr int V = Vec<io_t>::V, H = K - 1, HP = H > 0 ? H : 1, SEG = 32 * U;
     const io_t* x = static_cast<const io_t*>(a.x);
     io_t* out = static_cast<io_t*>(a.out);
     const io_t* st_in = static_cast<const io_t*>(a.st_in);
     io_t* st_out = static_cast<io_t*>(a.st_out);
-    const int64_t nv_row = a.L / V, total = a.rows * nv_row;
+    const int64_t nv_row = a.L / V;
+    const int64_t nseg_row = (nv_row + SEG - 1) / SEG, nseg = a.rows * nseg_row;
     const int lane = threadIdx.x & 31;
-    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-    for (int64_t gv0 = int64_t(blockIdx.x) * blockDim.x + (threadIdx.x - lane); gv0 < total;
-         gv0 += stride) {
-        const int64_t gv = gv0 + lane;
-        const bool live = gv < total;
-        const int64_t row = live ? gv / nv_row : 0, vr = live ? gv % nv_row : 0;
-        const uint4 raw = live ? ldg16(x + gv * V) : make_uint4(0u, 0u, 0u, 0u);
-        // the previous vector: from lane - 1, or loaded by the warp's first lane
-        uint4 pr;
-        pr.x = __shfl_up_sync(0xffffffffu, raw.x, 1);
-        pr.y = __shfl_up_sync(0xffffffffu, raw.y, 1);
-        pr.z = __shfl_up_sync(0xffffffffu, raw.z, 1);
-        pr.w = __shfl_up_sync(0xffffffffu, raw.w, 1);
-        if (!live) continue;
-        if (lane == 0 && vr > 0) pr = ldg16(x + (gv - 1) * V);
-        float win[HP + V];
-        Vec<io_t>::unpack(raw, win + HP);
-        if constexpr (H > 0) {
-            if (vr > 0) {
-                float pv[V];
-                Vec<io_t>::unpack(pr, pv);
-#pragma unroll
-                for (int i = 0; i < H; ++i) win[HP - H + i] = pv[V - H + i];
-            } else {
-#pragma unroll
-                for (int i = 0; i < H; ++i)
-                    win[HP - H + i] = st_in ? Io<io_t>::load(st_in + row * H + i) : 0.f;
-            }
-        }
+    const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x / 32);
+    for (int64_t sg = int64_t(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; sg < nseg;
+         sg += nwarps) {
+        const int64_t row = sg / nseg_row, v0 = (sg - row * nseg_row) * SEG;
         const int64_t d = row % a.dim;
+        const io_t* xr = x + row * a.L;
+        io_t* orow = out + row * a.L;
         float w[K];
 #pragma unroll
         for (int k = 0; k < K; ++k) w[k] = __ldg(a.w + d * K + k);
         const float bias = a.bias ? __ldg(a.bias + d) : 0.f;
-        float o[V];
+        uint4 raw[U];
 #pragma unroll
-        for (int j = 0; j < V; ++j) {
-            float pre = bias;
-#pragma unroll
-            for (int k = 0; k < K; ++k) pre = fmaf(w[k], win[HP - H + j + k], pre);
-            o[j] = act(pre, a.silu);
+        for (int u = 0; u < U; ++u) {
+            const int64_t vr = v0 + u * 32 + lane;
+            raw[u] = vr < nv_row ? ldg16(xr + vr * V) : make_uint4(0u, 0u, 0u, 0u);
         }
-        *reinterpret_cast<uint4*>(out + gv * V) = Vec<io_t>::pack(o);
-        if constexpr (H > 0) {
-            if (st_out && vr == nv_row - 1) {
 #pragma unroll
-                for (int i = 0; i < H; ++i) Io<io_t>::store(st_out + row * H + i, win[HP + V - H + i]);
+        for (int u = 0; u < U; ++u) {
+            const int64_t vr = v0 + u * 32 + lane;
+            const int src = lane == 0 ? 31 : lane - 1;
+            // lane 0 reads lane 31, which supplies its vector of the previous group
+            // (no other lane reads lane 31); the other lanes read lane - 1's vector
+            const uint4 cur = raw[u], prv = raw[u > 0 ? u - 1 : 0];
+            const bool take_prv = lane == 31 && u > 0;
+            uint4 pr;
+            pr.x = __shfl_sync(0xffffffffu, take_prv ? prv.x : cur.x, src);
+            pr.y = __shfl_sync(0xffffffffu, take_prv ? prv.y : cur.y, src);
+            pr.z = __shfl_sync(0xffffffffu, take_prv ? prv.z : cur.z, src);
+            pr.w = __shfl_sync(0xffffffffu, take_prv ? prv.w : cur.w, src);
+            if (vr >= nv_row) continue;
+            if (lane == 0 && u == 0 && vr > 0) pr = ldg16(xr + (vr - 1) * V);
+            float win[HP + V];
+            Vec<io_t>::unpack(cur, win + HP);
+            if constexpr (H > 0) {
+                if (vr > 0) {
+                    float pv[V];
+                    Vec<io_t>::unpack(pr, pv);
+#pragma unroll
+                    for (int i = 0; i < H; ++i) win[HP - H + i] = pv[V - H + i];
+                } else {
+#pragma unroll
+                    for (int i = 0; i < H; ++i)
+                        win[HP - H + i] = st_in ? Io<io_t>::load(st_in + row * H + i) : 0.f;
+                }
+            }
+            float o[V];
+#pragma unroll
+            for (int j = 0; j < V; ++j) {
+                float pre = bias;
+#pragma unroll
+                for (int k = 0; k < K; ++k) pre = fmaf(w[k], win[HP - H + j + k], pre);
+                o[j] = act(pre, a.silu);
+            }
+            *reinterpret_cast<uint4*>(orow + vr * V) = Vec<io_t>::pack(o);
+            if constexpr (H > 0) {
+                if (st_out && vr == nv_row - 1) {
+#pragma unroll
+                    for (int i = 0; i < H; ++i)
+                        Io<io_t>::store(st_out + row * H + i, win[HP + V - H + i]);
+                }
             }
         }
     }
@@ -220,8 +239,9 @@ bool al16(const void* q) { return q == nullptr || (reinterpret_cast<uintptr_t>(q
 
 template <typename io_t, int K>
 cudaError_t launch_vec(const ConvArgs& a, cudaStream_t s) {
-    const int64_t vecs = a.rows * (a.L / Vec<io_t>::V);
-    conv_vec_kernel<io_t, K><<<grid_for(vecs, 256), 256, 0, s>>>(a);
+    constexpr int U = 4;  // vectors per thread per pass
+    const int64_t segs = a.rows * ((a.L / Vec<io_t>::V + 32 * U - 1) / (32 * U));
+    conv_vec_kernel<io_t, K, U><<<grid_for(segs, 8), 256, 0, s>>>(a);  // 8 warps per block
     return cudaGetLastError();
 }
 
