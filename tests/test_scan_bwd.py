@@ -204,4 +204,3 @@ def test_selectable_dstate16_tiles(cuda, monkeypatch, tile, io):
     x = workloads.make_scan_inputs(2, 37, 201, 16, io, seed=16, d_mode="normal")
     dout = _dout(x, 16)
     _assert_grads(x, _gpu_bwd(x, dout, cuda), _oracle_bwd(x, dout), what=f"tile {tile}")
-
