@@ -297,6 +297,19 @@ def barrier_max(value: float, world: int, device) -> float:
     return float(t.item())
 
 
+def shard_seed(base_seed: int, rank: int) -> int:
+    """Each rank scans its own independent batch of the workload (weak
+    scaling: the per-rank problem is the configured one, drawn with a
+    rank-specific seed); rank 0 keeps the configured seed."""
+    return int(base_seed) + 1000003 * int(rank)
+
+
+def job_rate(units_per_rank: float, world: int, t_max: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time."""
+    return world * units_per_rank / t_max
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -419,7 +432,8 @@ def run_ours(args, cfg, dcfg, rank, world, local):
     cnt = scan_counts(cfg)
     peaks = measured_peaks()
 
-    x = workloads.make_config_inputs(cfg)
+    x = workloads.make_scan_inputs(cfg.batch, cfg.dim, cfg.seqlen, cfg.dstate, cfg.io_dtype,
+                                   shard_seed(cfg.seed, rank), cfg.d_mode)
     xd = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     y = torch.empty_like(xd["u"])
     h = torch.empty((cfg.batch, cfg.dim, cfg.dstate), device=device, dtype=torch.float32)
@@ -450,7 +464,7 @@ def run_ours(args, cfg, dcfg, rank, world, local):
     t_total = barrier_max(t_total, world, device)
     t_step = t_total / args.steps
 
-    value = world * cnt["updates"] / t_step
+    value = job_rate(cnt["updates"], world, t_step)
     gbs = cnt["bytes"] / t_step / 1e9
     hbm_peak = float(peaks["hbm_gbs"])
     exp_rate = cnt["exps"] / t_step
