@@ -372,9 +372,21 @@ def cpu_oracle_rate(cfg, x, seconds: float):
     _, _, used = oracle.selective_scan(*a, nthreads=0, **kw)
     dt = time.perf_counter() - t0
     updates = chains * cfg.seqlen * cfg.dstate
+    # the same oracle on one core, over channels of batch 0, for about a third
+    # of the time budget
+    per_chain_1 = dt * max(used, 1) / chains
+    k1 = max(1, min(cfg.dim, int(seconds / 3 / max(per_chain_1, 1e-12))))
+    a1, kw1, chains1, what1 = _oracle_sample(cfg, x, 0, k1)
+    t0 = time.perf_counter()
+    oracle.selective_scan(*a1, nthreads=1, **kw1)
+    dt1 = time.perf_counter() - t0
+    updates1 = chains1 * cfg.seqlen * cfg.dstate
     return {"value": updates / dt, "unit": UNIT, "cores": used, "kind": "oracle",
             "sample": f"fp64 oracle over {what}, full L={cfg.seqlen}, N={cfg.dstate} "
-                      f"({updates:.3g} updates in {dt:.2f} s)"}
+                      f"({updates:.3g} updates in {dt:.2f} s)",
+            "one_core": {"value": updates1 / dt1, "unit": UNIT, "cores": 1,
+                         "sample": f"fp64 oracle over {what1}, full L={cfg.seqlen} "
+                                   f"({updates1:.3g} updates in {dt1:.2f} s)"}}
 
 
 # ----------------------------------------------------------------------------
