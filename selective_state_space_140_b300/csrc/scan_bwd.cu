@@ -70,7 +70,15 @@ struct BwdCfg {
 
 struct BwdArgs : ScanBwdArgs {
     float* ckpt;  // [batch * dim][nchunks][N] scratch: state at each chunk start
+    // time split (nseg > 1): segment s covers chunks [s * seg_chunks, (s+1) * seg_chunks)
+    int nseg = 1, seg_chunks = 0;
+    float* hseg = nullptr;  // [chains][nseg][N]: summary: zero-start end state; main: state entering
+    float* gseg = nullptr;  // [chains][nseg][N]: summary: zero-start adjoint leaving to the left;
+                            //                    main: Abar g entering from the right
+    float* sdt = nullptr;   // [chains][nseg]: sum of dt over the segment
 };
+
+constexpr int kBwdFull = 0, kBwdSummary = 1;
 
 // One chunk's raw inputs as fetched (converted to float only when staged, so
 // that no instruction waits on the loads before the chunk is used).
@@ -167,7 +175,11 @@ __device__ __forceinline__ void chain_product(const float* sm, const float4* S, 
     }
 }
 
-template <typename io_t, int NPL, int G, int UA>
+// MODE kBwdFull: gradients of the segment's elements (the whole sequence when
+// unsplit).  MODE kBwdSummary: the segment's zero-start end state, its sum of
+// dt and its zero-start adjoint leaving to the left (no gradients), for the
+// carry pass of a time-split backward.
+template <typename io_t, int NPL, int G, int UA, int MODE>
 __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const int dblocks,
                                                          const bool vec_red) {
     using C = BwdCfg<io_t, NPL, G>;
@@ -179,8 +191,11 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
     const ScanArgs& p = a.f;
     const int64_t L = p.seqlen, dim = p.dim;
     const int N = p.dstate;
-    const int b = blockIdx.x / dblocks;
-    const int64_t d0 = int64_t(blockIdx.x % dblocks) * CH;
+    // blockIdx.x = (b * dblocks + channel block) * nseg + time segment
+    const int seg = blockIdx.x % a.nseg;
+    const int cblk = blockIdx.x / a.nseg;
+    const int b = cblk / dblocks;
+    const int64_t d0 = int64_t(cblk % dblocks) * CH;
     // recurrence role: chain c, states g * NPL ..; element role: chain ce, steps te0 ..
     const int tid = threadIdx.x, c = tid / G, g = tid % G;
     const int e0 = tid * EPT, ce = e0 / T, te0 = e0 % T;
@@ -193,6 +208,11 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
     const int64_t chain = int64_t(b) * dim + (chain_ok ? d : 0);
     const int64_t nchunks = (L + T - 1) / T;
     float* ck = a.ckpt + chain * nchunks * N;
+    const int64_t kbeg = a.nseg > 1 ? int64_t(seg) * a.seg_chunks : 0;
+    const int64_t kend = a.nseg > 1 ? (kbeg + a.seg_chunks < nchunks ? kbeg + a.seg_chunks : nchunks)
+                                    : nchunks;
+    float* hsg = a.nseg > 1 ? a.hseg + (chain * a.nseg + seg) * N : nullptr;
+    float* gsg = a.nseg > 1 ? a.gseg + (chain * a.nseg + seg) * N : nullptr;
 
     float A[NPL], A2[NPL], h[NPL];
 #pragma unroll
@@ -200,8 +220,10 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
         const int n = g * NPL + i;
         A[i] = (chain_ok && n < N) ? -expf(__ldg(p.A_log + d * N + n)) : 0.f;
         A2[i] = A[i] * kLog2e;
-        h[i] = 0.f;
+        // a later segment of a split starts from the carried state
+        h[i] = (MODE == kBwdFull && hsg && chain_ok && n < N) ? hsg[n] : 0.f;
     }
+    float dtsum = 0.f;  // summary: sum of dt over the segment
 
     // dt (and softplus') of element j of this thread in chunk k; zero past the data
     auto step_of = [&](float raw_delta, int64_t k, int j, float& sp) {
@@ -219,8 +241,8 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
 
     Raw<io_t, NPL, G> r;
     // ---------------- forward phase: checkpoints ----------------
-    fetch<io_t, NPL, G, false>(a, r, b, d0, 0, tid, ck, chain_ok, g);
-    for (int64_t k = 0; k < nchunks; ++k) {
+    if (kbeg < kend) fetch<io_t, NPL, G, false>(a, r, b, d0, kbeg, tid, ck, chain_ok, g);
+    for (int64_t k = kbeg; k < kend; ++k) {
         __syncthreads();
 #pragma unroll
         for (int j = 0; j < EPT; ++j) {
@@ -234,31 +256,42 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
 #pragma unroll
         for (int j = 0; j < C::BPT; ++j)
             if (tid + j * NTH < T * NP) sm[C::oB + tid + j * NTH] = to_f(r.B[j]);
-        if (chain_ok) {
+        if (MODE == kBwdFull && chain_ok) {
 #pragma unroll
             for (int i = 0; i < NPL; ++i)
                 if (g * NPL + i < N) ck[k * N + g * NPL + i] = h[i];
         }
         __syncthreads();
-        if (k + 1 < nchunks)
+        if (k + 1 < kend)
             fetch<io_t, NPL, G, false>(a, r, b, d0, k + 1, tid, ck, chain_ok, g);
         else
             fetch<io_t, NPL, G, true>(a, r, b, d0, k, tid, ck, chain_ok, g);
 #pragma unroll
         for (int t = 0; t < T; ++t) {
             const float dt = sm[C::oDt + t * S + c], du = sm[C::oU + t * S + c];
+            if (MODE == kBwdSummary) dtsum += dt;
 #pragma unroll
             for (int i = 0; i < NPL; ++i)
                 h[i] = fmaf(ex2_approx(dt * A2[i]), h[i], du * sm[C::oB + t * NP + g * NPL + i]);
         }
     }
+    if (MODE == kBwdSummary && chain_ok) {
+#pragma unroll
+        for (int i = 0; i < NPL; ++i)
+            if (g * NPL + i < N) hsg[g * NPL + i] = h[i];
+        if (g == 0) a.sdt[chain * a.nseg + seg] = dtsum;
+    }
 
     // ---------------- reverse phase ----------------
     float gc[NPL], dA[NPL];  // Abar_{t+1} g_{t+1}; sum of g dt Abar h_{t-1}
 #pragma unroll
-    for (int i = 0; i < NPL; ++i) gc[i] = dA[i] = 0.f;
+    for (int i = 0; i < NPL; ++i) {
+        // a segment before the last starts from the carried adjoint
+        gc[i] = (MODE == kBwdFull && gsg && chain_ok && g * NPL + i < N) ? gsg[g * NPL + i] : 0.f;
+        dA[i] = 0.f;
+    }
     float accD = 0.f, accB = 0.f;  // this thread's elements: sums of dy u and ddelta
-    for (int64_t k = nchunks - 1; k >= 0; --k) {
+    for (int64_t k = kend - 1; k >= kbeg; --k) {
         const int64_t t0 = k * T;
         const int tlen = L - t0 < T ? int(L - t0) : T;
         float* dBg = a.dB + (int64_t(b) * L + t0) * N;
@@ -285,7 +318,33 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
 #pragma unroll
         for (int i = 0; i < NPL; ++i) hs[i] = r.hs[i];
         __syncthreads();
-        if (k > 0) fetch<io_t, NPL, G, true>(a, r, b, d0, k - 1, tid, ck, chain_ok, g);
+        if (k > kbeg) fetch<io_t, NPL, G, true>(a, r, b, d0, k - 1, tid, ck, chain_ok, g);
+        if constexpr (MODE == kBwdSummary) {
+            // dy for every element, then the adjoint alone (no states needed)
+#pragma unroll
+            for (int j = 0; j < EPT; ++j) {
+                if (e0 + j >= C::kE) continue;
+                const int s = (te0 + j) * S + ce;
+                float dy = e_go[j];
+                if (p.z) {
+                    const float z = e_z[j];
+                    dy = e_go[j] * (z * rcp_approx(1.f + ex2_approx(-z * kLog2e)));
+                }
+                sm[C::oDy + s] = dy;
+            }
+            __syncthreads();
+#pragma unroll UA
+            for (int t = T - 1; t >= 0; --t) {
+                const int s = t * S + c;
+                const float dy = sm[C::oDy + s], dt = sm[C::oDt + s];
+#pragma unroll
+                for (int i = 0; i < NPL; ++i) {
+                    const float gn = fmaf(dy, sm[C::oC + t * NP + g * NPL + i], gc[i]);
+                    gc[i] = ex2_approx(dt * A2[i]) * gn;
+                }
+            }
+            continue;
+        }
 
         // recompute the chunk's states into shared memory; C.h summed over the
         // chain's lanes by a butterfly per step
@@ -407,6 +466,14 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
         }
     }
 
+    if constexpr (MODE == kBwdSummary) {
+        if (chain_ok) {
+#pragma unroll
+            for (int i = 0; i < NPL; ++i)
+                if (g * NPL + i < N) gsg[g * NPL + i] = gc[i];
+        }
+        return;
+    }
     // dA_log = dA * A (A = -exp(A_log)); dD and the bias gradient per chain
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
@@ -425,19 +492,106 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
     }
 }
 
+// Carry pass of a time-split backward, one thread per (chain, state).  With
+// P(s) = exp(A * sum of dt over s), the product of the segment's decays:
+//   forward: the state entering s + 1 is P(s) times the state entering s plus
+//            the zero-start end state of s (hseg becomes the entering states);
+//   adjoint: Abar g entering s from the right is a(s + 1) + P(s + 1) times the
+//            value entering s + 1, a(s) the zero-start adjoint leaving s to the
+//            left, zero for the last segment (gseg becomes the entering values).
+__global__ void __launch_bounds__(256) bwd_carry_kernel(const float* A_log, float* hseg,
+                                                        float* gseg, const float* sdt,
+                                                        int64_t chains, int64_t dim, int N,
+                                                        int nseg) {
+    const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= chains * N) return;
+    const int64_t chain = i / N;
+    const int n = int(i % N);
+    const float A2 = -expf(__ldg(A_log + (chain % dim) * N + n)) * kLog2e;
+    float* hs = hseg + chain * nseg * N + n;
+    float* gs = gseg + chain * nseg * N + n;
+    const float* sd = sdt + chain * nseg;
+    float H = 0.f;
+    for (int s = 0; s < nseg; ++s) {
+        const float e = hs[int64_t(s) * N];
+        hs[int64_t(s) * N] = H;
+        H = fmaf(ex2_approx(A2 * sd[s]), H, e);
+    }
+    float Gv = 0.f;
+    for (int s = nseg - 1; s >= 0; --s) {
+        const float e = gs[int64_t(s) * N];
+        gs[int64_t(s) * N] = Gv;
+        Gv = fmaf(ex2_approx(A2 * sd[s]), Gv, e);
+    }
+}
+
 template <typename io_t, int NPL, int G, int UA = 2>
-cudaError_t launch_bwd(const BwdArgs& a, bool vec_red, cudaStream_t stream) {
+cudaError_t launch_bwd(const BwdArgs& a0, bool vec_red, cudaStream_t stream) {
     using C = BwdCfg<io_t, NPL, G>;
-    const int64_t dblocks = (a.f.dim + C::CH - 1) / C::CH;
-    const int64_t blocks = dblocks * a.f.batch;
-    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    cudaError_t err = cudaFuncSetAttribute(scan_bwd_kernel<io_t, NPL, G, UA>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           int(C::kSmem));
-    if (err != cudaSuccess) return err;
-    scan_bwd_kernel<io_t, NPL, G, UA>
-        <<<unsigned(blocks), C::NTH, C::kSmem, stream>>>(a, int(dblocks), vec_red);
-    return cudaGetLastError();
+    const int64_t dblocks = (a0.f.dim + C::CH - 1) / C::CH;
+    const int64_t ctas = dblocks * a0.f.batch;
+    const int64_t nchunks = (a0.f.seqlen + kBT - 1) / kBT;
+    // Few CTAs for the GPU (under two per SM) and a long sequence: split the
+    // sequence into segments (at least 32 chunks each) so that every SM holds
+    // about 7 CTAs.  MAMBA_BWD_SEGMENTS forces a segment count.
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int64_t nseg = 1;
+    const char* env = getenv("MAMBA_BWD_SEGMENTS");
+    if (env && atoi(env) > 0) {
+        nseg = atoi(env);
+    } else if (ctas < 2 * int64_t(sms) && nchunks >= 64) {
+        nseg = (7 * int64_t(sms) + ctas - 1) / ctas;
+        if (nseg > nchunks / 32) nseg = nchunks / 32;
+    }
+    if (nseg > nchunks) nseg = nchunks;
+    if (nseg < 1) nseg = 1;
+    const int64_t seg_chunks = (nchunks + nseg - 1) / nseg;
+    nseg = (nchunks + seg_chunks - 1) / seg_chunks;
+    if (ctas * nseg > 0x7fffffff) return cudaErrorInvalidConfiguration;
+
+    cudaError_t err = cudaSuccess;
+    BwdArgs a = a0;
+    a.nseg = int(nseg);
+    a.seg_chunks = int(seg_chunks);
+    void* seg_mem = nullptr;
+    if (nseg > 1) {
+        const int64_t chains = a.f.batch * a.f.dim;
+        const size_t nst = size_t(chains) * nseg * a.f.dstate;
+        if ((err = cudaMallocAsync(&seg_mem, (2 * nst + size_t(chains) * nseg) * sizeof(float),
+                                   stream)) != cudaSuccess)
+            return err;
+        a.hseg = static_cast<float*>(seg_mem);
+        a.gseg = a.hseg + nst;
+        a.sdt = a.gseg + nst;
+        err = cudaFuncSetAttribute(scan_bwd_kernel<io_t, NPL, G, UA, kBwdSummary>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmem));
+        if (err == cudaSuccess) {
+            scan_bwd_kernel<io_t, NPL, G, UA, kBwdSummary>
+                <<<unsigned(ctas * nseg), C::NTH, C::kSmem, stream>>>(a, int(dblocks), vec_red);
+            err = cudaGetLastError();
+        }
+        if (err == cudaSuccess) {
+            const int64_t n = chains * a.f.dstate;
+            bwd_carry_kernel<<<unsigned((n + 255) / 256), 256, 0, stream>>>(
+                a.f.A_log, a.hseg, a.gseg, a.sdt, chains, a.f.dim, a.f.dstate, a.nseg);
+            err = cudaGetLastError();
+        }
+    }
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(scan_bwd_kernel<io_t, NPL, G, UA, kBwdFull>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmem));
+    if (err == cudaSuccess) {
+        scan_bwd_kernel<io_t, NPL, G, UA, kBwdFull>
+            <<<unsigned(ctas * nseg), C::NTH, C::kSmem, stream>>>(a, int(dblocks), vec_red);
+        err = cudaGetLastError();
+    }
+    if (seg_mem) {
+        const cudaError_t ferr = cudaFreeAsync(seg_mem, stream);
+        if (err == cudaSuccess) err = ferr;
+    }
+    return err;
 }
 
 // Tile by dstate: NPL states per lane, G lanes per chain (G * NPL >= N).
