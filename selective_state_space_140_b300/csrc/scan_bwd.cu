@@ -532,8 +532,11 @@ cudaError_t launch_bwd(const BwdArgs& a0, bool vec_red, cudaStream_t stream) {
     const int64_t ctas = dblocks * a0.f.batch;
     const int64_t nchunks = (a0.f.seqlen + kBT - 1) / kBT;
     // Few CTAs for the GPU (under two per SM) and a long sequence: split the
-    // sequence into segments (at least 32 chunks each) so that every SM holds
-    // about 7 CTAs.  MAMBA_BWD_SEGMENTS forces a segment count.
+    // sequence into segments (at least 32 chunks each), about two waves of 7
+    // CTAs per SM (measured on the 1 x 1536 x 131072 layer: 11.7 ms against
+    // 12.6 ms with one wave; with two or more CTAs per SM unsplit a split was
+    // slower: 9.6 vs 7.2 ms at 2 x 2048 x 8192, N 64).  MAMBA_BWD_SEGMENTS
+    // forces a segment count.
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess)
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -542,7 +545,7 @@ cudaError_t launch_bwd(const BwdArgs& a0, bool vec_red, cudaStream_t stream) {
     if (env && atoi(env) > 0) {
         nseg = atoi(env);
     } else if (ctas < 2 * int64_t(sms) && nchunks >= 64) {
-        nseg = (7 * int64_t(sms) + ctas - 1) / ctas;
+        nseg = (14 * int64_t(sms) + ctas - 1) / ctas;
         if (nseg > nchunks / 32) nseg = nchunks / 32;
     }
     if (nseg > nchunks) nseg = nchunks;
