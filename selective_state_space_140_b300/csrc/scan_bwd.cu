@@ -598,22 +598,26 @@ cudaError_t launch_bwd(const BwdArgs& a0, bool vec_red, cudaStream_t stream) {
 }
 
 // Tile by dstate: NPL states per lane, G lanes per chain (G * NPL >= N).
-// Four lanes per chain at dstate 16 give twice the warps of two and measured
-// faster on B300 (Mamba-1.4B-style layer: 3.2 ms vs 4.4 ms); the adjoint's
-// step loop is unrolled by two, which keeps the registers at 128 (8 CTAs per
-// SM) and beat a full unroll.  MAMBA_BWD_TILE=1 selects 8 states x 2 lanes at
-// dstate <= 16.
+// Four states per lane up to dstate 64: more lanes per chain give more warps
+// to hide latency, and measured faster on B300 than eight states per lane
+// (Mamba-1.4B-style layer at dstate 16: 3.2 ms vs 4.3 ms with 8 x 2; 2 x 2048
+// x 8192 at dstate 64: 6.1 vs 7.2 ms with 8 x 8; 4 x 2048 x 4096 at dstate
+// 32: 2.8 vs 3.1 ms with 8 x 4).  The adjoint's step loop is unrolled by two,
+// which keeps the 4-state tiles at 128 registers (8 CTAs per SM).
+// MAMBA_BWD_TILE selects the 8-state tiles instead: 1 for dstate <= 16 (8 x 2),
+// 3 for dstate 17..64 (8 x 4, 8 x 8).
 template <typename io_t>
 cudaError_t dispatch_bwd(const BwdArgs& a, bool vec_red, cudaStream_t stream) {
     const int N = a.f.dstate;
-    if (N <= 16) {
-        const char* v = getenv("MAMBA_BWD_TILE");
-        if (v && atoi(v) == 1) return launch_bwd<io_t, 8, 2>(a, vec_red, stream);
-    }
+    const char* v = getenv("MAMBA_BWD_TILE");
+    const int tile = v ? atoi(v) : 0;
+    if (tile == 1 && N <= 16) return launch_bwd<io_t, 8, 2>(a, vec_red, stream);
+    if (tile == 3 && N > 16 && N <= 32) return launch_bwd<io_t, 8, 4>(a, vec_red, stream);
+    if (tile == 3 && N > 32 && N <= 64) return launch_bwd<io_t, 8, 8>(a, vec_red, stream);
     if (N <= 8) return launch_bwd<io_t, 4, 2>(a, vec_red, stream);
     if (N <= 16) return launch_bwd<io_t, 4, 4>(a, vec_red, stream);
-    if (N <= 32) return launch_bwd<io_t, 8, 4>(a, vec_red, stream);
-    if (N <= 64) return launch_bwd<io_t, 8, 8>(a, vec_red, stream);
+    if (N <= 32) return launch_bwd<io_t, 4, 8>(a, vec_red, stream);
+    if (N <= 64) return launch_bwd<io_t, 4, 16>(a, vec_red, stream);
     if (N <= 128) return launch_bwd<io_t, 8, 16>(a, vec_red, stream);
     return launch_bwd<io_t, 8, 32>(a, vec_red, stream);
 }

@@ -248,3 +248,15 @@ def test_long_sequence_layer_on_sampled_channels(cuda):
         part.update({"dA_log": gg["dA_log"][d:d + 1], "dD": gg["dD"][d:d + 1],
                      "ddelta_bias": gg["ddelta_bias"][d:d + 1]})
         _assert_grads(x, part, {k: gr[k] for k in part}, what=f"channel {d}")
+
+
+@pytest.mark.parametrize("N", [24, 32, 40, 64])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_eight_state_tiles_for_wide_states(cuda, monkeypatch, N, io):
+    """The selectable 8-state tiles for dstate 17..64 (8 x 4 and 8 x 8 lanes
+    per chain, MAMBA_BWD_TILE=3) match the oracle, with a partial CTA and
+    padded states (the default 4-state tiles are covered by every other test)."""
+    monkeypatch.setenv("MAMBA_BWD_TILE", "3")
+    x = workloads.make_scan_inputs(2, 11, 150, N, io, seed=21 + N, d_mode="normal")
+    dout = _dout(x, 21)
+    _assert_grads(x, _gpu_bwd(x, dout, cuda), _oracle_bwd(x, dout), what=f"N={N} tile 3")
