@@ -3,7 +3,6 @@
 The library must load, export every function include/mamba_scan.h declares,
 and reject bad arguments with the documented status before touching CUDA.
 """
-import ctypes
 import os
 import re
 
