@@ -32,8 +32,10 @@
  *     mamba_selective_scan_fwd_noalloc) and mamba_selective_scan_bwd take
  *     scratch memory, stream-ordered on the call's stream.
  *   - io_dtype (MAMBA_F32 or MAMBA_BF16) is the element type of every
- *     "io" array (u, delta, z, B, C, y; x, dt, z, B, C, out for decode).
- *     A_log, D, the bias and the state are always fp32.  Arithmetic is fp32;
+ *     "io" array (u, delta, z, B, C, y; x, dt, z, B, C, out for decode; dout,
+ *     du, ddelta, dz for the backward; x, out and the conv state for conv1d).
+ *     A_log, D, the bias, the scan state and the parameter gradients are
+ *     always fp32.  Arithmetic is fp32;
  *     bf16 results are rounded to nearest even.
  *   - Work is enqueued on `stream` (0 = legacy default stream) and runs
  *     asynchronously; the call does not synchronise.  A non-zero return means
@@ -44,7 +46,9 @@
  *     lengths that keep it) lets the kernels use 128-bit accesses; any other
  *     aligned input takes a scalar path and gives the same results.
  *   - Outputs must not overlap inputs (MAMBA_ERR_ALIAS), except that the
- *     decode state is updated in place by design.
+ *     decode state (mamba_selective_state_update) and the conv state
+ *     (mamba_causal_conv1d_update) are updated in place by design, and that
+ *     mamba_selective_scan_fwd_ex may read h0 from its last_state buffer.
  *   - A required array that has no elements (a zero size) may be NULL.
  */
 #ifndef MAMBA_SCAN_H
