@@ -117,8 +117,12 @@ int mamba_selective_scan_fwd(const void *u, const void *delta, const float *A_lo
 
 /*
  * mamba_selective_scan_fwd without any allocation.  This entry point has no
- * counterpart in the pages: it exists for callers that must not allocate
- * (CUDA graph capture without memory nodes, no allocator at hand).
+ * counterpart in the pages.  It is for callers that cannot call cudaMalloc or
+ * cudaMallocAsync: a framework that hands out all device memory from its own
+ * pool and does not let libraries allocate behind its back, or a serving loop
+ * that must not enter the driver's allocator mid-request (an allocation can
+ * synchronise the device or fail under memory pressure at a moment the caller
+ * does not control).
  *
  * Same arguments, same operation and same results as mamba_selective_scan_fwd
  * (bit for bit: the same kernels run with the same split).  When the scan is
@@ -134,8 +138,8 @@ int mamba_selective_scan_fwd(const void *u, const void *delta, const float *A_lo
  *     before anything is launched.
  *   - Nothing in the buffer has to start at zero.
  *   - Calls that overlap in time on one device (other streams, other host
- *     threads, or graphs replayed concurrently) share the buffer and race.
- *     Calls ordered on one stream are safe.
+ *     threads) share the buffer and race.  Calls ordered on one stream are
+ *     safe.
  */
 int mamba_selective_scan_fwd_noalloc(const void *u, const void *delta, const float *A_log,
                                      const void *B, const void *C, const float *D,
