@@ -47,3 +47,13 @@ def test_decode_counts():
     assert c["bytes"] == 8 * B * D * N + 4 * B * D * 2 + 2 * B * N * 2 + 4 * D * N + 8 * D
     assert c["bytes"] == 142_917_632
     assert c["updates"] == B * D * N
+
+
+def test_launch_count_mirrors_the_split_planner():
+    """One kernel per step when the grid fills the GPU; summary, carry and full
+    pass (3) for few chains and a long sequence, on a 148-SM B300."""
+    cfgs = workloads.SCAN_CONFIGS
+    assert bench.launches_per_step(cfgs["mamba1p4b_bf16"], 148) == 1
+    assert bench.launches_per_step(cfgs["mamba130m_bf16"], 148) == 1
+    assert bench.launches_per_step(cfgs["dna_long_bf16"], 148) == 3
+    assert bench.launches_per_step(cfgs["large_state_f32"], 148) == 1
