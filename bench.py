@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import sys
 import threading
@@ -102,13 +103,22 @@ PROFILED_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """C++/CUDA source without comments and whitespace runs, so that a stored
+    figure stays matched while only comments change."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(prefix: str = "scan_fwd") -> str:
-    """Hash of the sources of one kernel family, to match stored ncu figures."""
+    """Hash of the code (comments and whitespace removed) of one kernel
+    family's sources, to match stored ncu figures."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "selective_state_space_140_b300", "csrc")
     for name in PROFILED_SOURCES[prefix]:
-        with open(os.path.join(csrc, name), "rb") as fh:
-            h.update(name.encode() + fh.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as fh:
+            h.update(name.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -14,6 +14,13 @@
 //                     and form every gradient of the step (the fp64 oracle
 //                     writes the same chain rule out).
 //
+// Few chains over a long sequence split it along time: a summary pass gives
+// each (chain, segment) its zero-start end state, sum of dt and zero-start
+// adjoint leaving to the left; a carry pass passes states forwards and
+// adjoints backwards across segments (both decay by exp(A * sum of dt over
+// the segment)); the full pass then runs every segment from its entering
+// state and adjoint, all segments in parallel.
+//
 // Latency: every chunk's raw inputs (delta, u, dout, z, B, C and the
 // checkpoint) are fetched into registers one chunk ahead, so the loads of
 // chunk k-1 are in flight while chunk k computes; loops have compile-time trip
