@@ -100,6 +100,7 @@ PROFILED_SOURCES = {
     "scan_bwd": ("scan_bwd.cu", "common.cuh"),
     "conv1d": ("conv1d.cu", "common.cuh"),
     "scan_complex": ("scan_complex.cu", "common.cuh"),
+    "state_update": ("state_update.cu", "common.cuh"),
 }
 
 
@@ -767,7 +768,10 @@ def bench_decode(args, dcfg, device, peaks) -> dict:
             "state_updates_per_s": cnt["updates"] / t, "gbs": round(gbs, 1),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
                          "peak": float(peaks["hbm_gbs"]), "unit": "GB/s",
-                         "frac": round(gbs / float(peaks["hbm_gbs"]), 4), "traffic": None},
+                         "frac": round(gbs / float(peaks["hbm_gbs"]), 4),
+                         "traffic": stored_traffic(dcfg.name, kernel_source_hash("state_update"),
+                                                   "state_update"),
+                         "bytes_per_launch": cnt["bytes"]},
             "steps": steps, "state_buffers": nbuf, "gpu_launches": steps}
 
 
