@@ -198,13 +198,18 @@ int oracle_selective_scan_f64(const double *u, const double *delta, const double
  * [dim]; all are overwritten.  Single-threaded: the shared sums are formed in
  * a fixed order.  Returns 0, or a negative value on a bad argument.
  */
-int oracle_selective_scan_bwd_f64(const double *u, const double *delta, const double *A_log,
-                                  const double *B, const double *C, const double *D,
-                                  const double *z, const double *delta_bias, int softplus_flag,
-                                  const double *dout, double *du, double *ddelta,
-                                  double *dA_log, double *dB, double *dC, double *dD,
-                                  double *dz, double *ddelta_bias, int64_t batch, int64_t dim,
-                                  int64_t seqlen, int64_t dstate) {
+/* The backward with an optional starting state h0 [batch][dim][dstate], an
+ * optional reset mask [batch][seqlen] (non-zero: the state restarts from zero
+ * before that step, as in oracle_selective_scan_f64) and the gradient of h0
+ * (dh0, same layout; written when non-NULL).  A reset makes the step's decay
+ * exactly zero: h_t = 0 * h_{t-1} + dt B u, so nothing flows back across it. */
+static int scan_bwd_impl(const double *u, const double *delta, const double *A_log,
+                         const double *B, const double *C, const double *D, const double *z,
+                         const double *delta_bias, int softplus_flag, const double *h0,
+                         const unsigned char *reset, const double *dout, double *du,
+                         double *ddelta, double *dA_log, double *dB, double *dC, double *dD,
+                         double *dz, double *ddelta_bias, double *dh0, int64_t batch,
+                         int64_t dim, int64_t seqlen, int64_t dstate) {
     if (!u || !delta || !A_log || !B || !C || !dout || !du || !ddelta || !dA_log || !dB || !dC)
         return -1;
     if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 0) return -2;
@@ -233,6 +238,8 @@ int oracle_selective_scan_bwd_f64(const double *u, const double *delta, const do
             const double *zz = z ? z + chain * L : NULL;
             const double *Bb = B + b * L * N, *Cb = C + b * L * N;
             const double Dd = D ? D[d] : 0.0, bias = delta_bias ? delta_bias[d] : 0.0;
+            const double *hin = h0 ? h0 + chain * N : NULL;         /* state before step 0 */
+            const unsigned char *rsb = reset ? reset + b * L : NULL;  /* document starts */
             for (int64_t n = 0; n < N; ++n) A[n] = -exp(A_log[d * N + n]);
             /* forward, keeping every state */
             for (int64_t t = 0; t < L; ++t) {
@@ -241,8 +248,8 @@ int oracle_selective_scan_bwd_f64(const double *u, const double *delta, const do
                 dts[t] = dt;
                 double acc = 0.0;
                 for (int64_t n = 0; n < N; ++n) {
-                    const double hp = t > 0 ? hs[(t - 1) * N + n] : 0.0;
-                    const double a = exp(dt * A[n]);
+                    const double hp = t > 0 ? hs[(t - 1) * N + n] : (hin ? hin[n] : 0.0);
+                    const double a = (rsb && rsb[t]) ? 0.0 : exp(dt * A[n]);
                     ab[t * N + n] = a;
                     hs[t * N + n] = a * hp + dt * Bb[t * N + n] * uc[t];
                     acc += Cb[t * N + n] * hs[t * N + n];
@@ -263,7 +270,7 @@ int oracle_selective_scan_bwd_f64(const double *u, const double *delta, const do
                 const double dt = dts[t];
                 for (int64_t n = 0; n < N; ++n) {
                     const double gn = dy * Cb[t * N + n] + g[n];
-                    const double hp = t > 0 ? hs[(t - 1) * N + n] : 0.0;
+                    const double hp = t > 0 ? hs[(t - 1) * N + n] : (hin ? hin[n] : 0.0);
                     const double a = ab[t * N + n];
                     dC[(b * L + t) * N + n] += dy * hs[t * N + n];
                     dB[(b * L + t) * N + n] += gn * dt * uc[t];
@@ -278,12 +285,44 @@ int oracle_selective_scan_bwd_f64(const double *u, const double *delta, const do
                 ddelta[chain * L + t] = dr;
                 if (ddelta_bias) ddelta_bias[d] += dr;
             }
+            /* Abar_0 g_0: what flows into the state before step 0 */
+            if (dh0)
+                for (int64_t n = 0; n < N; ++n) dh0[chain * N + n] = g[n];
         }
     }
     for (int64_t d = 0; d < dim; ++d)
         for (int64_t n = 0; n < N; ++n) dA_log[d * N + n] = dA[d * N + n] * -exp(A_log[d * N + n]);
     free(hs); free(ab); free(dts); free(ys); free(A); free(g); free(dA);
     return 0;
+}
+
+int oracle_selective_scan_bwd_f64(const double *u, const double *delta, const double *A_log,
+                                  const double *B, const double *C, const double *D,
+                                  const double *z, const double *delta_bias, int softplus_flag,
+                                  const double *dout, double *du, double *ddelta,
+                                  double *dA_log, double *dB, double *dC, double *dD,
+                                  double *dz, double *ddelta_bias, int64_t batch, int64_t dim,
+                                  int64_t seqlen, int64_t dstate) {
+    return scan_bwd_impl(u, delta, A_log, B, C, D, z, delta_bias, softplus_flag, NULL, NULL,
+                         dout, du, ddelta, dA_log, dB, dC, dD, dz, ddelta_bias, NULL, batch,
+                         dim, seqlen, dstate);
+}
+
+/* The backward of oracle_selective_scan_f64 with h0 and document resets
+ * (codechina.net overview, section 3.2 point 2 and the deployment notes on
+ * block-by-block processing); dh0 receives the gradient of h0. */
+int oracle_selective_scan_bwd_ex_f64(const double *u, const double *delta, const double *A_log,
+                                     const double *B, const double *C, const double *D,
+                                     const double *z, const double *delta_bias,
+                                     int softplus_flag, const double *h0,
+                                     const unsigned char *reset, const double *dout, double *du,
+                                     double *ddelta, double *dA_log, double *dB, double *dC,
+                                     double *dD, double *dz, double *ddelta_bias, double *dh0,
+                                     int64_t batch, int64_t dim, int64_t seqlen,
+                                     int64_t dstate) {
+    return scan_bwd_impl(u, delta, A_log, B, C, D, z, delta_bias, softplus_flag, h0, reset,
+                         dout, du, ddelta, dA_log, dB, dC, dD, dz, ddelta_bias, dh0, batch, dim,
+                         seqlen, dstate);
 }
 
 /*

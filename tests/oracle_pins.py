@@ -369,10 +369,12 @@ def check_reset_at_start_ignores_h0(lib):
     _close(h1, h0, rtol=0, what="state after a reset on step 0")
 
 
-def _fd_check(lib, softplus, with_opt, seed):
+def _fd_check(lib, softplus, with_opt, seed, ex=False):
     """Central differences of the forward oracle's loss sum(dout * y) with
     respect to every element of every input must equal the gradients of the
-    backward oracle (fp64: steps of 1e-6 leave errors near 1e-9)."""
+    backward oracle (fp64: steps of 1e-6 leave errors near 1e-9).  With
+    ``ex`` the scans also start from a random h0 (its gradient checked too)
+    and carry document boundaries (a reset inside each batch row)."""
     r = _rng(seed)
     b, d, L, N = 2, 2, 5, 3
     x = dict(u=r.normal(size=(b, d, L)), delta=r.normal(size=(b, d, L)),
@@ -382,20 +384,25 @@ def _fd_check(lib, softplus, with_opt, seed):
         x["delta"] = np.abs(x["delta"]) * 0.3 + 0.05
     if with_opt:
         x.update(D=r.normal(size=d), z=r.normal(size=(b, d, L)), delta_bias=r.normal(size=d))
+    reset = None
+    if ex:
+        x["h0"] = r.normal(size=(b, d, N))
+        reset = np.zeros((b, L), dtype=np.uint8)
+        reset[0, 2] = reset[1, 3] = 1
     dout = r.normal(size=(b, d, L))
 
     def loss(xx):
         y, _, _ = oracle.selective_scan(xx["u"], xx["delta"], xx["A_log"], xx["B"], xx["C"],
                                         D=xx.get("D"), z=xx.get("z"),
                                         delta_bias=xx.get("delta_bias"), softplus=softplus,
-                                        nthreads=1, lib=lib)
+                                        h0=xx.get("h0"), reset=reset, nthreads=1, lib=lib)
         return float(np.sum(dout * y))
 
     g = oracle.selective_scan_bwd(x["u"], x["delta"], x["A_log"], x["B"], x["C"], dout,
                                   D=x.get("D"), z=x.get("z"), delta_bias=x.get("delta_bias"),
-                                  softplus=softplus, lib=lib)
+                                  softplus=softplus, h0=x.get("h0"), reset=reset, lib=lib)
     names = {"u": "du", "delta": "ddelta", "A_log": "dA_log", "B": "dB", "C": "dC", "D": "dD",
-             "z": "dz", "delta_bias": "ddelta_bias"}
+             "z": "dz", "delta_bias": "ddelta_bias", "h0": "dh0"}
     eps = 1e-6
     for k, gk in names.items():
         if k not in x:
@@ -608,6 +615,61 @@ def check_complex_conjugation_symmetry(lib):
     _close(h2, h1.conj(), rtol=1e-12, what="conjugated state")
 
 
+def check_backward_finite_differences_h0_reset(lib):
+    _fd_check(lib, softplus=True, with_opt=True, seed=15, ex=True)
+
+
+def check_backward_reset_splits_documents(lib):
+    """A document boundary at step L1 makes the backward of the whole row equal
+    the backwards of the two documents taken alone (the second from a zero
+    state): per-element gradients and dB/dC per step match piecewise, the
+    summed dA_log, dD and bias gradients add up, and no gradient reaches h0
+    from the second document."""
+    r = _rng(16)
+    b, d, L, N, L1 = 1, 3, 12, 4, 5
+    x = dict(u=r.normal(size=(b, d, L)), delta=r.normal(size=(b, d, L)),
+             A_log=r.normal(size=(d, N)) * 0.5, B=r.normal(size=(b, L, N)),
+             C=r.normal(size=(b, L, N)), dout=r.normal(size=(b, d, L)))
+    kw = dict(D=r.normal(size=d), z=r.normal(size=(b, d, L)), delta_bias=r.normal(size=d))
+    h0 = r.normal(size=(b, d, N))
+    reset = np.zeros((b, L))
+    reset[0, L1] = 1
+    whole = oracle.selective_scan_bwd(x["u"], x["delta"], x["A_log"], x["B"], x["C"], x["dout"],
+                                      h0=h0, reset=reset, lib=lib, **kw)
+
+    def piece(lo, hi, start):
+        t = lambda a: a[:, :, lo:hi] if a.ndim == 3 and a.shape[2] == L else a
+        return oracle.selective_scan_bwd(
+            t(x["u"]), t(x["delta"]), x["A_log"], x["B"][:, lo:hi], x["C"][:, lo:hi],
+            t(x["dout"]), D=kw["D"], z=t(kw["z"]), delta_bias=kw["delta_bias"], h0=start,
+            lib=lib)
+
+    first, second = piece(0, L1, h0), piece(L1, L, np.zeros_like(h0))
+    for k in ("du", "ddelta", "dz"):
+        _close(whole[k], np.concatenate([first[k], second[k]], axis=2), rtol=1e-12, what=k)
+    for k in ("dB", "dC"):
+        _close(whole[k], np.concatenate([first[k], second[k]], axis=1), rtol=1e-12, what=k)
+    for k in ("dA_log", "dD", "ddelta_bias"):
+        _close(whole[k], first[k] + second[k], rtol=1e-12, what=k)
+    _close(whole["dh0"], first["dh0"], rtol=1e-12, what="dh0")
+
+
+def check_backward_reset_at_start_cuts_h0(lib):
+    """A reset at step 0 discards h0: its gradient is exactly zero and every
+    other gradient equals that of the scan started from zero."""
+    r = _rng(17)
+    b, d, L, N = 2, 2, 9, 3
+    a = [r.normal(size=(b, d, L)), r.normal(size=(b, d, L)), r.normal(size=(d, N)),
+         r.normal(size=(b, L, N)), r.normal(size=(b, L, N)), r.normal(size=(b, d, L))]
+    reset = np.zeros((b, L))
+    reset[:, 0] = 1
+    g = oracle.selective_scan_bwd(*a, h0=r.normal(size=(b, d, N)), reset=reset, lib=lib)
+    g0 = oracle.selective_scan_bwd(*a, lib=lib)
+    assert np.all(g["dh0"] == 0.0)
+    for k in g0:
+        _close(g[k], g0[k], rtol=1e-12, what=k)
+
+
 ALL_CHECKS = [
     check_delta_zero_limit,
     check_single_step,
@@ -626,6 +688,9 @@ ALL_CHECKS = [
     check_reset_at_start_ignores_h0,
     check_backward_finite_differences,
     check_backward_finite_differences_plain,
+    check_backward_finite_differences_h0_reset,
+    check_backward_reset_splits_documents,
+    check_backward_reset_at_start_cuts_h0,
     check_conv_against_numpy_convolve,
     check_conv_impulse_response,
     check_conv_silu_closed_forms,

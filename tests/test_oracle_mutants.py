@@ -56,6 +56,16 @@ MUTANTS = [
     ("bwd_ddt_without_input_term", "ddt += gn * (A[n] * a * hp + uc[t] * Bb[t * N + n]);",
      "ddt += gn * (A[n] * a * hp);"),
     ("bwd_du_without_skip", "double dut = dy * Dd, ddt = 0.0;", "double dut = 0.0, ddt = 0.0;"),
+    ("bwd_reset_ignored", "const double a = (rsb && rsb[t]) ? 0.0 : exp(dt * A[n]);",
+     "const double a = exp(dt * A[n]);"),
+    ("bwd_reset_one_step_late", "const double a = (rsb && rsb[t]) ? 0.0 : exp(dt * A[n]);",
+     "const double a = (rsb && t > 0 && rsb[t - 1]) ? 0.0 : exp(dt * A[n]);"),
+    ("bwd_adjoint_ignores_h0",
+     "const double gn = dy * Cb[t * N + n] + g[n];\n"
+     "                    const double hp = t > 0 ? hs[(t - 1) * N + n] : (hin ? hin[n] : 0.0);",
+     "const double gn = dy * Cb[t * N + n] + g[n];\n"
+     "                    const double hp = t > 0 ? hs[(t - 1) * N + n] : 0.0;"),
+    ("bwd_dh0_dropped", "dh0[chain * N + n] = g[n];", "dh0[chain * N + n] = 0.0;"),
     ("conv_window_one_step_late", "pre += w[k] * conv_input(xr, st, width, t - (width - 1) + k);",
      "pre += w[k] * conv_input(xr, st, width, t - width + k);"),
     ("conv_taps_reversed", "pre += w[k] * conv_input(xr, st, width, t - (width - 1) + k);",
