@@ -219,6 +219,35 @@ int mamba_selective_scan_bwd(const void *u, const void *delta, const float *A_lo
                              mamba_stream_t stream);
 
 /*
+ * mamba_selective_scan_bwd for the scan of mamba_selective_scan_fwd_ex: from a
+ * starting state h0 and with document boundaries (codechina.net overview,
+ * section 3.2 point 2: resetting the hidden state isolates documents; the
+ * same page's deployment notes on block-by-block processing of long
+ * sequences).  Training on packed documents, or on one long sequence cut into
+ * blocks, needs these gradients.
+ *
+ *   h0    : [batch, dim, dstate] fp32 or NULL (zero start), as for the forward
+ *   reset : [batch, seqlen] bytes or NULL; non-zero at a token that starts a
+ *           document (the state restarts from zero before it): no gradient
+ *           flows back across it
+ *   dh0   : [batch, dim, dstate] fp32 or NULL (not wanted), written with the
+ *           gradient of h0 (of a zero start when h0 is NULL); zero when
+ *           seqlen == 0
+ *
+ * Every other argument, layout, scratch rule and error is as for
+ * mamba_selective_scan_bwd, which is this call with h0, reset and dh0 NULL
+ * (bit for bit).  h0 and reset must not overlap any output (MAMBA_ERR_ALIAS).
+ */
+int mamba_selective_scan_bwd_ex(const void *u, const void *delta, const float *A_log,
+                                const void *B, const void *C, const float *D, const void *z,
+                                const float *delta_bias, int softplus_flag, const float *h0,
+                                const unsigned char *reset, const void *dout, void *du,
+                                void *ddelta, void *dz, float *dA_log, float *dB, float *dC,
+                                float *dD, float *ddelta_bias, float *dh0, int64_t batch,
+                                int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
+                                mamba_stream_t stream);
+
+/*
  * Single-token decode step (recurrent inference: each new token touches only
  * the previous state -- tutorial "核心概念"; mhpn.cn article section 3).
  *

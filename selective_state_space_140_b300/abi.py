@@ -25,6 +25,7 @@ MAX_DSTATE = 256
 # Every symbol include/mamba_scan.h declares.
 EXPORTED = ("mamba_selective_scan_fwd", "mamba_selective_scan_fwd_noalloc",
             "mamba_selective_scan_fwd_ex", "mamba_selective_scan_bwd",
+            "mamba_selective_scan_bwd_ex",
             "mamba_selective_scan_complex_fwd",
             "mamba_causal_conv1d_fwd", "mamba_causal_conv1d_update",
             "mamba_selective_state_update", "mamba_device_status", "mamba_status_string",
@@ -54,6 +55,10 @@ def _declare(lib):
     lib.mamba_selective_scan_bwd.restype = ci
     lib.mamba_selective_scan_bwd.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, vp, vp, vp, vp,
                                              fp, fp, fp, fp, fp, i64, i64, i64, i64, ci, vp]
+    lib.mamba_selective_scan_bwd_ex.restype = ci
+    lib.mamba_selective_scan_bwd_ex.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, fp, vp, vp, vp,
+                                                vp, vp, fp, fp, fp, fp, fp, fp, i64, i64, i64, i64,
+                                                ci, vp]
     lib.mamba_selective_scan_complex_fwd.restype = ci
     lib.mamba_selective_scan_complex_fwd.argtypes = [vp, vp, fp, fp, vp, vp, fp, vp, fp, ci, vp,
                                                      fp, i64, i64, i64, i64, ci, vp]
@@ -216,7 +221,7 @@ def _scan_fwd(entry, u, delta, A_log, B, C, D, z, delta_bias, softplus, y, last_
 
 def mamba_selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_bias=None,
                              softplus=True, want_dD=True, want_ddelta_bias=True, grads=None,
-                             stream=None):
+                             stream=None, h0=None, reset=None, want_dh0=None):
     """Gradients of ``mamba_selective_scan_fwd`` (zero initial state) for the
     output gradient ``dout``; returns a dict with ``du``, ``ddelta``,
     ``dA_log``, ``dB``, ``dC`` and, when wanted, ``dz`` (iff ``z`` is given),
@@ -225,7 +230,13 @@ def mamba_selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_
     du/ddelta/dz have the io dtype of ``u``; dA_log [dim, dstate], dB/dC
     [batch, seqlen, dstate], dD/ddelta_bias [dim] are float32 (dB and dC sum
     over the channels).  ``grads`` may hold preallocated outputs by the same
-    names.  Runs on ``stream`` and does not synchronise."""
+    names.  Runs on ``stream`` and does not synchronise.
+
+    ``h0`` [batch, dim, dstate] float32 (the state before step 0) and ``reset``
+    [batch, seqlen] uint8 or bool (non-zero at a document start) select the
+    backward of ``mamba_selective_scan_fwd_ex`` (C entry
+    ``mamba_selective_scan_bwd_ex``); ``dh0``, the gradient of h0, is
+    returned when h0 is given (or ``want_dh0``)."""
     dev = u.device
     batch, dim, seqlen = u.shape
     dstate = A_log.shape[-1]
@@ -251,13 +262,37 @@ def mamba_selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_
         _check(g[k], k, dev, dtype)
         if tuple(g[k].shape) != tuple(shape):
             raise TypeError(f"{k} must have shape {tuple(shape)}")
-    rc = load().mamba_selective_scan_bwd(
-        _ptr(u), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
-        int(bool(softplus)), _ptr(dout), _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g.get("dz")),
-        _ptr(g["dA_log"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g.get("dD")),
-        _ptr(g.get("ddelta_bias")), batch, dim, seqlen, dstate, io, _stream(stream, dev))
+    if want_dh0 is None:
+        want_dh0 = h0 is not None
+    _check(h0, "h0", dev, torch.float32)
+    if reset is not None:
+        _check(reset, "reset", dev)
+        if reset.dtype == torch.bool:
+            reset = reset.view(torch.uint8)
+        if reset.dtype != torch.uint8 or reset.shape != (batch, seqlen):
+            raise TypeError("reset must be uint8 or bool of shape [batch, seqlen]")
+    if want_dh0:
+        shapes["dh0"] = ((batch, dim, dstate), f32)
+        if g.get("dh0") is None:
+            g["dh0"] = torch.empty((batch, dim, dstate), device=dev, dtype=f32)
+        _check(g["dh0"], "dh0", dev, f32)
+    if h0 is None and reset is None and not want_dh0:
+        rc = load().mamba_selective_scan_bwd(
+            _ptr(u), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+            _ptr(delta_bias), int(bool(softplus)), _ptr(dout), _ptr(g["du"]), _ptr(g["ddelta"]),
+            _ptr(g.get("dz")), _ptr(g["dA_log"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g.get("dD")),
+            _ptr(g.get("ddelta_bias")), batch, dim, seqlen, dstate, io, _stream(stream, dev))
+        entry = "mamba_selective_scan_bwd"
+    else:
+        rc = load().mamba_selective_scan_bwd_ex(
+            _ptr(u), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+            _ptr(delta_bias), int(bool(softplus)), _ptr(h0), _ptr(reset), _ptr(dout),
+            _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g.get("dz")), _ptr(g["dA_log"]), _ptr(g["dB"]),
+            _ptr(g["dC"]), _ptr(g.get("dD")), _ptr(g.get("ddelta_bias")), _ptr(g.get("dh0")),
+            batch, dim, seqlen, dstate, io, _stream(stream, dev))
+        entry = "mamba_selective_scan_bwd_ex"
     if rc != 0:
-        raise MambaError(rc, "mamba_selective_scan_bwd")
+        raise MambaError(rc, entry)
     return {k: g[k] for k in shapes}
 
 
@@ -433,3 +468,13 @@ def raw_scan_complex_fwd(u, delta, A_log_re, A_im, B, C, D, z, delta_bias, softp
     return load().mamba_selective_scan_complex_fwd(u, delta, A_log_re, A_im, B, C, D, z,
                                                    delta_bias, softplus_flag, y, last_state, batch,
                                                    dim, seqlen, dstate, io_dtype, stream)
+
+
+def raw_scan_bwd_ex(u, delta, A_log, B, C, D, z, delta_bias, softplus_flag, h0, reset, dout, du,
+                    ddelta, dz, dA_log, dB, dC, dD, ddelta_bias, dh0, batch, dim, seqlen, dstate,
+                    io_dtype, stream) -> int:
+    """``mamba_selective_scan_bwd_ex`` with plain integers as pointers."""
+    return load().mamba_selective_scan_bwd_ex(u, delta, A_log, B, C, D, z, delta_bias,
+                                              softplus_flag, h0, reset, dout, du, ddelta, dz,
+                                              dA_log, dB, dC, dD, ddelta_bias, dh0, batch, dim,
+                                              seqlen, dstate, io_dtype, stream)

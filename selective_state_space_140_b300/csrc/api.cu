@@ -198,6 +198,20 @@ int mamba_selective_scan_bwd(const void* u, const void* delta, const float* A_lo
                              float* dC, float* dD, float* ddelta_bias, int64_t batch,
                              int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
                              mamba_stream_t stream) {
+    return mamba_selective_scan_bwd_ex(u, delta, A_log, B, C, D, z, delta_bias, softplus_flag,
+                                       nullptr, nullptr, dout, du, ddelta, dz, dA_log, dB, dC,
+                                       dD, ddelta_bias, nullptr, batch, dim, seqlen, dstate,
+                                       io_dtype, stream);
+}
+
+int mamba_selective_scan_bwd_ex(const void* u, const void* delta, const float* A_log,
+                                const void* B, const void* C, const float* D, const void* z,
+                                const float* delta_bias, int softplus_flag, const float* h0,
+                                const unsigned char* reset, const void* dout, void* du,
+                                void* ddelta, void* dz, float* dA_log, float* dB, float* dC,
+                                float* dD, float* ddelta_bias, float* dh0, int64_t batch,
+                                int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
+                                mamba_stream_t stream) {
     if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
     if (dstate < 1 || dstate > MAMBA_MAX_DSTATE) return MAMBA_ERR_DSTATE;
     if (!size_ok(batch, dim, seqlen) || !size_ok(batch, seqlen, dstate) ||
@@ -212,20 +226,25 @@ int mamba_selective_scan_bwd(const void* u, const void* delta, const float* A_lo
         misaligned(C, es) || misaligned(dout, es) || misaligned(du, es) ||
         misaligned(ddelta, es) || misaligned(dz, es) || misaligned(A_log, 4) ||
         misaligned(D, 4) || misaligned(delta_bias, 4) || misaligned(dA_log, 4) ||
-        misaligned(dB, 4) || misaligned(dC, 4) || misaligned(dD, 4) || misaligned(ddelta_bias, 4))
+        misaligned(dB, 4) || misaligned(dC, 4) || misaligned(dD, 4) ||
+        misaligned(ddelta_bias, 4) || misaligned(h0, 4) || misaligned(dh0, 4))
         return MAMBA_ERR_ALIGN;
     const int64_t elems = batch * dim * seqlen, nbc = batch * seqlen * dstate;
+    const int64_t nst = batch * dim * dstate;
     const Range ins[] = {range_of(u, elems, es), range_of(delta, elems, es),
                          z ? range_of(z, elems, es) : Range{0, 0}, range_of(B, nbc, es),
                          range_of(C, nbc, es), range_of(A_log, dim * dstate, 4),
                          D ? range_of(D, dim, 4) : Range{0, 0},
                          delta_bias ? range_of(delta_bias, dim, 4) : Range{0, 0},
-                         range_of(dout, elems, es)};
+                         range_of(dout, elems, es),
+                         h0 ? range_of(h0, nst, 4) : Range{0, 0},
+                         reset ? range_of(reset, batch * seqlen, 1) : Range{0, 0}};
     const Range outs[] = {range_of(du, elems, es), range_of(ddelta, elems, es),
                           z ? range_of(dz, elems, es) : Range{0, 0},
                           range_of(dA_log, dim * dstate, 4), range_of(dB, nbc, 4),
                           range_of(dC, nbc, 4), dD ? range_of(dD, dim, 4) : Range{0, 0},
-                          ddelta_bias ? range_of(ddelta_bias, dim, 4) : Range{0, 0}};
+                          ddelta_bias ? range_of(ddelta_bias, dim, 4) : Range{0, 0},
+                          dh0 ? range_of(dh0, nst, 4) : Range{0, 0}};
     for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
         for (const Range& r : ins)
             if (overlaps(outs[i], r)) return MAMBA_ERR_ALIAS;
@@ -237,6 +256,8 @@ int mamba_selective_scan_bwd(const void* u, const void* delta, const float* A_lo
     mamba::ScanBwdArgs a{};
     a.f = mamba::ScanArgs{u, delta, A_log, B, C, D, z, delta_bias, nullptr, nullptr,
                           batch, dim, seqlen, int(dstate), softplus_flag != 0};
+    a.f.h0 = h0;
+    a.f.reset = reset;
     a.dout = dout;
     a.du = du;
     a.ddelta = ddelta;
@@ -246,6 +267,7 @@ int mamba_selective_scan_bwd(const void* u, const void* delta, const float* A_lo
     a.dC = dC;
     a.dD = dD;
     a.ddelta_bias = ddelta_bias;
+    a.dh0 = dh0;
     const cudaError_t err =
         mamba::launch_scan_bwd(a, io_dtype == MAMBA_BF16, reinterpret_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;

@@ -66,7 +66,8 @@ struct BwdCfg {
     static constexpr int oDt = 0, oU = kF, oDy = 2 * kF;
     static constexpr int oGu = 3 * kF, oGdt = 4 * kF;   // reduced sum_n g B, sum_n g (...)
     static constexpr int oYs = 5 * kF;                   // C.h
-    static constexpr int oB = 6 * kF, oC = oB + T * NP;
+    static constexpr int oDe = 6 * kF;  // dt in the decay: +inf at a document start (reset only)
+    static constexpr int oB = 7 * kF, oC = oB + T * NP;
     static constexpr int oH = oC + T * NP;  // [T][NQ][NTH] float4: states, then adjoints
     static constexpr int kFloats = oH + T * NQ * NTH * 4;
     static constexpr size_t kSmem = size_t(kFloats) * 4;
@@ -95,6 +96,7 @@ struct Raw {
     io_t dl[C::EPT], u[C::EPT], go[C::EPT], z[C::EPT];
     io_t B[C::BPT], Cc[C::BPT];
     float hs[NPL];  // checkpoint: the state at the chunk's start
+    unsigned char rs[C::EPT];  // document starts (when a reset mask is given)
 };
 
 template <typename io_t>
@@ -106,7 +108,7 @@ __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return _
 
 // Issue the loads of chunk k (REV: everything the reverse phase needs; else
 // only delta, u and B).  Out-of-range elements read as zero.
-template <typename io_t, int NPL, int G, bool REV>
+template <typename io_t, int NPL, int G, bool REV, bool EX>
 __device__ __forceinline__ void fetch(const BwdArgs& a, Raw<io_t, NPL, G>& r, int b, int64_t d0,
                                       int64_t k, int tid, const float* ck, bool chain_ok, int g) {
     using C = BwdCfg<io_t, NPL, G>;
@@ -123,6 +125,7 @@ __device__ __forceinline__ void fetch(const BwdArgs& a, Raw<io_t, NPL, G>& r, in
         const int64_t idx = ok ? (int64_t(b) * dim + d0 + c) * L + t0 + t : 0;
         r.dl[j] = ok ? __ldg(static_cast<const io_t*>(p.delta) + idx) : zero;
         r.u[j] = ok ? __ldg(static_cast<const io_t*>(p.u) + idx) : zero;
+        if constexpr (EX) r.rs[j] = (ok && p.reset) ? __ldg(p.reset + int64_t(b) * L + t0 + t) : 0;
         if constexpr (REV) {
             r.go[j] = ok ? __ldg(static_cast<const io_t*>(a.dout) + idx) : zero;
             r.z[j] = (ok && p.z) ? __ldg(static_cast<const io_t*>(p.z) + idx) : zero;
@@ -186,7 +189,9 @@ __device__ __forceinline__ void chain_product(const float* sm, const float4* S, 
 // unsplit).  MODE kBwdSummary: the segment's zero-start end state, its sum of
 // dt and its zero-start adjoint leaving to the left (no gradients), for the
 // carry pass of a time-split backward.
-template <typename io_t, int NPL, int G, int UA, int MODE>
+// EX: h0, document resets and dh0 are handled (compiled separately so that the
+// plain backward's code is unchanged by them).
+template <typename io_t, int NPL, int G, int UA, int MODE, bool EX>
 __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const int dblocks,
                                                          const bool vec_red) {
     using C = BwdCfg<io_t, NPL, G>;
@@ -226,11 +231,19 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
     for (int i = 0; i < NPL; ++i) {
         const int n = g * NPL + i;
         A[i] = (chain_ok && n < N) ? -expf(__ldg(p.A_log + d * N + n)) : 0.f;
-        A2[i] = A[i] * kLog2e;
-        // a later segment of a split starts from the carried state
-        h[i] = (MODE == kBwdFull && hsg && chain_ok && n < N) ? hsg[n] : 0.f;
+        // at most -1e-30, so that a document start's infinite decay step gives
+        // Abar = 0 exactly (and padded states, with B = C = 0, stay zero)
+        A2[i] = EX ? fminf(A[i] * kLog2e, -1e-30f) : A[i] * kLog2e;
+        // the first segment starts from h0 (or zero), a later one of a split
+        // from the carried state
+        float h_in = 0.f;
+        if (MODE == kBwdFull && chain_ok && n < N)
+            h_in = hsg ? hsg[n] : ((EX && p.h0) ? p.h0[chain * N + n] : 0.f);
+        h[i] = h_in;
     }
-    float dtsum = 0.f;  // summary: sum of dt over the segment
+    float dtsum = 0.f;  // summary: sum of the decay steps over the segment
+    const bool has_reset = EX && p.reset != nullptr;
+    constexpr float kDocStart = __builtin_inff();  // decay step of a document's first token
 
     // dt (and softplus') of element j of this thread in chunk k; zero past the data
     auto step_of = [&](float raw_delta, int64_t k, int j, float& sp) {
@@ -248,7 +261,7 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
 
     Raw<io_t, NPL, G> r;
     // ---------------- forward phase: checkpoints ----------------
-    if (kbeg < kend) fetch<io_t, NPL, G, false>(a, r, b, d0, kbeg, tid, ck, chain_ok, g);
+    if (kbeg < kend) fetch<io_t, NPL, G, false, EX>(a, r, b, d0, kbeg, tid, ck, chain_ok, g);
     for (int64_t k = kbeg; k < kend; ++k) {
         __syncthreads();
 #pragma unroll
@@ -258,6 +271,7 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
             if (e0 + j < C::kE) {
                 sm[C::oDt + (te0 + j) * S + ce] = dt;
                 sm[C::oU + (te0 + j) * S + ce] = dt * to_f(r.u[j]);  // dt u
+                if (has_reset) sm[C::oDe + (te0 + j) * S + ce] = r.rs[j] ? kDocStart : dt;
             }
         }
 #pragma unroll
@@ -270,16 +284,17 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
         }
         __syncthreads();
         if (k + 1 < kend)
-            fetch<io_t, NPL, G, false>(a, r, b, d0, k + 1, tid, ck, chain_ok, g);
+            fetch<io_t, NPL, G, false, EX>(a, r, b, d0, k + 1, tid, ck, chain_ok, g);
         else
-            fetch<io_t, NPL, G, true>(a, r, b, d0, k, tid, ck, chain_ok, g);
+            fetch<io_t, NPL, G, true, EX>(a, r, b, d0, k, tid, ck, chain_ok, g);
 #pragma unroll
         for (int t = 0; t < T; ++t) {
             const float dt = sm[C::oDt + t * S + c], du = sm[C::oU + t * S + c];
-            if (MODE == kBwdSummary) dtsum += dt;
+            const float de = has_reset ? sm[C::oDe + t * S + c] : dt;
+            if (MODE == kBwdSummary) dtsum += de;
 #pragma unroll
             for (int i = 0; i < NPL; ++i)
-                h[i] = fmaf(ex2_approx(dt * A2[i]), h[i], du * sm[C::oB + t * NP + g * NPL + i]);
+                h[i] = fmaf(ex2_approx(de * A2[i]), h[i], du * sm[C::oB + t * NP + g * NPL + i]);
         }
     }
     if (MODE == kBwdSummary && chain_ok) {
@@ -314,6 +329,7 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
             if (e0 + j < C::kE) {
                 sm[C::oDt + (te0 + j) * S + ce] = dt;
                 sm[C::oU + (te0 + j) * S + ce] = to_f(r.u[j]);
+                if (has_reset) sm[C::oDe + (te0 + j) * S + ce] = r.rs[j] ? kDocStart : dt;
             }
         }
 #pragma unroll
@@ -325,7 +341,7 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
 #pragma unroll
         for (int i = 0; i < NPL; ++i) hs[i] = r.hs[i];
         __syncthreads();
-        if (k > kbeg) fetch<io_t, NPL, G, true>(a, r, b, d0, k - 1, tid, ck, chain_ok, g);
+        if (k > kbeg) fetch<io_t, NPL, G, true, EX>(a, r, b, d0, k - 1, tid, ck, chain_ok, g);
         if constexpr (MODE == kBwdSummary) {
             // dy for every element, then the adjoint alone (no states needed)
 #pragma unroll
@@ -343,11 +359,12 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
 #pragma unroll UA
             for (int t = T - 1; t >= 0; --t) {
                 const int s = t * S + c;
-                const float dy = sm[C::oDy + s], dt = sm[C::oDt + s];
+                const float dy = sm[C::oDy + s];
+                const float de = has_reset ? sm[C::oDe + s] : sm[C::oDt + s];
 #pragma unroll
                 for (int i = 0; i < NPL; ++i) {
                     const float gn = fmaf(dy, sm[C::oC + t * NP + g * NPL + i], gc[i]);
-                    gc[i] = ex2_approx(dt * A2[i]) * gn;
+                    gc[i] = ex2_approx(de * A2[i]) * gn;
                 }
             }
             continue;
@@ -363,11 +380,12 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
             for (int t = 0; t < T; ++t) {
                 const float dt = sm[C::oDt + t * S + c];
                 const float du = dt * sm[C::oU + t * S + c];
+                const float de = has_reset ? sm[C::oDe + t * S + c] : dt;
                 float acc = 0.f;
 #pragma unroll
                 for (int i = 0; i < NPL; ++i) {
                     const int n = g * NPL + i;
-                    hh[i] = fmaf(ex2_approx(dt * A2[i]), hh[i], du * sm[C::oB + t * NP + n]);
+                    hh[i] = fmaf(ex2_approx(de * A2[i]), hh[i], du * sm[C::oB + t * NP + n]);
                     acc = fmaf(sm[C::oC + t * NP + n], hh[i], acc);
                 }
 #pragma unroll
@@ -411,6 +429,7 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
         for (int t = T - 1; t >= 0; --t) {
             const int s = t * S + c;
             const float dy = sm[C::oDy + s], dt = sm[C::oDt + s], u = sm[C::oU + s];
+            const float de = has_reset ? sm[C::oDe + s] : dt;  // Abar = 0 at a document start
             float hp[NPL];
 #pragma unroll
             for (int q = 0; q < NQ; ++q) {
@@ -427,7 +446,7 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
             for (int i = 0; i < NPL; ++i) {
                 const int n = g * NPL + i;
                 const float Bn = sm[C::oB + t * NP + n], Cn = sm[C::oC + t * NP + n];
-                const float ab = ex2_approx(dt * A2[i]);
+                const float ab = ex2_approx(de * A2[i]);
                 const float gn = fmaf(dy, Cn, gc[i]);
                 const float w = gn * (ab * hp[i]);
                 gv[i] = gn;
@@ -481,6 +500,12 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
         }
         return;
     }
+    // the adjoint carried out of step 0 is the gradient of h0
+    if (EX && a.dh0 && seg == 0 && chain_ok) {
+#pragma unroll
+        for (int i = 0; i < NPL; ++i)
+            if (g * NPL + i < N) a.dh0[chain * N + g * NPL + i] = gc[i];
+    }
     // dA_log = dA * A (A = -exp(A_log)); dD and the bias gradient per chain
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
@@ -506,19 +531,19 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
 //   adjoint: Abar g entering s from the right is a(s + 1) + P(s + 1) times the
 //            value entering s + 1, a(s) the zero-start adjoint leaving s to the
 //            left, zero for the last segment (gseg becomes the entering values).
-__global__ void __launch_bounds__(256) bwd_carry_kernel(const float* A_log, float* hseg,
-                                                        float* gseg, const float* sdt,
-                                                        int64_t chains, int64_t dim, int N,
-                                                        int nseg) {
+__global__ void __launch_bounds__(256) bwd_carry_kernel(const float* A_log, const float* h0,
+                                                        float* hseg, float* gseg,
+                                                        const float* sdt, int64_t chains,
+                                                        int64_t dim, int N, int nseg) {
     const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= chains * N) return;
     const int64_t chain = i / N;
     const int n = int(i % N);
-    const float A2 = -expf(__ldg(A_log + (chain % dim) * N + n)) * kLog2e;
+    const float A2 = fminf(-expf(__ldg(A_log + (chain % dim) * N + n)) * kLog2e, -1e-30f);
     float* hs = hseg + chain * nseg * N + n;
     float* gs = gseg + chain * nseg * N + n;
     const float* sd = sdt + chain * nseg;
-    float H = 0.f;
+    float H = h0 ? h0[i] : 0.f;  // the state entering segment 0
     for (int s = 0; s < nseg; ++s) {
         const float e = hs[int64_t(s) * N];
         hs[int64_t(s) * N] = H;
@@ -532,8 +557,8 @@ __global__ void __launch_bounds__(256) bwd_carry_kernel(const float* A_log, floa
     }
 }
 
-template <typename io_t, int NPL, int G, int UA = 2>
-cudaError_t launch_bwd(const BwdArgs& a0, bool vec_red, cudaStream_t stream) {
+template <typename io_t, int NPL, int G, int UA, bool EX>
+cudaError_t launch_bwd_impl(const BwdArgs& a0, bool vec_red, cudaStream_t stream) {
     using C = BwdCfg<io_t, NPL, G>;
     const int64_t dblocks = (a0.f.dim + C::CH - 1) / C::CH;
     const int64_t ctas = dblocks * a0.f.batch;
@@ -575,25 +600,25 @@ cudaError_t launch_bwd(const BwdArgs& a0, bool vec_red, cudaStream_t stream) {
         a.hseg = static_cast<float*>(seg_mem);
         a.gseg = a.hseg + nst;
         a.sdt = a.gseg + nst;
-        err = cudaFuncSetAttribute(scan_bwd_kernel<io_t, NPL, G, UA, kBwdSummary>,
+        err = cudaFuncSetAttribute(scan_bwd_kernel<io_t, NPL, G, UA, kBwdSummary, EX>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmem));
         if (err == cudaSuccess) {
-            scan_bwd_kernel<io_t, NPL, G, UA, kBwdSummary>
+            scan_bwd_kernel<io_t, NPL, G, UA, kBwdSummary, EX>
                 <<<unsigned(ctas * nseg), C::NTH, C::kSmem, stream>>>(a, int(dblocks), vec_red);
             err = cudaGetLastError();
         }
         if (err == cudaSuccess) {
             const int64_t n = chains * a.f.dstate;
             bwd_carry_kernel<<<unsigned((n + 255) / 256), 256, 0, stream>>>(
-                a.f.A_log, a.hseg, a.gseg, a.sdt, chains, a.f.dim, a.f.dstate, a.nseg);
+                a.f.A_log, a.f.h0, a.hseg, a.gseg, a.sdt, chains, a.f.dim, a.f.dstate, a.nseg);
             err = cudaGetLastError();
         }
     }
     if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(scan_bwd_kernel<io_t, NPL, G, UA, kBwdFull>,
+        err = cudaFuncSetAttribute(scan_bwd_kernel<io_t, NPL, G, UA, kBwdFull, EX>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmem));
     if (err == cudaSuccess) {
-        scan_bwd_kernel<io_t, NPL, G, UA, kBwdFull>
+        scan_bwd_kernel<io_t, NPL, G, UA, kBwdFull, EX>
             <<<unsigned(ctas * nseg), C::NTH, C::kSmem, stream>>>(a, int(dblocks), vec_red);
         err = cudaGetLastError();
     }
@@ -602,6 +627,14 @@ cudaError_t launch_bwd(const BwdArgs& a0, bool vec_red, cudaStream_t stream) {
         if (err == cudaSuccess) err = ferr;
     }
     return err;
+}
+
+// The plain backward, or (h0, resets or dh0 given) the extended one.
+template <typename io_t, int NPL, int G, int UA = 2>
+cudaError_t launch_bwd(const BwdArgs& a, bool vec_red, cudaStream_t stream) {
+    if (a.f.h0 || a.f.reset || a.dh0)
+        return launch_bwd_impl<io_t, NPL, G, UA, true>(a, vec_red, stream);
+    return launch_bwd_impl<io_t, NPL, G, UA, false>(a, vec_red, stream);
 }
 
 // Tile by dstate: NPL states per lane, G lanes per chain (G * NPL >= N).
@@ -647,7 +680,11 @@ cudaError_t launch_scan_bwd(const ScanBwdArgs& s, bool bf16, cudaStream_t stream
     if (s.ddelta_bias && s.f.dim &&
         (err = cudaMemsetAsync(s.ddelta_bias, 0, size_t(s.f.dim) * 4, stream)) != cudaSuccess)
         return err;
-    if (chains == 0 || nchunks == 0) return cudaSuccess;
+    if (chains == 0 || nchunks == 0) {  // nothing depends on h0
+        if (s.dh0 && chains > 0)
+            err = cudaMemsetAsync(s.dh0, 0, size_t(chains) * s.f.dstate * sizeof(float), stream);
+        return err;
+    }
     // checkpoints: the state at the start of every chunk, stream-ordered scratch
     void* ck = nullptr;
     const size_t ckb = size_t(chains) * nchunks * s.f.dstate * sizeof(float);

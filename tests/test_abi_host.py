@@ -249,3 +249,19 @@ def test_complex_scan_entry_validation(lib):
     assert cx(u=Q[0] + 1) == 4 and cx(last_state=Q[10] + 4) == 4    # state needs 8 bytes
     assert cx(y=Q[0]) == 8 and cx(last_state=Q[4] + 64) == 8         # y over u, state in B
     assert cx(dim=0) == 0 and cx(batch=0) == 0
+
+
+def test_bwd_ex_entry_validation(lib):
+    """mamba_selective_scan_bwd_ex validates like mamba_selective_scan_bwd and
+    adds h0 / dh0 alignment and the aliasing of h0, the reset mask and dh0."""
+    kw = {**BGOOD, "h0": Q[17], "reset": Q[18], "dh0": Q[19]}
+    bx = lambda **o: abi.raw_scan_bwd_ex(**{**kw, **o})
+    for over in (dict(u=None), dict(dz=None), dict(dstate=0), dict(io_dtype=4),
+                 dict(du=Q[9] + 1), dict(du=Q[0]), dict(dC=Q[13] + 256), dict(dim=0)):
+        plain = {k: v for k, v in {**BGOOD, **over}.items()}
+        assert bx(**over) == abi.raw_scan_bwd(**plain), over
+    assert bx(h0=Q[17] + 2) == 4 and bx(dh0=Q[19] + 2) == 4      # MAMBA_ERR_ALIGN
+    assert bx(dh0=Q[17]) == 8                                    # dh0 over h0
+    assert bx(dh0=Q[12]) == 8                                    # dh0 over dA_log
+    assert bx(du=Q[18]) == 8                                     # du over the reset mask
+    assert bx(dim=0, h0=None, reset=None, dh0=None) == 0

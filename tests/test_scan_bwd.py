@@ -260,3 +260,77 @@ def test_eight_state_tiles_for_wide_states(cuda, monkeypatch, N, io):
     x = workloads.make_scan_inputs(2, 11, 150, N, io, seed=21 + N, d_mode="normal")
     dout = _dout(x, 21)
     _assert_grads(x, _gpu_bwd(x, dout, cuda), _oracle_bwd(x, dout), what=f"N={N} tile 3")
+
+
+def _bwd_ex(x, dout, device, h0, reset, **kw):
+    xd = to_device(x, device)
+    g = abi.mamba_selective_scan_bwd(xd["u"], xd["delta"], xd["A_log"], xd["B"], xd["C"],
+                                     dout.to(device), D=xd["D"], z=xd["z"],
+                                     delta_bias=xd["delta_bias"], softplus=xd["softplus"],
+                                     h0=None if h0 is None else h0.to(device),
+                                     reset=None if reset is None else reset.to(device), **kw)
+    torch.cuda.synchronize()
+    return {k: v.float().cpu().numpy() for k, v in g.items()}
+
+
+def _oracle_bwd_ex(x, dout, h0, reset):
+    f = workloads.to_f64
+    return oracle.selective_scan_bwd(f(x["u"]), f(x["delta"]), f(x["A_log"]), f(x["B"]),
+                                     f(x["C"]), f(dout), D=f(x["D"]), z=f(x["z"]),
+                                     delta_bias=f(x["delta_bias"]), softplus=x["softplus"],
+                                     h0=f(h0), reset=None if reset is None else reset.numpy())
+
+
+def _doc_starts(batch, L, every, offset):
+    r = torch.zeros((batch, L), dtype=torch.uint8)
+    for b in range(batch):
+        r[b, (offset + 29 * b) % every::every] = 1
+    return r
+
+
+@pytest.mark.parametrize("batch,dim,L,N,io", [(2, 37, 201, 16, "f32"), (2, 37, 201, 16, "bf16"),
+                                              (1, 6, 130, 3, "f32"), (1, 5, 100, 64, "f32"),
+                                              (2, 20, 64, 16, "f32")],
+                         ids=lambda v: str(v))
+def test_h0_and_document_resets_match_oracle(cuda, batch, dim, L, N, io):
+    """The backward of the scan from h0 with document boundaries (every 37
+    tokens, offset per row; the last case also at step 0, which must zero
+    that row's dh0) against the oracle, dh0 included."""
+    x = workloads.make_scan_inputs(batch, dim, L, N, io, seed=23 + L, d_mode="normal")
+    dout = _dout(x, 23)
+    h0 = torch.randn((batch, dim, N), generator=torch.Generator().manual_seed(24))
+    reset = _doc_starts(batch, L, 37, 5)
+    if L == 64:
+        reset[0, 0] = 1
+    g = _bwd_ex(x, dout, cuda, h0, reset)
+    _assert_grads(x, g, _oracle_bwd_ex(x, dout, h0, reset), what=str((batch, dim, L, N, io)))
+    if L == 64:
+        assert not np.any(g["dh0"][0])
+
+
+@pytest.mark.parametrize("segments", ["3", "7"])
+def test_h0_and_resets_with_a_time_split(cuda, monkeypatch, segments):
+    """Forced segments with h0 and document starts, one of them on a segment
+    boundary (step 336 starts the second of 3 segments of 21 chunks)."""
+    monkeypatch.setenv("MAMBA_BWD_SEGMENTS", segments)
+    x = workloads.make_scan_inputs(1, 5, 1000, 16, "f32", seed=25, d_mode="normal")
+    dout = _dout(x, 25)
+    h0 = torch.randn((1, 5, 16), generator=torch.Generator().manual_seed(26))
+    reset = _doc_starts(1, 1000, 97, 11)
+    reset[0, 336] = 1
+    g = _bwd_ex(x, dout, cuda, h0, reset)
+    _assert_grads(x, g, _oracle_bwd_ex(x, dout, h0, reset), what=f"{segments} segments")
+
+
+def test_ex_without_h0_or_resets_is_the_plain_backward(cuda):
+    """No h0 and no resets: the per-element gradients equal the plain
+    backward's bit for bit, and dh0 is the gradient of a zero start."""
+    x = workloads.make_scan_inputs(2, 40, 300, 16, "bf16", seed=27, d_mode="normal")
+    dout = _dout(x, 27)
+    g_plain = _gpu_bwd(x, dout, cuda)
+    g_ex = _bwd_ex(x, dout, cuda, None, None, want_dh0=True)
+    for k in PER_ELEMENT:
+        assert np.array_equal(g_plain[k], g_ex[k]), k
+    zero = torch.zeros((2, 40, 16))
+    gr = _oracle_bwd_ex(x, dout, zero, None)
+    assert rel_err(g_ex["dh0"], gr["dh0"]) <= GTOL["bf16"]
