@@ -97,7 +97,7 @@ def launches_per_step(cfg, sms: int) -> int:
 # kernel sources behind each stored ncu summary (profiles/<prefix>_<workload>.md)
 PROFILED_SOURCES = {
     "scan_fwd": ("scan_fwd.cu", "common.cuh"),
-    "scan_bwd": ("scan_bwd.cu", "common.cuh"),
+    "scan_bwd": ("scan_bwd.cu", "scan_bwd.cuh", "common.cuh"),
     "conv1d": ("conv1d.cu", "common.cuh"),
     "scan_complex": ("scan_complex.cu", "common.cuh"),
     "state_update": ("state_update.cu", "common.cuh"),

@@ -5,6 +5,7 @@
 #include "../../include/mamba_scan.h"
 #include "../../include/mamba_scan_testing.h"
 #include "common.cuh"
+#include "scan_bwd.cuh"
 
 namespace {
 
@@ -267,9 +268,8 @@ int mamba_selective_scan_bwd_ex(const void* u, const void* delta, const float* A
     a.dC = dC;
     a.dD = dD;
     a.ddelta_bias = ddelta_bias;
-    a.dh0 = dh0;
-    const cudaError_t err =
-        mamba::launch_scan_bwd(a, io_dtype == MAMBA_BF16, reinterpret_cast<cudaStream_t>(stream));
+    const cudaError_t err = mamba::launch_scan_bwd_ex(a, dh0, io_dtype == MAMBA_BF16,
+                                                      reinterpret_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
 }
 

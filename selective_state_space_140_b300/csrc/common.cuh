@@ -240,7 +240,7 @@ struct StateUpdateArgs {
 
 // Arguments of the backward scan (gradients for dout = dLoss/dy).
 struct ScanBwdArgs {
-    ScanArgs f;          // the forward's inputs, h0 and reset included (y, last_state unused)
+    ScanArgs f;          // the forward's inputs (y, last_state unused; h0, reset read by the _ex form only)
     const void* dout;    // [batch, dim, L] io
     void* du;            // [batch, dim, L] io
     void* ddelta;        // [batch, dim, L] io
@@ -250,7 +250,6 @@ struct ScanBwdArgs {
     float* dC;           // [batch, L, N]
     float* dD;           // [dim] or nullptr
     float* ddelta_bias;  // [dim] or nullptr
-    float* dh0 = nullptr;  // [batch, dim, N] or nullptr: gradient of f.h0 (the state before step 0)
 };
 
 // Launchers (return the cudaError_t of the launch).

@@ -38,7 +38,7 @@
 // over the whole sequence and are added once at the end.
 #include <cstdlib>
 
-#include "common.cuh"
+#include "scan_bwd.cuh"
 
 namespace mamba {
 namespace {
@@ -78,6 +78,7 @@ struct BwdCfg {
 
 struct BwdArgs : ScanBwdArgs {
     float* ckpt;  // [batch * dim][nchunks][N] scratch: state at each chunk start
+    float* dh0 = nullptr;  // [batch * dim][N] or nullptr: gradient of f.h0
     // time split (nseg > 1): segment s covers chunks [s * seg_chunks, (s+1) * seg_chunks)
     int nseg = 1, seg_chunks = 0;
     float* hseg = nullptr;  // [chains][nseg][N]: summary: zero-start end state; main: state entering
@@ -665,6 +666,10 @@ cudaError_t dispatch_bwd(const BwdArgs& a, bool vec_red, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_scan_bwd(const ScanBwdArgs& s, bool bf16, cudaStream_t stream) {
+    return launch_scan_bwd_ex(s, nullptr, bf16, stream);
+}
+
+cudaError_t launch_scan_bwd_ex(const ScanBwdArgs& s, float* dh0, bool bf16, cudaStream_t stream) {
     const int64_t chains = s.f.batch * s.f.dim;
     const int64_t nchunks = (s.f.seqlen + kBT - 1) / kBT;
     cudaError_t err = cudaSuccess;
@@ -681,8 +686,8 @@ cudaError_t launch_scan_bwd(const ScanBwdArgs& s, bool bf16, cudaStream_t stream
         (err = cudaMemsetAsync(s.ddelta_bias, 0, size_t(s.f.dim) * 4, stream)) != cudaSuccess)
         return err;
     if (chains == 0 || nchunks == 0) {  // nothing depends on h0
-        if (s.dh0 && chains > 0)
-            err = cudaMemsetAsync(s.dh0, 0, size_t(chains) * s.f.dstate * sizeof(float), stream);
+        if (dh0 && chains > 0)
+            err = cudaMemsetAsync(dh0, 0, size_t(chains) * s.f.dstate * sizeof(float), stream);
         return err;
     }
     // checkpoints: the state at the start of every chunk, stream-ordered scratch
@@ -692,6 +697,7 @@ cudaError_t launch_scan_bwd(const ScanBwdArgs& s, bool bf16, cudaStream_t stream
     BwdArgs a;
     static_cast<ScanBwdArgs&>(a) = s;
     a.ckpt = static_cast<float*>(ck);
+    a.dh0 = dh0;
     // 16-byte atomics on dB / dC need rows of whole float4 and aligned bases
     const bool vec_red = s.f.dstate % 4 == 0 && (reinterpret_cast<uintptr_t>(s.dB) & 15) == 0 &&
                          (reinterpret_cast<uintptr_t>(s.dC) & 15) == 0;
