@@ -111,6 +111,51 @@ def test_results_are_deterministic(cuda):
     assert np.array_equal(y1, y2) and np.array_equal(h1, h2)
 
 
+def test_output_is_linear_in_u(cuda):
+    """With dt, B, C and z held fixed, the recurrence and the gated output are
+    linear in u: scanning al*u1 + be*u2 gives al*y1 + be*y2 and the same
+    combination of the final states.  Each of the three fp32 runs sits well
+    inside the 1e-4 parity bound of its exact result, so the residual is at
+    most (1 + |al| + |be|) times that; 1e-3 leaves room while any place where
+    u enters non-linearly (the step size, the gate) gives errors of order one."""
+    x1 = workloads.make_scan_inputs(2, 19, 300, 16, "f32", seed=18, d_mode="normal")
+    u2 = workloads.make_scan_inputs(2, 19, 300, 16, "f32", seed=19)["u"]
+    al, be = 0.75, -1.25
+    y1, h1 = _run(x1, cuda)
+    y2, h2 = _run(dict(x1, u=u2), cuda)
+    y3, h3 = _run(dict(x1, u=al * x1["u"] + be * u2), cuda)
+    assert rel_err(y3, al * y1 + be * y2) <= 1e-3
+    assert rel_err(h3, al * h1 + be * h2) <= 1e-3
+
+
+def test_permuting_channels_and_batches_permutes_the_outputs(cuda):
+    """Chains are independent: permuting channels (u, dt, z with their A_log
+    rows, D and bias) and batches (with their B, C) permutes y and the final
+    state the same way.  A_log gets a per-channel offset so that a row taken
+    from the wrong channel shows.  Every chain goes through the same
+    arithmetic wherever it sits in the grid, so the bound is a tenth of the
+    fp32 parity bound."""
+    x = workloads.make_scan_inputs(3, 45, 257, 16, "f32", seed=20, d_mode="normal")
+    g = torch.Generator().manual_seed(20)
+    x["A_log"] = (x["A_log"] + 0.5 * torch.rand(45, 1, generator=g)).contiguous()
+    yg, hg = _run(x, cuda)
+    p = torch.randperm(45, generator=g)
+    q = torch.tensor([2, 0, 1])
+    xp = dict(x)
+    for k in ("u", "delta", "z"):
+        xp[k] = x[k][q][:, p].contiguous()
+    for k in ("B", "C"):
+        xp[k] = x[k][q].contiguous()
+    for k in ("A_log", "D", "delta_bias"):
+        xp[k] = x[k][p].contiguous()
+    yp, hp = _run(xp, cuda)
+    pn, qn = p.numpy(), q.numpy()
+    assert rel_err(yp, yg[qn][:, pn]) <= 1e-5
+    assert rel_err(hp, hg[qn][:, pn]) <= 1e-5
+    yr, hr = oracle_scan(xp)
+    _assert_close(xp, yp, hp, yr, hr, what="permuted")
+
+
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 def test_element_aligned_buffers_give_the_same_result(cuda, io):
     """Inputs that start one element past a 16-byte boundary take the scalar
