@@ -153,3 +153,26 @@ def test_full_size_layer_with_state_and_boundaries_on_sampled_chains(cuda):
         hs.append(hr[0, 0])
     ey, eh = rel_err(yg, np.stack(ys)), rel_err(hg, np.stack(hs))
     assert ey <= TOL["bf16"] and eh <= TOL["bf16"], f"y {ey:.3e} state {eh:.3e}"
+
+
+def test_beyond_a_million_tokens_in_one_launch_and_in_blocks(cuda):
+    """2^20 + 4104 tokens on 4 channels (N 16, fp32, two document boundaries):
+    one launch, which the planner splits along time into about a thousand
+    segments, and the same sequence streamed as three blocks through h0 into
+    the same state buffer, both match the oracle element by element."""
+    batch, dim, L, N = 1, 4, (1 << 20) + 4104, 16
+    x = workloads.make_scan_inputs(batch, dim, L, N, "f32", seed=68, d_mode="normal")
+    reset = _mask(batch, L, 69, density=0.0, extra=[(0, 300001), (0, 777777)])
+    yr, hr = _oracle(x, None, reset)
+    xd = to_device(x, cuda)
+    rd = torch.from_numpy(reset).to(cuda)
+    y, h = _gpu(xd, reset=rd)
+    _check(x, y, h, yr, hr, "one launch")
+    state = torch.zeros((batch, dim, N), device=cuda)
+    ys = []
+    for t0, t1 in ((0, 400000), (400000, 800000), (800000, L)):
+        blk = {k: (v[..., t0:t1].contiguous() if k in ("u", "delta", "z") else
+                   v[:, t0:t1].contiguous() if k in ("B", "C") else v) for k, v in xd.items()}
+        yb, _ = _gpu(blk, h0=state, reset=rd[:, t0:t1].contiguous(), last_state=state)
+        ys.append(yb)
+    _check(x, torch.cat(ys, dim=-1), state, yr, hr, "three streamed blocks")
