@@ -37,6 +37,21 @@ MUTANTS = [
     ("initial_state_ignored", "h[n] = j->h0 ? j->h0[chain * N + n] : 0.0;", "h[n] = 0.0;"),
     ("decode_without_dt", "*h = abar * *h + step * B[b * N + n] * x[e];", "*h = abar * *h + B[b * N + n] * x[e];"),
     ("decode_no_gate", "out[e] = z ? yt * oracle_silu(z[e]) : yt;", "out[e] = yt;"),
+    ("decode_state_not_decayed", "*h = abar * *h + step * B[b * N + n] * x[e];",
+     "*h = *h + step * B[b * N + n] * x[e];"),
+    ("decode_C_is_B", "acc += C[b * N + n] * *h;", "acc += B[b * N + n] * *h;"),
+    ("decode_skip_dropped", "const double yt = acc + (D ? D[d] : 0.0) * x[e];",
+     "const double yt = acc;"),
+    ("decode_bias_ignored", "const double raw = dt[e] + (dt_bias ? dt_bias[d] : 0.0);",
+     "const double raw = dt[e];"),
+    ("softplus_negative_branch_wrong", "return log1p(exp(x));", "return exp(x);"),
+    ("dt_reads_first_step", "const double raw = dl[t] + bias;", "const double raw = dl[0] + bias;"),
+    ("D_ignores_channel", "const double Dd = j->D ? j->D[d] : 0.0;",
+     "const double Dd = j->D ? j->D[0] : 0.0;"),
+    ("bias_ignores_channel", "const double bias = j->delta_bias ? j->delta_bias[d] : 0.0;",
+     "const double bias = j->delta_bias ? j->delta_bias[0] : 0.0;"),
+    ("threads_skip_their_last_chain", "jobs[i].chain_end = chains * (i + 1) / nthreads;",
+     "jobs[i].chain_end = chains * (i + 1) / nthreads - (chains > nthreads);"),
     ("reset_ignored", "if (rs && rs[t])", "if (0)"),
     ("reset_after_the_flagged_step", "if (rs && rs[t])", "if (rs && t > 0 && rs[t - 1])"),
     ("reset_one_step_early", "if (rs && rs[t])", "if (rs && t + 1 < L && rs[t + 1])"),
@@ -56,6 +71,13 @@ MUTANTS = [
     ("bwd_ddt_without_input_term", "ddt += gn * (A[n] * a * hp + uc[t] * Bb[t * N + n]);",
      "ddt += gn * (A[n] * a * hp);"),
     ("bwd_du_without_skip", "double dut = dy * Dd, ddt = 0.0;", "double dut = 0.0, ddt = 0.0;"),
+    ("bwd_du_input_term_without_dt", "dut += gn * dt * Bb[t * N + n];", "dut += gn * Bb[t * N + n];"),
+    ("bwd_dD_ignores_gate", "if (dD) dD[d] += dy * uc[t];", "if (dD) dD[d] += go[t] * uc[t];"),
+    ("bwd_gate_factor_is_sigmoid", "dy = go[t] * zz[t] * s;", "dy = go[t] * s;"),
+    ("bwd_adjoint_drops_later_steps", "const double gn = dy * Cb[t * N + n] + g[n];",
+     "const double gn = dy * Cb[t * N + n];"),
+    ("bwd_bias_gradient_before_softplus", "if (ddelta_bias) ddelta_bias[d] += dr;",
+     "if (ddelta_bias) ddelta_bias[d] += ddt;"),
     ("bwd_reset_ignored", "const double a = (rsb && rsb[t]) ? 0.0 : exp(dt * A[n]);",
      "const double a = exp(dt * A[n]);"),
     ("bwd_reset_one_step_late", "const double a = (rsb && rsb[t]) ? 0.0 : exp(dt * A[n]);",
