@@ -114,6 +114,22 @@ MUTANTS = [
      "h[n] = cexp(dt * A[n]) * h[n] + Bn * ut;"),
     ("complex_state_written_conjugated", "last_state[(chain * N + n) * 2 + 1] = cimag(h[n]);",
      "last_state[(chain * N + n) * 2 + 1] = -cimag(h[n]);"),
+    ("complex_real_part_of_A_is_minus_A_log",
+     "A[n] = -exp(A_log_re[d * N + n]) + I * A_im[d * N + n];",
+     "A[n] = -A_log_re[d * N + n] + I * A_im[d * N + n];"),
+    ("complex_output_reads_state_before_update",
+     "h[n] = cexp(dt * A[n]) * h[n] + dt * Bn * ut;\n                    acc += Cn * h[n];",
+     "acc += Cn * h[n];\n                    h[n] = cexp(dt * A[n]) * h[n] + dt * Bn * ut;"),
+    ("complex_gate_dropped", "y[chain * L + t] = z ? yt * oracle_silu(z[chain * L + t]) : yt;",
+     "y[chain * L + t] = yt;"),
+    ("complex_bias_ignored",
+     "const double raw = delta[chain * L + t] + (delta_bias ? delta_bias[d] : 0.0);",
+     "const double raw = delta[chain * L + t];"),
+    ("conv_state_ignores_batch",
+     "const double *st = init_state ? init_state + row * (width - 1) : NULL;",
+     "const double *st = init_state ? init_state + d * (width - 1) : NULL;"),
+    ("conv_activation_always_on", "out[row * seqlen + t] = silu_flag ? oracle_silu(pre) : pre;",
+     "out[row * seqlen + t] = oracle_silu(pre);"),
 ]
 
 
