@@ -223,8 +223,11 @@ int mamba_selective_scan_bwd(const void *u, const void *delta, const float *A_lo
  * starting state h0 and with document boundaries (codechina.net overview,
  * section 3.2 point 2: resetting the hidden state isolates documents; the
  * same page's deployment notes on block-by-block processing of long
- * sequences).  Training on packed documents, or on one long sequence cut into
- * blocks, needs these gradients.
+ * sequences).  Training on packed documents needs these gradients, and dh0
+ * is the gradient a preceding block's final state receives.  This call takes
+ * no gradient for last_state (the loss is a function of y alone), so it
+ * gives the gradients of the last block of a chain, or of blocks whose final
+ * state feeds nothing that is differentiated.
  *
  *   h0    : [batch, dim, dstate] fp32 or NULL (zero start), as for the forward
  *   reset : [batch, seqlen] bytes or NULL; non-zero at a token that starts a

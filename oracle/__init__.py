@@ -57,7 +57,7 @@ def _declare(lib):
     lib.oracle_selective_scan_bwd_ex_f64.restype = ctypes.c_int
     lib.oracle_selective_scan_bwd_ex_f64.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int,
                                                      dp, ctypes.c_void_p, dp, dp, dp, dp, dp, dp,
-                                                     dp, dp, dp, dp, i64, i64, i64, i64]
+                                                     dp, dp, dp, dp, dp, i64, i64, i64, i64]
     lib.oracle_causal_conv1d_f64.restype = ctypes.c_int
     lib.oracle_causal_conv1d_f64.argtypes = [dp, dp, dp, dp, ctypes.c_int, dp, dp,
                                              i64, i64, i64, i64]
@@ -137,19 +137,22 @@ def selective_scan(u, delta, A_log, B, C, D=None, z=None, delta_bias=None, softp
 
 
 def selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_bias=None,
-                       softplus=True, h0=None, reset=None, lib=None):
+                       softplus=True, h0=None, reset=None, dlast_state=None, lib=None):
     """Gradients of the scan for the output gradient ``dout`` [batch, dim, L].
     Returns a dict with du, ddelta, dA_log, dB, dC and, when the matching input
     is given, dD, dz, ddelta_bias and dh0 (float64 arrays in the layouts of the
     inputs).  ``h0`` [batch, dim, N] is the state before step 0 (zero if None);
-    ``reset`` [batch, L] marks document starts as in :func:`selective_scan`."""
+    ``reset`` [batch, L] marks document starts as in :func:`selective_scan`;
+    ``dlast_state`` [batch, dim, N] is the loss's gradient on the final state
+    (none if None)."""
     lib = lib or load()
     u, delta, A_log, B, C, dout = map(_f64, (u, delta, A_log, B, C, dout))
-    D, z, delta_bias, h0 = map(_f64, (D, z, delta_bias, h0))
+    D, z, delta_bias, h0, dlast_state = map(_f64, (D, z, delta_bias, h0, dlast_state))
     batch, dim, L = u.shape
     N = A_log.shape[1]
     assert dout.shape == u.shape and B.shape == (batch, L, N) and C.shape == (batch, L, N)
     assert h0 is None or h0.shape == (batch, dim, N)
+    assert dlast_state is None or dlast_state.shape == (batch, dim, N)
     if reset is not None:
         reset = np.ascontiguousarray(np.asarray(reset) != 0, dtype=np.uint8)
         assert reset.shape == (batch, L)
@@ -158,7 +161,7 @@ def selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_bias=N
     g["dA_log"] = np.zeros((dim, N))
     g["dD"], g["ddelta_bias"] = np.zeros(dim), np.zeros(dim)
     g["dh0"] = np.zeros((batch, dim, N))
-    if h0 is None and reset is None:
+    if h0 is None and reset is None and dlast_state is None:
         rc = lib.oracle_selective_scan_bwd_f64(
             _ptr(u), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
             _ptr(delta_bias), int(bool(softplus)), _ptr(dout), _ptr(g["du"]), _ptr(g["ddelta"]),
@@ -168,7 +171,8 @@ def selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_bias=N
         rc = lib.oracle_selective_scan_bwd_ex_f64(
             _ptr(u), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
             _ptr(delta_bias), int(bool(softplus)), _ptr(h0),
-            None if reset is None else reset.ctypes.data, _ptr(dout), _ptr(g["du"]),
+            None if reset is None else reset.ctypes.data, _ptr(dout), _ptr(dlast_state),
+            _ptr(g["du"]),
             _ptr(g["ddelta"]), _ptr(g["dA_log"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),
             _ptr(g["dz"] if z is not None else None), _ptr(g["ddelta_bias"]), _ptr(g["dh0"]),
             batch, dim, L, N)

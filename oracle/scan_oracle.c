@@ -206,10 +206,11 @@ int oracle_selective_scan_f64(const double *u, const double *delta, const double
 static int scan_bwd_impl(const double *u, const double *delta, const double *A_log,
                          const double *B, const double *C, const double *D, const double *z,
                          const double *delta_bias, int softplus_flag, const double *h0,
-                         const unsigned char *reset, const double *dout, double *du,
-                         double *ddelta, double *dA_log, double *dB, double *dC, double *dD,
-                         double *dz, double *ddelta_bias, double *dh0, int64_t batch,
-                         int64_t dim, int64_t seqlen, int64_t dstate) {
+                         const unsigned char *reset, const double *dout,
+                         const double *dlast, double *du, double *ddelta, double *dA_log,
+                         double *dB, double *dC, double *dD, double *dz, double *ddelta_bias,
+                         double *dh0, int64_t batch, int64_t dim, int64_t seqlen,
+                         int64_t dstate) {
     if (!u || !delta || !A_log || !B || !C || !dout || !du || !ddelta || !dA_log || !dB || !dC)
         return -1;
     if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 0) return -2;
@@ -257,7 +258,9 @@ static int scan_bwd_impl(const double *u, const double *delta, const double *A_l
                 ys[t] = acc + Dd * uc[t];
             }
             /* reverse */
-            for (int64_t n = 0; n < N; ++n) g[n] = 0.0; /* Abar_{t+1} g_{t+1}, none after L-1 */
+            /* g = what reaches the state after step t from later on: Abar_{t+1} g_{t+1};
+             * after the last step, the loss's own gradient on the final state (if any) */
+            for (int64_t n = 0; n < N; ++n) g[n] = dlast ? dlast[chain * N + n] : 0.0;
             for (int64_t t = L - 1; t >= 0; --t) {
                 double dy = go[t];
                 if (zz) {
@@ -304,25 +307,28 @@ int oracle_selective_scan_bwd_f64(const double *u, const double *delta, const do
                                   double *dz, double *ddelta_bias, int64_t batch, int64_t dim,
                                   int64_t seqlen, int64_t dstate) {
     return scan_bwd_impl(u, delta, A_log, B, C, D, z, delta_bias, softplus_flag, NULL, NULL,
-                         dout, du, ddelta, dA_log, dB, dC, dD, dz, ddelta_bias, NULL, batch,
-                         dim, seqlen, dstate);
+                         dout, NULL, du, ddelta, dA_log, dB, dC, dD, dz, ddelta_bias, NULL,
+                         batch, dim, seqlen, dstate);
 }
 
 /* The backward of oracle_selective_scan_f64 with h0 and document resets
  * (codechina.net overview, section 3.2 point 2 and the deployment notes on
- * block-by-block processing); dh0 receives the gradient of h0. */
+ * block-by-block processing); dh0 receives the gradient of h0.  dlast
+ * [batch][dim][dstate] (optional) is the loss's gradient on last_state: a
+ * sequence cut into blocks is trained by passing one block's dh0 as the
+ * preceding block's dlast (its last_state is the next block's h0). */
 int oracle_selective_scan_bwd_ex_f64(const double *u, const double *delta, const double *A_log,
                                      const double *B, const double *C, const double *D,
                                      const double *z, const double *delta_bias,
                                      int softplus_flag, const double *h0,
-                                     const unsigned char *reset, const double *dout, double *du,
-                                     double *ddelta, double *dA_log, double *dB, double *dC,
-                                     double *dD, double *dz, double *ddelta_bias, double *dh0,
-                                     int64_t batch, int64_t dim, int64_t seqlen,
-                                     int64_t dstate) {
+                                     const unsigned char *reset, const double *dout,
+                                     const double *dlast, double *du, double *ddelta,
+                                     double *dA_log, double *dB, double *dC, double *dD,
+                                     double *dz, double *ddelta_bias, double *dh0, int64_t batch,
+                                     int64_t dim, int64_t seqlen, int64_t dstate) {
     return scan_bwd_impl(u, delta, A_log, B, C, D, z, delta_bias, softplus_flag, h0, reset,
-                         dout, du, ddelta, dA_log, dB, dC, dD, dz, ddelta_bias, dh0, batch, dim,
-                         seqlen, dstate);
+                         dout, dlast, du, ddelta, dA_log, dB, dC, dD, dz, ddelta_bias, dh0,
+                         batch, dim, seqlen, dstate);
 }
 
 /*

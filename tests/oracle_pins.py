@@ -369,12 +369,13 @@ def check_reset_at_start_ignores_h0(lib):
     _close(h1, h0, rtol=0, what="state after a reset on step 0")
 
 
-def _fd_check(lib, softplus, with_opt, seed, ex=False):
+def _fd_check(lib, softplus, with_opt, seed, ex=False, dlast=False):
     """Central differences of the forward oracle's loss sum(dout * y) with
     respect to every element of every input must equal the gradients of the
     backward oracle (fp64: steps of 1e-6 leave errors near 1e-9).  With
     ``ex`` the scans also start from a random h0 (its gradient checked too)
-    and carry document boundaries (a reset inside each batch row)."""
+    and carry document boundaries (a reset inside each batch row).  With
+    ``dlast`` the loss adds sum(w * last_state), w passed as dlast_state."""
     r = _rng(seed)
     b, d, L, N = 2, 2, 5, 3
     x = dict(u=r.normal(size=(b, d, L)), delta=r.normal(size=(b, d, L)),
@@ -390,17 +391,19 @@ def _fd_check(lib, softplus, with_opt, seed, ex=False):
         reset = np.zeros((b, L), dtype=np.uint8)
         reset[0, 2] = reset[1, 3] = 1
     dout = r.normal(size=(b, d, L))
+    w = r.normal(size=(b, d, N)) if dlast else None
 
     def loss(xx):
-        y, _, _ = oracle.selective_scan(xx["u"], xx["delta"], xx["A_log"], xx["B"], xx["C"],
-                                        D=xx.get("D"), z=xx.get("z"),
-                                        delta_bias=xx.get("delta_bias"), softplus=softplus,
-                                        h0=xx.get("h0"), reset=reset, nthreads=1, lib=lib)
-        return float(np.sum(dout * y))
+        y, hl, _ = oracle.selective_scan(xx["u"], xx["delta"], xx["A_log"], xx["B"], xx["C"],
+                                         D=xx.get("D"), z=xx.get("z"),
+                                         delta_bias=xx.get("delta_bias"), softplus=softplus,
+                                         h0=xx.get("h0"), reset=reset, nthreads=1, lib=lib)
+        return float(np.sum(dout * y)) + (float(np.sum(w * hl)) if dlast else 0.0)
 
     g = oracle.selective_scan_bwd(x["u"], x["delta"], x["A_log"], x["B"], x["C"], dout,
                                   D=x.get("D"), z=x.get("z"), delta_bias=x.get("delta_bias"),
-                                  softplus=softplus, h0=x.get("h0"), reset=reset, lib=lib)
+                                  softplus=softplus, h0=x.get("h0"), reset=reset,
+                                  dlast_state=w, lib=lib)
     names = {"u": "du", "delta": "ddelta", "A_log": "dA_log", "B": "dB", "C": "dC", "D": "dD",
              "z": "dz", "delta_bias": "ddelta_bias", "h0": "dh0"}
     eps = 1e-6
@@ -654,6 +657,53 @@ def check_backward_reset_splits_documents(lib):
     _close(whole["dh0"], first["dh0"], rtol=1e-12, what="dh0")
 
 
+def check_backward_final_state_gradient(lib):
+    """A loss on the final state as well as on y (its gradient given as
+    dlast_state): every gradient, dh0 included, against central differences,
+    from a random h0 and across document boundaries."""
+    _fd_check(lib, softplus=True, with_opt=True, seed=18, ex=True, dlast=True)
+
+
+def check_backward_chains_across_blocks(lib):
+    """A sequence cut into two blocks, the second started from the first's
+    final state (block-by-block processing of a long sequence), trained block
+    by block -- the second block's dh0 passed as the first block's gradient on
+    its final state -- gives the gradients of one backward over the whole
+    sequence: per-step gradients concatenated, summed ones added, the same
+    dh0.  A boundary inside each block and a loss on the final state too."""
+    r = _rng(19)
+    b, d, L, N, L1 = 2, 3, 11, 4, 5
+    x = dict(u=r.normal(size=(b, d, L)), delta=r.normal(size=(b, d, L)),
+             A_log=r.normal(size=(d, N)) * 0.5, B=r.normal(size=(b, L, N)),
+             C=r.normal(size=(b, L, N)), dout=r.normal(size=(b, d, L)))
+    kw = dict(D=r.normal(size=d), z=r.normal(size=(b, d, L)), delta_bias=r.normal(size=d))
+    h0, w = r.normal(size=(b, d, N)), r.normal(size=(b, d, N))
+    reset = np.zeros((b, L), dtype=np.uint8)
+    reset[0, 7] = reset[1, 2] = 1
+    whole = oracle.selective_scan_bwd(x["u"], x["delta"], x["A_log"], x["B"], x["C"], x["dout"],
+                                      h0=h0, reset=reset, dlast_state=w, lib=lib, **kw)
+
+    def cut(lo, hi):
+        t = lambda a: a[:, :, lo:hi]
+        return (t(x["u"]), t(x["delta"]), x["A_log"], x["B"][:, lo:hi], x["C"][:, lo:hi]), \
+            dict(kw, z=t(kw["z"])), t(x["dout"]), reset[:, lo:hi]
+
+    a1, k1, g1out, r1 = cut(0, L1)
+    a2, k2, g2out, r2 = cut(L1, L)
+    _, h_mid, _ = oracle.selective_scan(*a1, h0=h0, reset=r1, lib=lib, **k1)
+    second = oracle.selective_scan_bwd(*a2, g2out, h0=h_mid, reset=r2, dlast_state=w, lib=lib,
+                                       **k2)
+    first = oracle.selective_scan_bwd(*a1, g1out, h0=h0, reset=r1,
+                                      dlast_state=second["dh0"], lib=lib, **k1)
+    for k in ("du", "ddelta", "dz"):
+        _close(whole[k], np.concatenate([first[k], second[k]], axis=2), rtol=1e-12, what=k)
+    for k in ("dB", "dC"):
+        _close(whole[k], np.concatenate([first[k], second[k]], axis=1), rtol=1e-12, what=k)
+    for k in ("dA_log", "dD", "ddelta_bias"):
+        _close(whole[k], first[k] + second[k], rtol=1e-12, what=k)
+    _close(whole["dh0"], first["dh0"], rtol=1e-12, what="dh0")
+
+
 def check_backward_reset_at_start_cuts_h0(lib):
     """A reset at step 0 discards h0: its gradient is exactly zero and every
     other gradient equals that of the scan started from zero."""
@@ -691,6 +741,8 @@ ALL_CHECKS = [
     check_backward_finite_differences_h0_reset,
     check_backward_reset_splits_documents,
     check_backward_reset_at_start_cuts_h0,
+    check_backward_final_state_gradient,
+    check_backward_chains_across_blocks,
     check_conv_against_numpy_convolve,
     check_conv_impulse_response,
     check_conv_silu_closed_forms,

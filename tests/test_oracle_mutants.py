@@ -87,6 +87,12 @@ MUTANTS = [
      "                    const double hp = t > 0 ? hs[(t - 1) * N + n] : (hin ? hin[n] : 0.0);",
      "const double gn = dy * Cb[t * N + n] + g[n];\n"
      "                    const double hp = t > 0 ? hs[(t - 1) * N + n] : 0.0;"),
+    ("bwd_final_state_gradient_ignored",
+     "for (int64_t n = 0; n < N; ++n) g[n] = dlast ? dlast[chain * N + n] : 0.0;",
+     "for (int64_t n = 0; n < N; ++n) g[n] = 0.0;"),
+    ("bwd_final_state_gradient_from_first_chain",
+     "for (int64_t n = 0; n < N; ++n) g[n] = dlast ? dlast[chain * N + n] : 0.0;",
+     "for (int64_t n = 0; n < N; ++n) g[n] = dlast ? dlast[n] : 0.0;"),
     ("bwd_dh0_dropped", "dh0[chain * N + n] = g[n];", "dh0[chain * N + n] = 0.0;"),
     ("conv_window_one_step_late", "pre += w[k] * conv_input(xr, st, width, t - (width - 1) + k);",
      "pre += w[k] * conv_input(xr, st, width, t - width + k);"),
