@@ -493,6 +493,10 @@ def run_ours(args, cfg, dcfg, rank, world, local):
     exp_rate = cnt["exps"] / t_step
     t_hbm = cnt["bytes"] / (hbm_peak * 1e9)
     t_sfu = cnt["exps"] / sfu["ex2_per_s"]
+    # diagnostic: the recurrence's FMA-pipe work, 4 fp32 operations per update
+    # (dt*A, du*B, the state FMA, the C*h FMA) issued as 2 packed pairs, at the
+    # micro-benchmarked packed rate; element-side work comes on top
+    t_fma = 2 * cnt["updates"] / sfu["ffma2_per_s"] if sfu.get("ffma2_per_s") else None
     khash = kernel_source_hash()
     traffic = stored_traffic(args.workload, khash)
     roof_hbm = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
@@ -519,7 +523,8 @@ def run_ours(args, cfg, dcfg, rank, world, local):
         "roofline_hbm": roof_hbm,
         "roofline_sfu": roof_sfu,
         "binding_unit": "sfu" if t_sfu >= t_hbm else "hbm",
-        "t_floor_us": {"hbm": round(t_hbm * 1e6, 1), "sfu": round(t_sfu * 1e6, 1)},
+        "t_floor_us": {"hbm": round(t_hbm * 1e6, 1), "sfu": round(t_sfu * 1e6, 1),
+                       "fma_pipe_recurrence": None if t_fma is None else round(t_fma * 1e6, 1)},
         "ubench": {k: (round(v / 1e9, 1) if k.endswith("_per_s") else v) for k, v in sfu.items()},
         "gpu_launches": args.steps * launches_per_step(
             cfg, torch.cuda.get_device_properties(device).multi_processor_count),
