@@ -602,6 +602,40 @@ def check_complex_geometric_series(lib):
     _close(hL[0], want, rtol=1e-12, what="geometric series")
 
 
+def check_complex_bruteforce_unrolled(lib):
+    """Everything time-varying (complex B and C per step, any A_im), tiny
+    sizes: the complex state written as the explicit sum
+    h_t = sum_{s<=t} (prod_{s<r<=t} exp(dt_r A)) dt_s B_s u_s with numpy's
+    complex exp, y_t = (Re sum_n C_tn h_tn + D u_t) * SiLU(z_t)."""
+    r = _rng(54)
+    b, d, L, N = 2, 2, 6, 3
+    u, z, raw = r.normal(size=(b, d, L)), r.normal(size=(b, d, L)), r.normal(size=(b, d, L))
+    A_log, A_im = r.normal(size=(d, N)) * 0.5, r.normal(size=(d, N)) * 3.0
+    B, C = _cplx(r, (b, L, N)), _cplx(r, (b, L, N))
+    D, bias = r.normal(size=d), r.normal(size=d)
+    y, hL = oracle.selective_scan_complex(u, raw, A_log, A_im, B, C, D=D, z=z, delta_bias=bias,
+                                          lib=lib)
+    want_y = np.zeros((b, d, L))
+    want_h = np.zeros((b, d, N), dtype=complex)
+    for bi in range(b):
+        for di in range(d):
+            dt = np.logaddexp(0.0, raw[bi, di] + bias[di])
+            A = -np.exp(A_log[di]) + 1j * A_im[di]
+            for t in range(L):
+                h = np.zeros(N, dtype=complex)
+                for s_ in range(t + 1):
+                    decay = np.ones(N, dtype=complex)
+                    for rr in range(s_ + 1, t + 1):
+                        decay = decay * np.exp(dt[rr] * A)
+                    h = h + decay * dt[s_] * B[bi, s_] * u[bi, di, s_]
+                yt = float(np.sum(C[bi, t] * h).real) + D[di] * u[bi, di, t]
+                want_y[bi, di, t] = yt * z[bi, di, t] * expit(z[bi, di, t])
+                if t == L - 1:
+                    want_h[bi, di] = h
+    _close(hL, want_h, rtol=1e-12, what="complex unrolled final state")
+    _close(y, want_y, rtol=1e-12, what="complex unrolled outputs")
+
+
 def check_complex_conjugation_symmetry(lib):
     """Conjugating A, B and C conjugates every state and leaves the real
     output unchanged."""
@@ -753,4 +787,5 @@ ALL_CHECKS = [
     check_complex_impulse_response_closed_form,
     check_complex_geometric_series,
     check_complex_conjugation_symmetry,
+    check_complex_bruteforce_unrolled,
 ]
