@@ -74,7 +74,7 @@ typedef enum {
     MAMBA_ERR_ALIGN = 4,   /* a pointer is not aligned to its element size       */
     MAMBA_ERR_DTYPE = 5,   /* io_dtype is not a mamba_dtype_t                    */
     MAMBA_ERR_LAUNCH = 6,  /* the CUDA launch failed (see cudaGetLastError)      */
-    MAMBA_ERR_TIMEOUT = 7, /* reserved: a bounded device-side wait gave up       */
+    MAMBA_ERR_TIMEOUT = 7, /* a bounded device-side wait gave up (mamba_device_status) */
     MAMBA_ERR_ALIAS = 8,   /* an output overlaps an input                        */
     MAMBA_ERR_SCRATCH = 9  /* _noalloc: the split needs more than its fixed scratch */
 } mamba_status_t;
@@ -124,18 +124,23 @@ int mamba_selective_scan_fwd(const void *u, const void *delta, const float *A_lo
  * synchronise the device or fail under memory pressure at a moment the caller
  * does not control).
  *
- * Same arguments, same operation and same results as mamba_selective_scan_fwd
- * (bit for bit: the same kernels run with the same split).  When the scan is
- * split along time, the carried states live in a fixed device buffer of this
+ * Same arguments, same operation and same results as mamba_selective_scan_fwd:
+ * bit for bit whenever the allocating entry point obtains its scratch and the
+ * planner's split fits the fixed buffer (always, up to about 240 SMs), since
+ * the same kernels then run with the same split.  When the scan is split
+ * along time, the carried states live in a fixed device buffer of this
  * library (4 MiB per device, a static __device__ array) instead of
  * stream-ordered scratch:
- *   - The buffer's address is looked up once per device (cudaGetSymbolAddress)
- *     by the first call on that device.  Make that first call before any
- *     stream capture; it may also be where the driver loads this library's
- *     module on that device.  A failed look-up returns MAMBA_ERR_LAUNCH.
- *   - A split that needs more than 4 MiB (possible only when a test forces
- *     more segments than the planner would choose) returns MAMBA_ERR_SCRATCH
- *     before anything is launched.
+ *   - The buffer's address is looked up per device (cudaGetSymbolAddress) by
+ *     the first call on that device, and kept once the look-up succeeds.
+ *     Make that first call before any stream capture; it may also be where
+ *     the driver loads this library's module on that device.  A failed
+ *     look-up returns MAMBA_ERR_LAUNCH, leaves no CUDA error set, and is
+ *     tried again by the next call.
+ *   - A planned split that would need more than 4 MiB uses fewer segments.
+ *     Only a segment count forced through MAMBA_SCAN_SEGMENTS (a testing
+ *     switch) that needs more returns MAMBA_ERR_SCRATCH, before anything is
+ *     launched.
  *   - Nothing in the buffer has to start at zero.
  *   - Calls that overlap in time on one device (other streams, other host
  *     threads) share the buffer and race.  Calls ordered on one stream are

@@ -46,20 +46,29 @@ constexpr size_t kNoallocScratchBytes = size_t(4) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_scratch_once[kMaxDevices];
-void* g_scratch_addr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices];  // set once the look-up on that device has succeeded
 
+// Address of the fixed buffer on the current device.  Only a successful
+// look-up is kept: a failed one (e.g. made while the module cannot be loaded)
+// leaves no CUDA error behind and is retried by the next call.
 cudaError_t noalloc_scratch(void** out) {
     int dev = 0;
-    const cudaError_t err = cudaGetDevice(&dev);
+    cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::call_once(g_scratch_once[dev], [dev] {
-        g_scratch_err[dev] = cudaGetSymbolAddress(&g_scratch_addr[dev], g_noalloc_scratch);
-    });
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        void* p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (err != cudaSuccess) {
+            cudaGetLastError();
+            return err;
+        }
+        g_scratch_addr[dev] = p;
+    }
     *out = g_scratch_addr[dev];
-    return g_scratch_err[dev];
+    return cudaSuccess;
 }
 
 // Argument checks of the forward scan: MAMBA_OK to go on, else the status.

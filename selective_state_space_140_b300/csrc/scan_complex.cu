@@ -7,9 +7,13 @@
 //   h    = exp(dt * A) * h + dt * B[b,t,n] * u          (B, C complex)
 //   y    = (Re(sum_n C[b,t,n] * h) + D[d] * u) * SiLU(z)
 // exp(dt*A) = 2^(dt*Re A*log2 e) * (cos(dt*Im A) + i sin(dt*Im A)): one SFU
-// exponential and one sine/cosine pair per state and step; the angle is first
-// reduced to [-pi, pi] with a two-part 2*pi (2*pi = kTwoPiHi + kTwoPiLo in
-// fp32), since dt*Im A reaches hundreds of radians for large steps.
+// exponential and one sine/cosine pair per state and step.  The angle
+// dt*Im A reaches hundreds of radians for large steps, so its absolute error
+// grows with it.  fp32 io forms the step dt and the angle in fp64 and reduces
+// the angle to a quadrant there (exact to far below fp32 rounding), then takes
+// sine and cosine of the fp32 remainder; bf16 io (where the output rounding is
+// 2^-9) forms the angle in fp32 and reduces it to [-pi, pi] with a two-part
+// 2*pi (2*pi = kTwoPiHi + kTwoPiLo in fp32).
 //
 // Structure (one launch): 64-thread CTAs, G lanes per chain with NPL complex
 // states each, 64/G chains per CTA; the sequence runs in 16-step chunks whose
@@ -47,7 +51,10 @@ struct CxCfg {
     static constexpr int oDt = 0, oDu = kF, oU = 2 * kF, oYs = 3 * kF;
     static constexpr int oB = 4 * kF, oC = oB + T * NP * 2;  // [T][NP][re, im]
     static constexpr int kFloats = oC + T * NP * 2;
-    static constexpr size_t kSmem = size_t(kFloats) * 4;
+    // fp32 io only: the step dt in fp64, [t][chain] like oDt, after the floats
+    static constexpr bool kDt64 = sizeof(io_t) == 4;
+    static constexpr int oDt64 = (kFloats + 1) / 2;  // in doubles
+    static constexpr size_t kSmem = kDt64 ? size_t(oDt64 + kF) * 8 : size_t(kFloats) * 4;
     static_assert(T % EPT == 0, "a thread's elements stay within one chain");
 };
 
@@ -112,17 +119,11 @@ __device__ __forceinline__ void cx_fetch(const CxArgs& p, CxRaw<io_t, NPL, G>& r
     }
 }
 
-constexpr float kPio2Hi = 1.57079637050628662109375f;   // fp32 nearest to pi/2
-constexpr float kPio2Lo = -4.371139000186243e-8f;        // pi/2 - kPio2Hi
-constexpr float kTwoOverPi = 0.63661977236758134f;
-
-// sin and cos of x to fp32 accuracy on the FMA pipe: x = q*pi/2 + r with
-// |r| <= pi/4 (Cody-Waite with a two-part pi/2), Taylor series of sin r to
-// r^9 and of cos r to r^10 (next terms below 2e-10 at pi/4), then the
-// quadrant q mod 4 rotates (sin r, cos r).
-__device__ __forceinline__ void sincos_poly(float x, float& s, float& c) {
-    const float q = rintf(x * kTwoOverPi);
-    const float r = fmaf(-q, kPio2Lo, fmaf(-q, kPio2Hi, x));
+// sin and cos of q * pi/2 + r to fp32 accuracy on the FMA pipe, given |r| <=
+// pi/4 and the quadrant k = q mod 4: Taylor series of sin r to r^9 and of cos
+// r to r^10 (next terms below 2e-10 at pi/4), then the quadrant rotates
+// (sin r, cos r).
+__device__ __forceinline__ void sincos_reduced(float r, int k, float& s, float& c) {
     const float r2 = r * r;
     float ps = fmaf(r2, 1.f / 362880.f, -1.f / 5040.f);
     ps = fmaf(ps, r2, 1.f / 120.f);
@@ -133,24 +134,38 @@ __device__ __forceinline__ void sincos_poly(float x, float& s, float& c) {
     pc = fmaf(pc, r2, 1.f / 24.f);
     pc = fmaf(pc, r2, -0.5f);
     const float cr = fmaf(pc, r2, 1.f);
-    const int k = int(q) & 3;
+    k &= 3;
     const float a = (k & 1) ? cr : sr, b = (k & 1) ? sr : cr;
     s = (k & 2) ? -a : a;
     c = ((k + 1) & 2) ? -b : b;
 }
 
+// The angle dt * aim in fp64, written as q * pi/2 + r with |r| <= pi/4: the
+// product of an fp64 step and an fp32 rate is rounded once to fp64 (2^-53
+// relative), and the fp64 pi/2 (error 6e-17) keeps q * pi/2 exact to ~1e-12
+// rad for any angle this scan meets, so r carries only its own fp32 rounding.
+constexpr double kPio2D = 1.5707963267948966;
+constexpr double kTwoOverPiD = 0.6366197723675814;
+__device__ __forceinline__ void sincos_fp64_angle(double dt, float aim, float& s, float& c) {
+    const double ang = dt * double(aim);
+    const double q = rint(ang * kTwoOverPiD);
+    const float r = float(fma(-q, kPio2D, ang));
+    sincos_reduced(r, int(static_cast<long long>(q) & 3), s, c);
+}
+
 // exp(dt * (Re + i Im)) for one state: the magnitude on the SFU; the phase by
-// sincos_poly (ACC) or by the SFU's sine and cosine of the angle reduced to
-// [-pi, pi] (absolute error about 4e-7 per step, which a long-memory state
-// accumulates: used for bf16 io, where it stays far below the output's
-// rounding)
+// sincos_fp64_angle (ACC: fp32 io, dt64 the step in fp64) or by the SFU's
+// sine and cosine of the angle reduced to [-pi, pi] in fp32 (absolute error
+// about 4e-7 per step, which a long-memory state accumulates: used for bf16
+// io, where it stays far below the output's rounding)
 template <bool ACC>
-__device__ __forceinline__ void cx_decay(float dt, float a2, float aim, float& ar, float& ai) {
-    const float ang = dt * aim;
+__device__ __forceinline__ void cx_decay(float dt, double dt64, float a2, float aim, float& ar,
+                                         float& ai) {
     float s, c;
     if constexpr (ACC) {
-        sincos_poly(ang, s, c);
+        sincos_fp64_angle(dt64, aim, s, c);
     } else {
+        const float ang = dt * aim;
         const float q = rintf(ang * kInvTwoPi);
         const float red = fmaf(-q, kTwoPiLo, fmaf(-q, kTwoPiHi, ang));
         __sincosf(red, &s, &c);
@@ -165,6 +180,7 @@ __global__ void __launch_bounds__(kCNTH) scan_complex_kernel(const CxArgs p, con
     using C = CxCfg<io_t, NPL, G>;
     constexpr int T = C::T, NTH = C::NTH, CH = C::CH, NP = C::NP, S = C::kS, EPT = C::EPT;
     extern __shared__ __align__(16) float sm[];
+    double* smd = reinterpret_cast<double*>(sm);
 
     const int64_t L = p.seqlen, dim = p.dim;
     const int N = p.dstate;
@@ -200,10 +216,21 @@ __global__ void __launch_bounds__(kCNTH) scan_complex_kernel(const CxArgs p, con
 #pragma unroll
         for (int j = 0; j < EPT; ++j) {
             const bool ok = e_live && t0 + te0 + j < L;
-            const float raw = cx_f(r.dl[j]) + e_bias;
-            float dt = p.softplus ? (sizeof(io_t) == 2 ? softplus_fast(raw) : softplus_accurate(raw))
-                                  : raw;
-            if (!ok) dt = 0.f;
+            float dt;
+            if constexpr (C::kDt64) {
+                // fp64 step: its relative error would otherwise reach the
+                // phase multiplied by the angle
+                const double raw = double(cx_f(r.dl[j])) + double(e_bias);
+                double dt64 = p.softplus ? (raw > 0.0 ? raw + log1p(exp(-raw)) : log1p(exp(raw)))
+                                         : raw;
+                if (!ok) dt64 = 0.0;
+                if (e0 + j < C::kE) smd[C::oDt64 + (te0 + j) * S + ce] = dt64;
+                dt = float(dt64);
+            } else {
+                const float raw = cx_f(r.dl[j]) + e_bias;
+                dt = p.softplus ? softplus_fast(raw) : raw;
+                if (!ok) dt = 0.f;
+            }
             const float u = cx_f(r.u[j]);
             e_z[j] = cx_f(r.z[j]);
             if (e0 + j < C::kE) {
@@ -236,12 +263,13 @@ __global__ void __launch_bounds__(kCNTH) scan_complex_kernel(const CxArgs p, con
 #pragma unroll
         for (int t = 0; t < T; ++t) {
             const float dt = sm[C::oDt + t * S + c], du = sm[C::oDu + t * S + c];
+            const double dt64 = C::kDt64 ? smd[C::oDt64 + t * S + c] : 0.0;
             float acc = 0.f;
 #pragma unroll
             for (int i = 0; i < NPL; ++i) {
                 const int n = g * NPL + i;
                 float ar, ai;
-                cx_decay<sizeof(io_t) == 4>(dt, A2[i], Aim[i], ar, ai);
+                cx_decay<sizeof(io_t) == 4>(dt, dt64, A2[i], Aim[i], ar, ai);
                 const float2 Bn = *reinterpret_cast<const float2*>(sm + C::oB + (t * NP + n) * 2);
                 const float2 Cn = *reinterpret_cast<const float2*>(sm + C::oC + (t * NP + n) * 2);
                 const float nr = fmaf(ar, hr[i], fmaf(-ai, hi[i], Bn.x * du));

@@ -1823,26 +1823,42 @@ bool try_ws_split(const ScanArgs& a, cudaStream_t stream, const ScanScratch& sc,
     using C = WsCfg<io_t, 1, 8, 2, 64, 64>;
     if (!ws_ok<io_t, 1, 8, 2, 64, 64>(a) || a.seqlen == 0) return false;
     int seg_len = 0;
-    const int nseg = plan_segments(a, C::CH, &seg_len);
+    int nseg = plan_segments(a, C::CH, &seg_len);
     if (nseg < 2) return false;
     const int64_t chains = a.batch * a.dim;
     auto rnd = [](size_t x) { return (x + 255) / 256 * 256; };
-    const size_t hbytes = rnd(size_t(chains) * nseg * a.dstate * sizeof(float));
-    const size_t bytes = hbytes + rnd(size_t(chains) * (nseg - 1) * sizeof(float));
+    auto bytes_for = [&](int ns) {
+        return rnd(size_t(chains) * ns * a.dstate * sizeof(float)) +
+               rnd(size_t(chains) * (ns - 1) * sizeof(float));
+    };
     void* buf = sc.ptr;
     bool owned = false;
     if (buf) {
-        if (bytes > sc.bytes) {
+        // A caller buffer too small for the planner's split takes fewer
+        // segments (the planner's choice fits 4 MiB up to ~240 SMs); only a
+        // forced segment count that does not fit is an error.
+        if (bytes_for(nseg) > sc.bytes && env_int("MAMBA_SCAN_SEGMENTS") <= 0) {
+            while (nseg >= 2 && bytes_for(nseg) > sc.bytes) --nseg;
+            if (nseg < 2) return false;
+            seg_len = int(((a.seqlen + nseg - 1) / nseg + 15) / 16 * 16);
+            nseg = int((a.seqlen + seg_len - 1) / seg_len);
+        }
+        if (bytes_for(nseg) > sc.bytes) {
             *err = cudaErrorMemoryAllocation;
             return true;
         }
     } else {
-        if (!sc.may_alloc || cudaMallocAsync(&buf, bytes, stream) != cudaSuccess) {
-            cudaGetLastError();  // clear a failed allocation; run unsplit
+        // A failed allocation runs the scan unsplit.  It clears the error it
+        // set, but only when no error was pending before it.
+        const bool pending = cudaPeekAtLastError() != cudaSuccess;
+        if (!sc.may_alloc) return false;
+        if (cudaMallocAsync(&buf, bytes_for(nseg), stream) != cudaSuccess) {
+            if (!pending) cudaGetLastError();
             return false;
         }
         owned = true;
     }
+    const size_t hbytes = rnd(size_t(chains) * nseg * a.dstate * sizeof(float));
     SegArgs sg{seg_len, nseg, nseg - 1, static_cast<float*>(buf),
                reinterpret_cast<float*>(static_cast<char*>(buf) + hbytes)};
     *err = launch_ws<io_t, 1, 8, 2, 64, 64, 4, kScanSummary>(a, sg, stream);

@@ -112,6 +112,15 @@ def make_scan_inputs(batch: int, dim: int, seqlen: int, dstate: int, io_dtype: s
     }
 
 
+def wide_a_log(dim: int, dstate: int, seed: int) -> torch.Tensor:
+    """A_log [dim, dstate] fp32 with |A| = exp(A_log) log-uniform over [1e-2, 1e2]
+    per (channel, state): the spread of a trained layer, whose slow states
+    (|A| * dt far below 1/L) keep their whole history."""
+    g = torch.Generator().manual_seed(int(seed))
+    lo, hi = np.log(1e-2), np.log(1e2)
+    return (torch.rand(dim, dstate, generator=g, dtype=torch.float64) * (hi - lo) + lo).float()
+
+
 def make_config_inputs(cfg: ScanConfig) -> dict:
     return make_scan_inputs(cfg.batch, cfg.dim, cfg.seqlen, cfg.dstate, cfg.io_dtype, cfg.seed,
                             cfg.d_mode)

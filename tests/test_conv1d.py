@@ -6,12 +6,14 @@ form of SiLU (relative error about 2^-21); bf16 io 1e-2 -- the output is
 rounded to bf16 (relative 2^-9, up to 2^-8 against the 0.1 rms floor).  The
 states are copies of inputs and must match exactly.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from parity_util import rel_err, to_device
+from parity_util import blockwise_rel_err, channel_blocks, rel_err, to_device
 from selective_state_space_140_b300 import abi, workloads
 
 pytestmark = pytest.mark.gpu
@@ -146,17 +148,21 @@ def test_decode_steps_match_oracle_and_the_full_pass(cuda, io, width):
     assert torch.equal(dec, full) and torch.equal(state, fin)
 
 
-def test_full_size_layer_on_sampled_rows(cuda):
+def test_full_size_layer_every_row(cuda):
     """The conv in front of the Mamba-1.4B-style layer (batch 4, d_inner 4096,
-    L = 4096, width 4, bf16), launched as the bench times it; sampled rows
-    against the oracle."""
+    L = 4096, width 4, bf16), launched as the bench times it; every row
+    against the oracle, and every final state exactly."""
     x = workloads.make_conv_inputs(4, 4096, 4096, 4, "bf16", seed=27)
     out, fin = _gpu(x, cuda)
-    r = np.random.default_rng(0)
-    rows = [(0, 0), (3, 4095)] + [(int(r.integers(4)), int(r.integers(4096))) for _ in range(6)]
     f = workloads.to_f64
-    for b, d in rows:
-        o, s = oracle.causal_conv1d(f(x["x"][b:b + 1, d:d + 1]), f(x["weight"][d:d + 1]),
-                                    bias=f(x["bias"][d:d + 1]))
-        assert rel_err(out[b, d], o[0, 0]) <= CTOL["bf16"], (b, d)
-        assert np.array_equal(fin[b, d], s[0, 0]), (b, d)
+
+    def pair(blk):
+        b, d0, d1 = blk
+        o, s = oracle.causal_conv1d(f(x["x"][b:b + 1, d0:d1]), f(x["weight"][d0:d1]),
+                                    bias=f(x["bias"][d0:d1]))
+        assert np.array_equal(fin[b:b + 1, d0:d1], s), (b, d0)
+        return {"out": (out[b:b + 1, d0:d1], o)}
+
+    (e,) = blockwise_rel_err(channel_blocks(4, 4096, 512), pair, floors=(0.1,),
+                             workers=os.cpu_count() or 1)["out"]
+    assert e <= CTOL["bf16"], e

@@ -2,26 +2,29 @@
 
 Every gradient is compared element by element with the metric of the forward
 parity tests (``parity_util.rel_err``: max |gpu - ref| / max(|ref|, 0.1 rms)).
-Tolerances: per-element gradients (du, ddelta, dz) and the sums share one
-bound per io dtype.  fp32 io: 1e-3 -- ten times the forward's bound, because
-the adjoint runs the recurrence a second time (recomputed states feed it) and
-dA_log, dD and the bias gradient add one fp32 term per step over the whole
-sequence and every batch row; measured on B300 the largest error over the
-shapes below and L=4096 was 1.4e-4.  bf16 io: 1e-2 -- du, ddelta and dz are
-rounded to bf16 (relative 2^-9, up to 2^-8 against the 0.1 rms floor), and
-the measured largest error was 3.9e-3; the fp32 sums stay near 1e-4.
+Tolerances, per io dtype, shared by the per-element gradients (du, ddelta,
+dz) and the sums: fp32 io 3e-4 -- the backward is three fp32 evaluations in
+a row, each held to the forward's 1e-4: the recomputed forward states, the
+adjoint recurrence (a second length-L recurrence with the same decays, hence
+the same error growth), and the parameter sums (dA_log, dD and the bias
+gradient add one fp32 term per step and batch row).  bf16 io 1e-2 -- du,
+ddelta and dz are rounded to bf16 (relative 2^-8) on top of the fp32 bound
+of the bf16-input arithmetic (the bf16 forward's 2e-2 covers one pass; the
+gradients read inputs that carry no extra rounding).
 """
+import os
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from parity_util import rel_err, sample_chains, to_device
+from parity_util import blockwise_rel_err, rel_err, to_device
 from selective_state_space_140_b300 import abi, workloads
 
 pytestmark = pytest.mark.gpu
 
-GTOL = {"f32": 1e-3, "bf16": 1e-2}
+GTOL = {"f32": 3e-4, "bf16": 1e-2}
 PER_ELEMENT = ("du", "ddelta", "dz")
 
 
@@ -172,27 +175,45 @@ def test_gradient_check_against_forward_kernel(cuda):
         assert abs(fd - an) <= 2e-3 * max(1.0, abs(an)), (name, fd, an)
 
 
-def test_full_size_layer_on_sampled_chains(cuda):
-    """Mamba-1.4B-style layer (batch 4, d_inner 4096, L=4096, N=16, bf16): the
-    per-element gradients of sampled chains, and dA_log / dD / the bias
-    gradient of sampled channels (each a sum over the 4 batch rows), against
-    the oracle run on exactly those chains."""
+def test_full_size_layer_every_chain(cuda):
+    """Mamba-1.4B-style layer (batch 4, d_inner 4096, L=4096, N=16, bf16):
+    every per-element gradient of every chain, dA_log / dD / the bias gradient
+    of every channel (each a sum over the 4 batch rows) and dB / dC (sums over
+    all 4096 channels) against the oracle, run channel block by channel block
+    on the host's cores."""
     cfg = workloads.SCAN_CONFIGS["mamba1p4b_bf16"]
     x = workloads.make_config_inputs(cfg)
     dout = _dout(x, cfg.seed)
     gg = _gpu_bwd(x, dout, cuda)
-    chans = sorted({d for _, d in sample_chains(cfg.batch, cfg.dim, 6, seed=cfg.seed)})
     f = workloads.to_f64
-    for d in chans:
-        sl = lambda t: None if t is None else t[:, d:d + 1]
-        sd = lambda t: None if t is None else t[d:d + 1]
-        gr = oracle.selective_scan_bwd(f(sl(x["u"])), f(sl(x["delta"])), f(x["A_log"][d:d + 1]),
+    block = 64
+    blocks = [(d0, min(cfg.dim, d0 + block)) for d0 in range(0, cfg.dim, block)]
+    sums = {}
+
+    def pair(blk):
+        d0, d1 = blk
+        sl = lambda t: None if t is None else t[:, d0:d1]
+        sd = lambda t: None if t is None else t[d0:d1]
+        gr = oracle.selective_scan_bwd(f(sl(x["u"])), f(sl(x["delta"])), f(x["A_log"][d0:d1]),
                                        f(x["B"]), f(x["C"]), f(sl(dout)), D=f(sd(x["D"])),
                                        z=f(sl(x["z"])), delta_bias=f(sd(x["delta_bias"])))
-        part = {k: gg[k][:, d:d + 1] for k in PER_ELEMENT}
-        part.update({"dA_log": gg["dA_log"][d:d + 1], "dD": gg["dD"][d:d + 1],
-                     "ddelta_bias": gg["ddelta_bias"][d:d + 1]})
-        _assert_grads(x, part, {k: gr[k] for k in part}, what=f"channel {d}")
+        sums[blk] = (gr["dB"], gr["dC"])  # this block's share of the sums over channels
+        out = {k: (gg[k][:, d0:d1], gr[k]) for k in PER_ELEMENT}
+        out.update({"dA_log": (gg["dA_log"][d0:d1], gr["dA_log"]),
+                    "dD": (gg["dD"][d0:d1], gr["dD"]),
+                    "ddelta_bias": (gg["ddelta_bias"][d0:d1], gr["ddelta_bias"])})
+        return out
+
+    errs = {k: e[0] for k, e in blockwise_rel_err(blocks, pair, floors=(0.1,),
+                                                  workers=os.cpu_count() or 1).items()}
+    for i, k in enumerate(("dB", "dC")):
+        total = sums[blocks[0]][i].copy()
+        for blk in blocks[1:]:
+            total += sums[blk][i]
+        errs[k] = rel_err(gg[k], total)
+    tol = GTOL["bf16"]
+    bad = {k: e for k, e in errs.items() if e > tol}
+    assert not bad, ", ".join(f"{k} {e:.2e}" for k, e in errs.items()) + f" (tol {tol})"
 
 
 @pytest.mark.parametrize("tile", ["0", "1"])

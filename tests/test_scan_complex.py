@@ -2,21 +2,20 @@
 
 Error metric and tolerances as for the real scan (``parity_util``: 1e-4 for
 fp32 io, 2e-2 for bf16 io); the state is compared as (re, im) pairs with the
-same metric.  One addition for fp32 io: the phase step dt * Im A is formed in
-fp32 (relative error about 2^-23 of an angle that reaches hundreds of radians
-when Im A = n runs to 255), so the rotation -- and every state it feeds --
-inherits an error proportional to that angle.  The fp32 bound is therefore
-1e-4 * max(1, theta_max / 8), theta_max = max |dt * Im A| over the inputs:
-1e-4 up to 8 rad.  The slope is measured, not derived: on B300 the
-dstate-256 case (theta_max 37 rad) gave a state error of 1.03e-4, i.e. about
-2.8e-6 per radian; 1e-4 per 8 rad leaves 4.5x margin.
+same metric.  The angle dt * Im A reaches hundreds of radians for large steps
+and fast rotations, so an angle formed in fp32 would carry an absolute error
+of |dt * Im A| * 2^-24 per step (and the step dt's own rounding on top); the
+fp32-io kernel therefore forms dt and the angle in fp64 and the plain 1e-4
+bound applies to every case here, large angles included.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from parity_util import TOL, rel_err, sample_chains, to_device
+from parity_util import TOL, blockwise_rel_err, channel_blocks, rel_err, to_device
 from selective_state_space_140_b300 import abi, workloads
 
 pytestmark = pytest.mark.gpu
@@ -52,8 +51,6 @@ def _theta_max(x):
 
 def _check(x, got, want, what):
     tol = TOL[x["io_dtype"]]
-    if x["io_dtype"] == "f32":
-        tol *= max(1.0, _theta_max(x) / 8.0)
     ey, eh = rel_err(got[0], want[0]), rel_err(got[1], want[1])
     assert ey <= tol and eh <= tol, f"{what}: y err {ey:.2e}, state err {eh:.2e}, tol {tol}"
 
@@ -96,6 +93,7 @@ def test_large_steps_and_fast_rotations(cuda):
     x = workloads.make_complex_inputs(1, 8, 64, 16, "f32", seed=33)
     x["delta_bias"] = torch.linspace(-3.0, 25.0, 8)
     x["A_im"] = (torch.arange(16, dtype=torch.float32) * 2.7).repeat(8, 1).contiguous()
+    assert _theta_max(x) > 500.0  # the angles this test is about
     _check(x, _gpu(x, cuda), _ref(x), "large steps")
 
 
@@ -131,18 +129,26 @@ def test_empty_and_no_state(cuda):
     assert rel_err(y.float().cpu().numpy(), _ref(x)[0]) <= TOL["bf16"]
 
 
-def test_full_size_layer_on_sampled_chains(cuda):
+def test_full_size_layer_every_chain(cuda):
     """Complex variant of the Mamba-130M-style layer (batch 8, d_inner 1536,
-    L = 2048, N = 16, bf16): sampled chains against the oracle."""
+    L = 2048, N = 16, bf16): every chain against the oracle, channel block by
+    channel block on the host's cores."""
     x = workloads.make_complex_inputs(8, 1536, 2048, 16, "bf16", seed=37)
     y, h = _gpu(x, cuda)
     f = workloads.to_f64
-    for b, d in sample_chains(8, 1536, 8, seed=37):
-        sl = lambda t: None if t is None else t[b:b + 1, d:d + 1]
-        sd = lambda t: None if t is None else t[d:d + 1]
+
+    def pair(blk):
+        b, d0, d1 = blk
+        sl = lambda t: None if t is None else t[b:b + 1, d0:d1]
+        sd = lambda t: None if t is None else t[d0:d1]
         yr, hr = oracle.selective_scan_complex(
-            f(sl(x["u"])), f(sl(x["delta"])), f(x["A_log_re"][d:d + 1]), f(x["A_im"][d:d + 1]),
+            f(sl(x["u"])), f(sl(x["delta"])), f(x["A_log_re"][d0:d1]), f(x["A_im"][d0:d1]),
             f(x["B"][b:b + 1]), f(x["C"][b:b + 1]), D=f(sd(x["D"])), z=f(sl(x["z"])),
             delta_bias=f(sd(x["delta_bias"])))
-        assert rel_err(y[b, d], yr[0, 0]) <= TOL["bf16"], (b, d)
-        assert rel_err(h[b, d], np.stack([hr.real, hr.imag], -1)[0, 0]) <= TOL["bf16"], (b, d)
+        return {"y": (y[b:b + 1, d0:d1], yr),
+                "h": (h[b:b + 1, d0:d1], np.stack([hr.real, hr.imag], -1))}
+
+    errs = blockwise_rel_err(channel_blocks(8, 1536, 128), pair, floors=(0.1,),
+                             workers=os.cpu_count() or 1)
+    for k, (e,) in errs.items():
+        assert e <= TOL["bf16"], (k, e)

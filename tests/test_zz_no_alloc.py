@@ -21,12 +21,19 @@ def _call(fn, xd, y=None, h=None):
               delta_bias=xd["delta_bias"], softplus=xd["softplus"], y=y, last_state=h)
 
 
-@pytest.mark.parametrize("io,batch,dim,L", [("bf16", 1, 96, 8192), ("f32", 2, 48, 4096)])
-def test_noalloc_matches_the_allocating_entry_on_two_calls_in_a_row(cuda, io, batch, dim, L):
+@pytest.mark.parametrize("io,batch,dim,L,segments", [("bf16", 1, 96, 8192, None),
+                                                     ("f32", 2, 48, 4096, None),
+                                                     ("bf16", 2, 64, 2048, "4")])
+def test_noalloc_matches_the_allocating_entry_on_two_calls_in_a_row(cuda, io, batch, dim, L,
+                                                                    segments, monkeypatch):
     """Few chains and a long sequence: both entry points split the scan (the
-    planner's choice), so the no-alloc calls use the fixed scratch.  Two
-    no-alloc calls back to back on one stream reuse it; each must equal the
-    allocating entry point bit for bit and match the oracle."""
+    planner's choice, or a forced segment count so that the split and hence
+    the fixed scratch is used whatever the planner decides), so the no-alloc
+    calls use the fixed scratch.  Two no-alloc calls back to back on one
+    stream reuse it; each must equal the allocating entry point bit for bit
+    and match the oracle."""
+    if segments is not None:
+        monkeypatch.setenv("MAMBA_SCAN_SEGMENTS", segments)
     x = workloads.make_scan_inputs(batch, dim, L, 16, io, seed=31, d_mode="normal")
     xd = to_device(x, cuda)
     y_ref, h_ref = _call(abi.mamba_selective_scan_fwd, xd)
