@@ -228,30 +228,36 @@ int mamba_selective_scan_bwd(const void *u, const void *delta, const float *A_lo
  * starting state h0 and with document boundaries (codechina.net overview,
  * section 3.2 point 2: resetting the hidden state isolates documents; the
  * same page's deployment notes on block-by-block processing of long
- * sequences).  Training on packed documents needs these gradients, and dh0
- * is the gradient a preceding block's final state receives.  This call takes
- * no gradient for last_state (the loss is a function of y alone), so it
- * gives the gradients of the last block of a chain, or of blocks whose final
- * state feeds nothing that is differentiated.
+ * sequences).  Training on packed documents needs these gradients.  A long
+ * sequence trained block by block chains them backwards: dh0 of block k + 1
+ * is the gradient block k's final state receives, passed to block k as its
+ * dlast_state.
  *
  *   h0    : [batch, dim, dstate] fp32 or NULL (zero start), as for the forward
  *   reset : [batch, seqlen] bytes or NULL; non-zero at a token that starts a
  *           document (the state restarts from zero before it): no gradient
  *           flows back across it
+ *   dlast_state : [batch, dim, dstate] fp32 or NULL: the gradient of the loss
+ *           with respect to last_state (the state after the last step), added
+ *           to the adjoint where it enters from the right; NULL means the loss
+ *           does not depend on last_state.  It stops at the last document
+ *           start of a row, like the output gradients.
  *   dh0   : [batch, dim, dstate] fp32 or NULL (not wanted), written with the
- *           gradient of h0 (of a zero start when h0 is NULL); zero when
- *           seqlen == 0
+ *           gradient of h0 (of a zero start when h0 is NULL); equal to
+ *           dlast_state (or zero) when seqlen == 0
  *
  * Every other argument, layout, scratch rule and error is as for
- * mamba_selective_scan_bwd, which is this call with h0, reset and dh0 NULL
- * (bit for bit).  h0 and reset must not overlap any output (MAMBA_ERR_ALIAS).
+ * mamba_selective_scan_bwd, which is this call with h0, reset, dlast_state and
+ * dh0 NULL (bit for bit).  h0, reset and dlast_state must not overlap any
+ * output (MAMBA_ERR_ALIAS); dlast_state must be 4-byte aligned.
  */
 int mamba_selective_scan_bwd_ex(const void *u, const void *delta, const float *A_log,
                                 const void *B, const void *C, const float *D, const void *z,
                                 const float *delta_bias, int softplus_flag, const float *h0,
-                                const unsigned char *reset, const void *dout, void *du,
-                                void *ddelta, void *dz, float *dA_log, float *dB, float *dC,
-                                float *dD, float *ddelta_bias, float *dh0, int64_t batch,
+                                const unsigned char *reset, const void *dout,
+                                const float *dlast_state, void *du, void *ddelta, void *dz,
+                                float *dA_log, float *dB, float *dC, float *dD,
+                                float *ddelta_bias, float *dh0, int64_t batch,
                                 int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
                                 mamba_stream_t stream);
 

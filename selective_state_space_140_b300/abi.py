@@ -56,9 +56,9 @@ def _declare(lib):
     lib.mamba_selective_scan_bwd.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, vp, vp, vp, vp,
                                              fp, fp, fp, fp, fp, i64, i64, i64, i64, ci, vp]
     lib.mamba_selective_scan_bwd_ex.restype = ci
-    lib.mamba_selective_scan_bwd_ex.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, fp, vp, vp, vp,
-                                                vp, vp, fp, fp, fp, fp, fp, fp, i64, i64, i64, i64,
-                                                ci, vp]
+    lib.mamba_selective_scan_bwd_ex.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, fp, vp, vp, fp,
+                                                vp, vp, vp, fp, fp, fp, fp, fp, fp, i64, i64, i64,
+                                                i64, ci, vp]
     lib.mamba_selective_scan_complex_fwd.restype = ci
     lib.mamba_selective_scan_complex_fwd.argtypes = [vp, vp, fp, fp, vp, vp, fp, vp, fp, ci, vp,
                                                      fp, i64, i64, i64, i64, ci, vp]
@@ -221,7 +221,8 @@ def _scan_fwd(entry, u, delta, A_log, B, C, D, z, delta_bias, softplus, y, last_
 
 def mamba_selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_bias=None,
                              softplus=True, want_dD=True, want_ddelta_bias=True, grads=None,
-                             stream=None, h0=None, reset=None, want_dh0=None):
+                             stream=None, h0=None, reset=None, want_dh0=None,
+                             dlast_state=None):
     """Gradients of ``mamba_selective_scan_fwd`` (zero initial state) for the
     output gradient ``dout``; returns a dict with ``du``, ``ddelta``,
     ``dA_log``, ``dB``, ``dC`` and, when wanted, ``dz`` (iff ``z`` is given),
@@ -236,7 +237,9 @@ def mamba_selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_
     [batch, seqlen] uint8 or bool (non-zero at a document start) select the
     backward of ``mamba_selective_scan_fwd_ex`` (C entry
     ``mamba_selective_scan_bwd_ex``); ``dh0``, the gradient of h0, is
-    returned when h0 is given (or ``want_dh0``)."""
+    returned when h0 is given (or ``want_dh0``).  ``dlast_state`` [batch,
+    dim, dstate] float32 is the loss's gradient on the final state (e.g. the
+    ``dh0`` of the next block of the same sequence)."""
     dev = u.device
     batch, dim, seqlen = u.shape
     dstate = A_log.shape[-1]
@@ -265,6 +268,9 @@ def mamba_selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_
     if want_dh0 is None:
         want_dh0 = h0 is not None
     _check(h0, "h0", dev, torch.float32)
+    _check(dlast_state, "dlast_state", dev, torch.float32)
+    if dlast_state is not None and tuple(dlast_state.shape) != (batch, dim, dstate):
+        raise TypeError("dlast_state must have shape [batch, dim, dstate]")
     if reset is not None:
         _check(reset, "reset", dev)
         if reset.dtype == torch.bool:
@@ -276,7 +282,7 @@ def mamba_selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_
         if g.get("dh0") is None:
             g["dh0"] = torch.empty((batch, dim, dstate), device=dev, dtype=f32)
         _check(g["dh0"], "dh0", dev, f32)
-    if h0 is None and reset is None and not want_dh0:
+    if h0 is None and reset is None and dlast_state is None and not want_dh0:
         rc = load().mamba_selective_scan_bwd(
             _ptr(u), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
             _ptr(delta_bias), int(bool(softplus)), _ptr(dout), _ptr(g["du"]), _ptr(g["ddelta"]),
@@ -287,7 +293,8 @@ def mamba_selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_
         rc = load().mamba_selective_scan_bwd_ex(
             _ptr(u), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
             _ptr(delta_bias), int(bool(softplus)), _ptr(h0), _ptr(reset), _ptr(dout),
-            _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g.get("dz")), _ptr(g["dA_log"]), _ptr(g["dB"]),
+            _ptr(dlast_state), _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g.get("dz")),
+            _ptr(g["dA_log"]), _ptr(g["dB"]),
             _ptr(g["dC"]), _ptr(g.get("dD")), _ptr(g.get("ddelta_bias")), _ptr(g.get("dh0")),
             batch, dim, seqlen, dstate, io, _stream(stream, dev))
         entry = "mamba_selective_scan_bwd_ex"
@@ -472,9 +479,9 @@ def raw_scan_complex_fwd(u, delta, A_log_re, A_im, B, C, D, z, delta_bias, softp
 
 def raw_scan_bwd_ex(u, delta, A_log, B, C, D, z, delta_bias, softplus_flag, h0, reset, dout, du,
                     ddelta, dz, dA_log, dB, dC, dD, ddelta_bias, dh0, batch, dim, seqlen, dstate,
-                    io_dtype, stream) -> int:
+                    io_dtype, stream, dlast_state=None) -> int:
     """``mamba_selective_scan_bwd_ex`` with plain integers as pointers."""
     return load().mamba_selective_scan_bwd_ex(u, delta, A_log, B, C, D, z, delta_bias,
-                                              softplus_flag, h0, reset, dout, du, ddelta, dz,
-                                              dA_log, dB, dC, dD, ddelta_bias, dh0, batch, dim,
-                                              seqlen, dstate, io_dtype, stream)
+                                              softplus_flag, h0, reset, dout, dlast_state, du,
+                                              ddelta, dz, dA_log, dB, dC, dD, ddelta_bias, dh0,
+                                              batch, dim, seqlen, dstate, io_dtype, stream)

@@ -110,7 +110,7 @@ int check_scan_args(const void* u, const void* delta, const float* A_log, const 
 
 extern "C" {
 
-int mamba_abi_version(void) { return 1 * 10000 + 1 * 100 + 0; }
+int mamba_abi_version(void) { return 1 * 10000 + 2 * 100 + 0; }
 
 const char* mamba_status_string(int status) {
     switch (status) {
@@ -209,17 +209,18 @@ int mamba_selective_scan_bwd(const void* u, const void* delta, const float* A_lo
                              int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
                              mamba_stream_t stream) {
     return mamba_selective_scan_bwd_ex(u, delta, A_log, B, C, D, z, delta_bias, softplus_flag,
-                                       nullptr, nullptr, dout, du, ddelta, dz, dA_log, dB, dC,
-                                       dD, ddelta_bias, nullptr, batch, dim, seqlen, dstate,
-                                       io_dtype, stream);
+                                       nullptr, nullptr, dout, nullptr, du, ddelta, dz, dA_log,
+                                       dB, dC, dD, ddelta_bias, nullptr, batch, dim, seqlen,
+                                       dstate, io_dtype, stream);
 }
 
 int mamba_selective_scan_bwd_ex(const void* u, const void* delta, const float* A_log,
                                 const void* B, const void* C, const float* D, const void* z,
                                 const float* delta_bias, int softplus_flag, const float* h0,
-                                const unsigned char* reset, const void* dout, void* du,
-                                void* ddelta, void* dz, float* dA_log, float* dB, float* dC,
-                                float* dD, float* ddelta_bias, float* dh0, int64_t batch,
+                                const unsigned char* reset, const void* dout,
+                                const float* dlast_state, void* du, void* ddelta, void* dz,
+                                float* dA_log, float* dB, float* dC, float* dD,
+                                float* ddelta_bias, float* dh0, int64_t batch,
                                 int64_t dim, int64_t seqlen, int64_t dstate, int io_dtype,
                                 mamba_stream_t stream) {
     if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
@@ -237,7 +238,8 @@ int mamba_selective_scan_bwd_ex(const void* u, const void* delta, const float* A
         misaligned(ddelta, es) || misaligned(dz, es) || misaligned(A_log, 4) ||
         misaligned(D, 4) || misaligned(delta_bias, 4) || misaligned(dA_log, 4) ||
         misaligned(dB, 4) || misaligned(dC, 4) || misaligned(dD, 4) ||
-        misaligned(ddelta_bias, 4) || misaligned(h0, 4) || misaligned(dh0, 4))
+        misaligned(ddelta_bias, 4) || misaligned(h0, 4) || misaligned(dh0, 4) ||
+        misaligned(dlast_state, 4))
         return MAMBA_ERR_ALIGN;
     const int64_t elems = batch * dim * seqlen, nbc = batch * seqlen * dstate;
     const int64_t nst = batch * dim * dstate;
@@ -248,7 +250,8 @@ int mamba_selective_scan_bwd_ex(const void* u, const void* delta, const float* A
                          delta_bias ? range_of(delta_bias, dim, 4) : Range{0, 0},
                          range_of(dout, elems, es),
                          h0 ? range_of(h0, nst, 4) : Range{0, 0},
-                         reset ? range_of(reset, batch * seqlen, 1) : Range{0, 0}};
+                         reset ? range_of(reset, batch * seqlen, 1) : Range{0, 0},
+                         dlast_state ? range_of(dlast_state, nst, 4) : Range{0, 0}};
     const Range outs[] = {range_of(du, elems, es), range_of(ddelta, elems, es),
                           z ? range_of(dz, elems, es) : Range{0, 0},
                           range_of(dA_log, dim * dstate, 4), range_of(dB, nbc, 4),
@@ -277,6 +280,7 @@ int mamba_selective_scan_bwd_ex(const void* u, const void* delta, const float* A
     a.dC = dC;
     a.dD = dD;
     a.ddelta_bias = ddelta_bias;
+    a.dlast = dlast_state;
     const cudaError_t err = mamba::launch_scan_bwd_ex(a, dh0, io_dtype == MAMBA_BF16,
                                                       reinterpret_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;

@@ -84,6 +84,52 @@ __device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
     return d;
 }
 
+// ---- the decay Abar = 2^x of the recurrence ---------------------------------
+// x = dt * A * log2 e <= 0.  ex2.approx is biased near x = 0 (on B300 its
+// results over [-1, 0) average 0.1 to 0.4 ulp low), and a state whose decay is
+// within a few 1e-5 of 1 keeps such a bias for its whole memory 1/(1 - Abar),
+// where it adds up linearly instead of averaging out like rounding does.  The
+// fp32-io kernels (ACC) therefore form Abar for |x| < 1/16 as 1 + (2^x - 1)
+// from the Taylor series of e^(v), v = x ln 2, to v^4/4! (the next term is
+// below 2e-9), rounded once, so that Abar is unbiased there; beyond 1/16 a
+// state forgets within 23 steps and ex2.approx's bias stays below 1e-6.
+// kAbarC[k] = (ln 2)^k / k!.
+constexpr float kAbarC1 = 0.693147180559945f, kAbarC2 = 0.240226506959101f,
+                kAbarC3 = 0.0555041086648216f, kAbarC4 = 0.00961812910762848f;
+constexpr float kAbarSmall = 0.0625f;
+
+template <bool ACC>
+__device__ __forceinline__ float abar_exp2(float x) {
+    if constexpr (ACC) {
+        float q = __fmaf_rn(x, kAbarC4, kAbarC3);
+        q = __fmaf_rn(x, q, kAbarC2);
+        q = __fmaf_rn(x, q, kAbarC1);
+        const float s = __fmaf_rn(x, q, 1.f);
+        return fabsf(x) < kAbarSmall ? s : ex2_approx(x);
+    } else {
+        return ex2_approx(x);
+    }
+}
+
+// The same on a pair (the series in packed f32x2 arithmetic; each lane equals
+// abar_exp2's result bit for bit).
+template <bool ACC>
+__device__ __forceinline__ f32x2 abar_exp2_pair(f32x2 x) {
+    float x0, x1;
+    unpack2(x, x0, x1);
+    if constexpr (ACC) {
+        f32x2 q = fma2(x, pack2(kAbarC4, kAbarC4), pack2(kAbarC3, kAbarC3));
+        q = fma2(x, q, pack2(kAbarC2, kAbarC2));
+        q = fma2(x, q, pack2(kAbarC1, kAbarC1));
+        float s0, s1;
+        unpack2(fma2(x, q, pack2(1.f, 1.f)), s0, s1);
+        return pack2(fabsf(x0) < kAbarSmall ? s0 : ex2_approx(x0),
+                     fabsf(x1) < kAbarSmall ? s1 : ex2_approx(x1));
+    } else {
+        return pack2(ex2_approx(x0), ex2_approx(x1));
+    }
+}
+
 // ---- pointwise functions --------------------------------------------------
 // softplus(x) = log(1 + e^x), accurate version (fp32 io): libdevice expf and
 // log1pf; above 20 the correction is below 2e-9 relative and x is returned.
@@ -250,6 +296,7 @@ struct ScanBwdArgs {
     float* dC;           // [batch, L, N]
     float* dD;           // [dim] or nullptr
     float* ddelta_bias;  // [dim] or nullptr
+    const float* dlast = nullptr;  // [batch, dim, N] gradient on the final state, or nullptr (_ex only)
 };
 
 // Launchers (return the cudaError_t of the launch).

@@ -309,8 +309,18 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
     float gc[NPL], dA[NPL];  // Abar_{t+1} g_{t+1}; sum of g dt Abar h_{t-1}
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
-        // a segment before the last starts from the carried adjoint
-        gc[i] = (MODE == kBwdFull && gsg && chain_ok && g * NPL + i < N) ? gsg[g * NPL + i] : 0.f;
+        // The adjoint entering the last step from the right is the gradient on
+        // the final state (zero without one); a split's segments start from
+        // the carried adjoint, which holds it for the last segment.
+        const int n = g * NPL + i;
+        float gin = 0.f;
+        if (MODE == kBwdFull && chain_ok && n < N) {
+            if (gsg)
+                gin = gsg[n];
+            else if (EX && a.dlast)
+                gin = a.dlast[chain * N + n];
+        }
+        gc[i] = gin;
         dA[i] = 0.f;
     }
     float accD = 0.f, accB = 0.f;  // this thread's elements: sums of dy u and ddelta
@@ -531,9 +541,10 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
 //            the zero-start end state of s (hseg becomes the entering states);
 //   adjoint: Abar g entering s from the right is a(s + 1) + P(s + 1) times the
 //            value entering s + 1, a(s) the zero-start adjoint leaving s to the
-//            left, zero for the last segment (gseg becomes the entering values).
+//            left; for the last segment it is the gradient on the final state
+//            (or zero) (gseg becomes the entering values).
 __global__ void __launch_bounds__(256) bwd_carry_kernel(const float* A_log, const float* h0,
-                                                        float* hseg, float* gseg,
+                                                        const float* dlast, float* hseg, float* gseg,
                                                         const float* sdt, int64_t chains,
                                                         int64_t dim, int N, int nseg) {
     const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -550,7 +561,7 @@ __global__ void __launch_bounds__(256) bwd_carry_kernel(const float* A_log, cons
         hs[int64_t(s) * N] = H;
         H = fmaf(ex2_approx(A2 * sd[s]), H, e);
     }
-    float Gv = 0.f;
+    float Gv = dlast ? dlast[i] : 0.f;  // the gradient on the final state enters the last segment
     for (int s = nseg - 1; s >= 0; --s) {
         const float e = gs[int64_t(s) * N];
         gs[int64_t(s) * N] = Gv;
@@ -611,7 +622,8 @@ cudaError_t launch_bwd_impl(const BwdArgs& a0, bool vec_red, cudaStream_t stream
         if (err == cudaSuccess) {
             const int64_t n = chains * a.f.dstate;
             bwd_carry_kernel<<<unsigned((n + 255) / 256), 256, 0, stream>>>(
-                a.f.A_log, a.f.h0, a.hseg, a.gseg, a.sdt, chains, a.f.dim, a.f.dstate, a.nseg);
+                a.f.A_log, a.f.h0, a.dlast, a.hseg, a.gseg, a.sdt, chains, a.f.dim, a.f.dstate,
+                a.nseg);
             err = cudaGetLastError();
         }
     }
@@ -630,10 +642,11 @@ cudaError_t launch_bwd_impl(const BwdArgs& a0, bool vec_red, cudaStream_t stream
     return err;
 }
 
-// The plain backward, or (h0, resets or dh0 given) the extended one.
+// The plain backward, or (h0, resets, dh0 or a final-state gradient given)
+// the extended one.
 template <typename io_t, int NPL, int G, int UA = 2>
 cudaError_t launch_bwd(const BwdArgs& a, bool vec_red, cudaStream_t stream) {
-    if (a.f.h0 || a.f.reset || a.dh0)
+    if (a.f.h0 || a.f.reset || a.dh0 || a.dlast)
         return launch_bwd_impl<io_t, NPL, G, UA, true>(a, vec_red, stream);
     return launch_bwd_impl<io_t, NPL, G, UA, false>(a, vec_red, stream);
 }
@@ -685,9 +698,11 @@ cudaError_t launch_scan_bwd_ex(const ScanBwdArgs& s, float* dh0, bool bf16, cuda
     if (s.ddelta_bias && s.f.dim &&
         (err = cudaMemsetAsync(s.ddelta_bias, 0, size_t(s.f.dim) * 4, stream)) != cudaSuccess)
         return err;
-    if (chains == 0 || nchunks == 0) {  // nothing depends on h0
+    if (chains == 0 || nchunks == 0) {  // no steps: the final state is h0 itself
+        const size_t nst = size_t(chains) * s.f.dstate * sizeof(float);
         if (dh0 && chains > 0)
-            err = cudaMemsetAsync(dh0, 0, size_t(chains) * s.f.dstate * sizeof(float), stream);
+            err = s.dlast ? cudaMemcpyAsync(dh0, s.dlast, nst, cudaMemcpyDeviceToDevice, stream)
+                          : cudaMemsetAsync(dh0, 0, nst, stream);
         return err;
     }
     // checkpoints: the state at the start of every chunk, stream-ordered scratch

@@ -170,7 +170,7 @@ __device__ __forceinline__ void cx_decay(float dt, double dt64, float a2, float 
         const float red = fmaf(-q, kTwoPiLo, fmaf(-q, kTwoPiHi, ang));
         __sincosf(red, &s, &c);
     }
-    const float mag = ex2_approx(dt * a2);
+    const float mag = abar_exp2<ACC>(dt * a2);
     ar = mag * c;
     ai = mag * s;
 }

@@ -161,7 +161,7 @@ __device__ __forceinline__ int yunit(int q, int row) {
 // The recurrence over one chunk for one thread: NQ quads of states of chain
 // c (state group g).  sdu: (dt, dt, dt*u, dt*u) per [step][column]; sB, sC:
 // fp32 [T][NP]; sy: partial sums [NTH rows][T], 16-byte chunks swizzled.
-template <int NPL, int G, int CH, int T>
+template <bool ACC, int NPL, int G, int CH, int T>
 __device__ __forceinline__ void recurrence(const float4* sdu, const float* sB, const float* sC,
                                            float* sy, f32x2 (&h)[NPL / 2],
                                            const f32x2 (&A2)[NPL / 2], int c, int g, int tid,
@@ -180,11 +180,8 @@ __device__ __forceinline__ void recurrence(const float4* sdu, const float* sB, c
         st.sd = du2[t * CH + du_col<CH>(t, c)];
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
-            float x0, x1, x2, x3;
-            unpack2(mul2(st.sd.x, A2[2 * q]), x0, x1);
-            unpack2(mul2(st.sd.x, A2[2 * q + 1]), x2, x3);
-            st.a[2 * q] = pack2(ex2_approx(x0), ex2_approx(x1));
-            st.a[2 * q + 1] = pack2(ex2_approx(x2), ex2_approx(x3));
+            st.a[2 * q] = abar_exp2_pair<ACC>(mul2(st.sd.x, A2[2 * q]));
+            st.a[2 * q + 1] = abar_exp2_pair<ACC>(mul2(st.sd.x, A2[2 * q + 1]));
             st.bq[q] = b2[t * (NP / 4) + q];
             st.cq[q] = c2[t * (NP / 4) + q];
         }
@@ -514,7 +511,7 @@ __global__ void __launch_bounds__(CH* G)
         }
 
         // ---- phase B ----
-        recurrence<NPL, G, CH, T>(sdu, sB, sC, sy, h, A2, c, g, tid, tlen);
+        recurrence<sizeof(io_t) == 4, NPL, G, CH, T>(sdu, sB, sC, sy, h, A2, c, g, tid, tlen);
         __syncthreads();
 
         // ---- phase C ----
@@ -601,7 +598,7 @@ struct WsCfg {
 
 // The recurrence over one chunk for P chains x NPL states of one thread (the
 // multi-chain form of recurrence() above; rows of sy are chain * G + g).
-template <int P, int NPL, int G, int CH, int T>
+template <bool ACC, int P, int NPL, int G, int CH, int T>
 __device__ __forceinline__ void recurrence_multi(const float4* sdu, const float* sB,
                                                  const float* sC, float* sy,
                                                  f32x2 (&h)[P][NPL / 2],
@@ -631,11 +628,7 @@ __device__ __forceinline__ void recurrence_multi(const float4* sdu, const float*
 #pragma unroll
         for (int p = 0; p < P; ++p) {
 #pragma unroll
-            for (int q = 0; q < 2 * NQ; ++q) {
-                float x0, x1;
-                unpack2(mul2(st.sd[p].x, A2[p][q]), x0, x1);
-                st.a[p][q] = pack2(ex2_approx(x0), ex2_approx(x1));
-            }
+            for (int q = 0; q < 2 * NQ; ++q) st.a[p][q] = abar_exp2_pair<ACC>(mul2(st.sd[p].x, A2[p][q]));
         }
     };
     auto update = [&](const Step& st, float (&out)[P]) {
@@ -699,7 +692,7 @@ __device__ __forceinline__ void recurrence_multi(const float4* sdu, const float*
 
 // State-only recurrence over one chunk (no C, no partial sums): the summary
 // pass of a segmented scan needs only the state at the end of the segment.
-template <int NPL, int G, int CH, int T>
+template <bool ACC, int NPL, int G, int CH, int T>
 __device__ __forceinline__ void recurrence_state(const float4* sdu, const float* sB,
                                                  f32x2 (&h)[NPL / 2], const f32x2 (&A2)[NPL / 2],
                                                  int c, int g, int tlen) {
@@ -716,11 +709,7 @@ __device__ __forceinline__ void recurrence_state(const float4* sdu, const float*
 #pragma unroll
         for (int q = 0; q < NQ; ++q) st.bq[q] = b2[t * (NP / 4) + q];
 #pragma unroll
-        for (int q = 0; q < 2 * NQ; ++q) {
-            float x0, x1;
-            unpack2(mul2(st.sd.x, A2[q]), x0, x1);
-            st.a[q] = pack2(ex2_approx(x0), ex2_approx(x1));
-        }
+        for (int q = 0; q < 2 * NQ; ++q) st.a[q] = abar_exp2_pair<ACC>(mul2(st.sd.x, A2[q]));
     };
     auto update = [&](const Step& st) {
 #pragma unroll
@@ -849,12 +838,12 @@ __global__ void __launch_bounds__(NR + NE, MINB)
             named_sync(kBarReady + (k & 1), NTH);
             const float* sB = bcbuf(k);
             if constexpr (MODE == kScanSummary) {
-                recurrence_state<NPL, G, CH, T>(dubuf(k), sB, h[0], A2[0], cc[0], g, chunk_len(k));
+                recurrence_state<sizeof(io_t) == 4, NPL, G, CH, T>(dubuf(k), sB, h[0], A2[0], cc[0], g, chunk_len(k));
             } else if constexpr (P == 1) {
-                recurrence<NPL, G, CH, T>(dubuf(k), sB, sB + T * NP, ybuf(k), h[0], A2[0], cc[0],
+                recurrence<sizeof(io_t) == 4, NPL, G, CH, T>(dubuf(k), sB, sB + T * NP, ybuf(k), h[0], A2[0], cc[0],
                                           g, tid, chunk_len(k));
             } else {
-                recurrence_multi<P, NPL, G, CH, T>(dubuf(k), sB, sB + T * NP, ybuf(k), h, A2, cc,
+                recurrence_multi<sizeof(io_t) == 4, P, NPL, G, CH, T>(dubuf(k), sB, sB + T * NP, ybuf(k), h, A2, cc,
                                                    g, chunk_len(k));
             }
             named_arrive(kBarDone + (k & 1), NTH);
@@ -1285,10 +1274,11 @@ __global__ void __launch_bounds__(64)
             float xa[4], xb[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) unpack2(mul2(st.sd.x, A2p[j]), xa[j], xb[j]);
-            st.aa01 = pack2(ex2_approx(xa[0]), ex2_approx(xa[1]));
-            st.aa23 = pack2(ex2_approx(xa[2]), ex2_approx(xa[3]));
-            st.ab01 = pack2(ex2_approx(xb[0]), ex2_approx(xb[1]));
-            st.ab23 = pack2(ex2_approx(xb[2]), ex2_approx(xb[3]));
+            constexpr bool ACC = sizeof(io_t) == 4;
+            st.aa01 = abar_exp2_pair<ACC>(pack2(xa[0], xa[1]));
+            st.aa23 = abar_exp2_pair<ACC>(pack2(xa[2], xa[3]));
+            st.ab01 = abar_exp2_pair<ACC>(pack2(xb[0], xb[1]));
+            st.ab23 = abar_exp2_pair<ACC>(pack2(xb[2], xb[3]));
             const quad_t bq = rB[t * G + g], cq = rC[t * G + g];
             st.b01 = get_pair<io_t>(bq, 0);
             st.b23 = get_pair<io_t>(bq, 1);
@@ -1556,7 +1546,7 @@ __global__ void __launch_bounds__(CH* G)
         __syncthreads();
 
         // ---- phase B ----
-        recurrence<NPL, G, CH, T>(sdu, sB, sC, sy, h, A2, c, g, tid, tlen);
+        recurrence<sizeof(io_t) == 4, NPL, G, CH, T>(sdu, sB, sC, sy, h, A2, c, g, tid, tlen);
         __syncthreads();
         if (tid == 0 && k + 2 < nchunks && chunk_by_tma(k + 2)) {
             fence_proxy_async_smem();
@@ -1782,7 +1772,7 @@ __global__ void __launch_bounds__(256) scan_carry_kernel(const float* A_log, con
     slots[0] = h;
     for (int s = 0; s + 1 < sg.nseg; ++s) {
         // sdt = +inf when segment s holds a document boundary: decay 0
-        h = fmaf(ex2_approx(A2 * sg.sdt[chain * (sg.nseg - 1) + s]), h, slots[(s + 1) * N]);
+        h = fmaf(abar_exp2<true>(A2 * sg.sdt[chain * (sg.nseg - 1) + s]), h, slots[(s + 1) * N]);
         slots[(s + 1) * N] = h;
     }
 }

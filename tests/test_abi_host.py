@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert abi.abi_version() == 10100
+    assert abi.abi_version() == 10200
     for code, name in abi.STATUS.items():
         assert abi.status_string(code).startswith(name)
     assert abi.status_string(12345) == "unknown mamba_status_t"
@@ -264,4 +264,7 @@ def test_bwd_ex_entry_validation(lib):
     assert bx(dh0=Q[17]) == 8                                    # dh0 over h0
     assert bx(dh0=Q[12]) == 8                                    # dh0 over dA_log
     assert bx(du=Q[18]) == 8                                     # du over the reset mask
+    assert bx(dlast_state=Q[17] + 2) == 4                        # MAMBA_ERR_ALIGN
+    assert bx(dlast_state=Q[19]) == 8                            # dh0 over dlast_state
+    assert bx(dlast_state=Q[12]) == 8                            # dlast_state under dA_log
     assert bx(dim=0, h0=None, reset=None, dh0=None) == 0

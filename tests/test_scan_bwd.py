@@ -355,3 +355,75 @@ def test_ex_without_h0_or_resets_is_the_plain_backward(cuda):
     zero = torch.zeros((2, 40, 16))
     gr = _oracle_bwd_ex(x, dout, zero, None)
     assert rel_err(g_ex["dh0"], gr["dh0"]) <= GTOL["bf16"]
+
+
+def _oracle_bwd_dlast(x, dout, h0, reset, dlast):
+    f = workloads.to_f64
+    return oracle.selective_scan_bwd(f(x["u"]), f(x["delta"]), f(x["A_log"]), f(x["B"]),
+                                     f(x["C"]), f(dout), D=f(x["D"]), z=f(x["z"]),
+                                     delta_bias=f(x["delta_bias"]), softplus=x["softplus"],
+                                     h0=f(h0), reset=None if reset is None else reset.numpy(),
+                                     dlast_state=f(dlast))
+
+
+@pytest.mark.parametrize("segments", [None, "3"])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("with_reset", [False, True])
+def test_final_state_gradient_matches_oracle(cuda, monkeypatch, segments, io, with_reset):
+    """A loss on the final state as well as on y (dlast_state, the gradient of
+    last_state): every gradient and dh0 against the oracle, unsplit and with a
+    forced time split (the carry pass starts its reverse sweep from it), with
+    and without document starts (it must stop at the last one of a row)."""
+    if segments:
+        monkeypatch.setenv("MAMBA_BWD_SEGMENTS", segments)
+    x = workloads.make_scan_inputs(2, 21, 700, 16, io, seed=81, d_mode="normal")
+    dout = _dout(x, 81)
+    gen = torch.Generator().manual_seed(82)
+    h0 = torch.randn((2, 21, 16), generator=gen)
+    dlast = torch.randn((2, 21, 16), generator=gen)
+    reset = _doc_starts(2, 700, 173, 7) if with_reset else None
+    g = _bwd_ex(x, dout, cuda, h0, reset, dlast_state=dlast.to(cuda))
+    _assert_grads(x, g, _oracle_bwd_dlast(x, dout, h0, reset, dlast),
+                  what=f"dlast, {segments} segments, reset {with_reset}")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_two_blocks_train_as_one_sequence(cuda, io):
+    """Block-by-block training of one long sequence: the forward runs block 1
+    from zero and block 2 from block 1's final state; the backward runs block 2
+    from that state, and block 1 with block 2's dh0 as its final-state
+    gradient.  Together they must give the oracle's backward of the whole
+    sequence: per-element gradients and dB / dC block by block, dA_log, dD and
+    the bias gradient as the sum of the two blocks."""
+    L1, L2 = 320, 208
+    x = workloads.make_scan_inputs(2, 19, L1 + L2, 16, io, seed=83, d_mode="normal")
+    dout = _dout(x, 83)
+    whole = _oracle_bwd(x, dout)
+    part = lambda t, lo, hi: None if t is None else t[..., lo:hi].contiguous()
+    rows = lambda t, lo, hi: t[:, lo:hi].contiguous()
+    x1 = dict(x, u=part(x["u"], 0, L1), delta=part(x["delta"], 0, L1), z=part(x["z"], 0, L1),
+              B=rows(x["B"], 0, L1), C=rows(x["C"], 0, L1))
+    x2 = dict(x, u=part(x["u"], L1, None), delta=part(x["delta"], L1, None),
+              z=part(x["z"], L1, None), B=rows(x["B"], L1, None), C=rows(x["C"], L1, None))
+    xd1 = to_device(x1, cuda)
+    _, h1 = abi.mamba_selective_scan_fwd(xd1["u"], xd1["delta"], xd1["A_log"], xd1["B"],
+                                         xd1["C"], D=xd1["D"], z=xd1["z"],
+                                         delta_bias=xd1["delta_bias"])
+    torch.cuda.synchronize()
+    h1 = h1.cpu()
+    g2 = _bwd_ex(x2, part(dout, L1, None), cuda, h1, None)
+    g1 = _bwd_ex(x1, part(dout, 0, L1), cuda, None, None,
+                 dlast_state=torch.from_numpy(g2["dh0"]).to(cuda))
+    got = {k: np.concatenate([g1[k], g2[k]], axis=-1) for k in PER_ELEMENT}
+    got.update({k: np.concatenate([g1[k], g2[k]], axis=1) for k in ("dB", "dC")})
+    got.update({k: g1[k] + g2[k] for k in ("dA_log", "dD", "ddelta_bias")})
+    _assert_grads(x, got, {k: whole[k] for k in got}, what="two blocks")
+
+
+def test_final_state_gradient_of_an_empty_sequence_is_dh0(cuda):
+    """No steps: the final state is h0, so dh0 equals the final-state gradient."""
+    x = workloads.make_scan_inputs(2, 5, 0, 16, "f32", seed=84)
+    dlast = torch.randn((2, 5, 16), generator=torch.Generator().manual_seed(84))
+    g = _bwd_ex(x, torch.zeros(x["u"].shape), cuda, torch.zeros((2, 5, 16)), None,
+                dlast_state=dlast.to(cuda))
+    assert np.array_equal(g["dh0"], dlast.numpy())
