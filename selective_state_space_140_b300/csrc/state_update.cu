@@ -109,34 +109,35 @@ cudaError_t launch(const StateUpdateArgs& a, cudaStream_t stream) {
 
 // ---- bulk-copy ring path ------------------------------------------------
 // One 16-byte state access per thread keeps too few bytes in flight for the
-// HBM.  Here a persistent CTA of 256 threads walks tiles of TC = 4096 / N
-// chains of one batch row (16 KB of state); thread 0 keeps S = 2 tiles in
-// flight as bulk copies (cp.async.bulk: the state rows, the tile's A_log, bias
-// and D rows and its dt, x and z) into a shared-memory ring completed on
-// mbarriers.  B and C of the batch are loaded before a tile's copy is waited
-// for; each pass is then arithmetic on shared memory, and the new state is
-// stored straight to global memory.
+// HBM.  Here persistent CTAs of 256 threads walk tiles of TC = 4096 / N
+// chains (16 KB of state) of one channel block: CTA c owns channel block
+// c mod T1 (and every T1-th block after it when there are more blocks than
+// CTAs) and, within it, the batch rows c / T1, c / T1 + R, ...  A_log, the
+// bias and D do not depend on the batch row, so A * log2 e, the bias and D of
+// the thread's chains stay in registers while the CTA walks its batch rows,
+// and the copies carry only what changes per tile: thread 0 keeps S tiles in
+// flight as bulk copies (cp.async.bulk: the state rows and the tile's dt, x
+// and z) into a shared-memory ring completed on mbarriers.  B and C of the
+// batch row are loaded before a tile's copy is waited for; each pass is then
+// arithmetic on shared memory, and the new state is stored straight to
+// global memory.
 constexpr int kRingTileBytes = 16384;
 
-// Stage layout: state rows | A_log rows | dt | x | z | bias | D (each 16-byte
-// multiple).  A tile lies inside one batch row, so the A_log, bias and D rows
-// of its channels are contiguous too.
+// Stage layout: state rows | dt | x | z (each a 16-byte multiple).
 template <typename io_t, int G>
 struct RingCfg {
     static constexpr int NPL = 4, N = NPL * G, TC = kRingTileBytes / (N * 4), CPP = 256 / G;
-    static constexpr int PASSES = TC / CPP, ES = sizeof(io_t), S = 2;
+    static constexpr int PASSES = TC / CPP, ES = sizeof(io_t), S = 3;
     static constexpr int kIoBytes = TC * ES;  // dt, x or z of one tile
-    static constexpr int kParBytes = TC * 4;  // bias or D of one tile
-    static constexpr int kA = kRingTileBytes, kDt = 2 * kRingTileBytes, kX = kDt + kIoBytes;
-    static constexpr int kZ = kX + kIoBytes, kBias = kZ + kIoBytes, kD = kBias + kParBytes;
-    static constexpr int kStage = kD + kParBytes;
+    static constexpr int kDt = kRingTileBytes, kX = kDt + kIoBytes, kZ = kX + kIoBytes;
+    static constexpr int kStage = (kZ + kIoBytes + 127) / 128 * 128;
     static constexpr int kSmem = 128 + S * kStage;
     static_assert(PASSES * CPP == TC && kIoBytes % 16 == 0, "tile shape");
 };
 
 template <typename io_t, int G>
-__global__ void __launch_bounds__(256, 4) state_update_ring_kernel(StateUpdateArgs p,
-                                                                   int64_t ntiles) {
+__global__ void __launch_bounds__(256, 3) state_update_ring_kernel(StateUpdateArgs p, int T1,
+                                                                   int R) {
     using C = RingCfg<io_t, G>;
     constexpr int N = C::N, TC = C::TC, CPP = C::CPP, PASSES = C::PASSES, S = C::S;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -145,40 +146,61 @@ __global__ void __launch_bounds__(256, 4) state_update_ring_kernel(StateUpdateAr
     const int tid = threadIdx.x, g = tid % G, cl = tid / G;
     const bool has_z = p.z != nullptr;
 
-    const int64_t tiles_per_row = p.dim / TC;
-    auto issue = [&](int64_t tile, int st) {  // thread 0
-        const int64_t c0 = tile * TC;
-        const int64_t d0 = (tile % tiles_per_row) * TC;
+    // this CTA's tiles j = 0 .. njobs-1: channel block cb0 + (j / nb) * T1,
+    // batch row b0 + (j % nb) * R
+    const int64_t tpr = p.dim / TC;  // channel blocks per batch row
+    const int64_t cb0 = blockIdx.x % T1, b0 = blockIdx.x / T1;
+    const int64_t nb = b0 < p.batch ? (p.batch - b0 + R - 1) / R : 0;
+    const int64_t ncb = cb0 < tpr ? (tpr - cb0 + T1 - 1) / T1 : 0;
+    const int64_t njobs = nb * ncb;
+    auto tile_cb = [&](int64_t j) { return cb0 + (j / nb) * T1; };
+    auto tile_b = [&](int64_t j) { return b0 + (j % nb) * R; };
+    auto issue = [&](int64_t j, int st) {  // thread 0
+        const int64_t c0 = tile_b(j) * p.dim + tile_cb(j) * TC;  // first chain of the tile
         unsigned char* sp = stage(st);
-        const uint32_t bytes = 2 * kRingTileBytes + (has_z ? 3 : 2) * C::kIoBytes +
-                               (p.dt_bias ? C::kParBytes : 0) + (p.D ? C::kParBytes : 0);
-        mbar_arrive_expect_tx(&bar[st], bytes);
+        mbar_arrive_expect_tx(&bar[st], kRingTileBytes + (has_z ? 3 : 2) * C::kIoBytes);
         bulk_g2s(sp, p.state + c0 * N, kRingTileBytes, &bar[st]);
-        bulk_g2s(sp + C::kA, p.A_log + d0 * N, kRingTileBytes, &bar[st]);
         bulk_g2s(sp + C::kDt, static_cast<const io_t*>(p.dt) + c0, C::kIoBytes, &bar[st]);
         bulk_g2s(sp + C::kX, static_cast<const io_t*>(p.x) + c0, C::kIoBytes, &bar[st]);
         if (has_z) bulk_g2s(sp + C::kZ, static_cast<const io_t*>(p.z) + c0, C::kIoBytes, &bar[st]);
-        if (p.dt_bias) bulk_g2s(sp + C::kBias, p.dt_bias + d0, C::kParBytes, &bar[st]);
-        if (p.D) bulk_g2s(sp + C::kD, p.D + d0, C::kParBytes, &bar[st]);
     };
     if (tid == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);  // (S <= 16 fit in 128 bytes)
         fence_mbar_init();
-        for (int s = 0; s < S; ++s) {
-            const int64_t tile = blockIdx.x + int64_t(s) * gridDim.x;
-            if (tile < ntiles) issue(tile, s);
-        }
+        for (int s = 0; s < S && s < njobs; ++s) issue(s, s);
     }
     __syncthreads();
 
     const unsigned lane = tid & 31u;
     const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane / G * G));
     bool failed = false;
-    int j = 0;
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++j) {
-        const int st = j % S;
-        // ---- B and C of the batch first: they do not depend on the copy ----
-        const int64_t b = tile / tiles_per_row;
+    // per-channel parameters of the thread's chain in each pass, for the
+    // current channel block (A2 = A * log2 e, A = -exp(A_log) = -2^(A_log log2 e))
+    float A2[PASSES][4], bias[PASSES], Dd[PASSES];
+    float bias_e = 0.f, D_e = 0.f;  // of the chain whose per-chain work this lane does (G >= PASSES)
+    int64_t cur_cb = -1;
+    for (int64_t j = 0; j < njobs; ++j) {
+        const int st = int(j % S);
+        const int64_t b = tile_b(j), cb = tile_cb(j);
+        if (cb != cur_cb) {
+            cur_cb = cb;
+#pragma unroll
+            for (int ps = 0; ps < PASSES; ++ps) {
+                const int64_t d = cb * TC + ps * CPP + cl;
+                const float4 al = __ldg(reinterpret_cast<const float4*>(p.A_log + d * N) + g);
+                const float av[4] = {al.x, al.y, al.z, al.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) A2[ps][i] = -ex2_approx(av[i] * kLog2e) * kLog2e;
+                bias[ps] = p.dt_bias ? __ldg(p.dt_bias + d) : 0.f;
+                Dd[ps] = p.D ? __ldg(p.D + d) : 0.f;
+            }
+            if constexpr (G >= PASSES) {
+                const int64_t d = cb * TC + (g < PASSES ? g : 0) * CPP + cl;
+                bias_e = p.dt_bias ? __ldg(p.dt_bias + d) : 0.f;
+                D_e = p.D ? __ldg(p.D + d) : 0.f;
+            }
+        }
+        // ---- B and C of the batch row first: they do not depend on the copy ----
         float Bv[4], Cv[4];
         {
             const io_t* Bb = static_cast<const io_t*>(p.B) + b * N + g * 4;
@@ -203,20 +225,59 @@ __global__ void __launch_bounds__(256, 4) state_update_ring_kernel(StateUpdateAr
             atomicOr(&g_decode_error, kErrWaitTimeout);
         }
         const unsigned char* sp = stage(st);
-        const float4* sA = reinterpret_cast<const float4*>(sp + C::kA);
         const io_t* sdt = reinterpret_cast<const io_t*>(sp + C::kDt);
         const io_t* sx = reinterpret_cast<const io_t*>(sp + C::kX);
         const io_t* sz = reinterpret_cast<const io_t*>(sp + C::kZ);
-        const float* sbias = reinterpret_cast<const float*>(sp + C::kBias);
-        const float* sD = reinterpret_cast<const float*>(sp + C::kD);
+        const int64_t c0 = b * p.dim + cb * TC;
+        if constexpr (G >= PASSES) {
+            // Lane g < PASSES of a chain group does the per-chain work of pass g
+            // (dt, dt * x, skip, gate, store); dt and dt * x reach the group's
+            // lanes by shuffles, and every lane updates its 4 states of each pass.
+            const int ge = g < PASSES ? g : 0, local_e = ge * CPP + cl;
+            const float raw = float(sdt[local_e]) + bias_e;
+            const float x_e = float(sx[local_e]);
+            const float dt_e = !p.softplus ? raw : sizeof(io_t) == 2 ? softplus_fast(raw)
+                                                                       : softplus_accurate(raw);
+            const float dx_e = dt_e * x_e;
+            float acc[PASSES];
+#pragma unroll
+            for (int ps = 0; ps < PASSES; ++ps) {
+                const int local = ps * CPP + cl;
+                const float dt = __shfl_sync(gmask, dt_e, ps, G);
+                const float dx = __shfl_sync(gmask, dx_e, ps, G);
+                const float4 hv = reinterpret_cast<const float4*>(sp)[local * G + g];
+                float h[4] = {hv.x, hv.y, hv.z, hv.w};
+                float a = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    h[i] = fmaf(ex2_approx(dt * A2[ps][i]), h[i], dx * Bv[i]);
+                    a = fmaf(Cv[i], h[i], a);
+                }
+                reinterpret_cast<float4*>(p.state + (c0 + local) * N)[g] =
+                    make_float4(h[0], h[1], h[2], h[3]);
+                acc[ps] = a;
+            }
+#pragma unroll
+            for (int ps = 0; ps < PASSES; ++ps)
+#pragma unroll
+                for (int off = G / 2; off > 0; off /= 2)
+                    acc[ps] += __shfl_xor_sync(gmask, acc[ps], off, G);
+            if (g < PASSES) {
+                float tot = acc[0];
+#pragma unroll
+                for (int ps = 1; ps < PASSES; ++ps)
+                    if (g == ps) tot = acc[ps];
+                if (p.D) tot = fmaf(D_e, x_e, tot);
+                if (has_z) tot *= silu_fast(float(sz[local_e]));
+                Io<io_t>::store(static_cast<io_t*>(p.out) + c0 + local_e, tot);
+            }
+        } else {
 #pragma unroll
         for (int ps = 0; ps < PASSES; ++ps) {
             const int local = ps * CPP + cl;
-            const int64_t chain = tile * TC + local;
+            const int64_t chain = c0 + local;
             const float4 hv = reinterpret_cast<const float4*>(sp)[local * G + g];
-            const float4 av = sA[local * G + g];
-            const float A[4] = {av.x, av.y, av.z, av.w};
-            const float raw = float(sdt[local]) + (p.dt_bias ? sbias[local] : 0.f);
+            const float raw = float(sdt[local]) + bias[ps];
             const float x = float(sx[local]);
             const float dt = !p.softplus ? raw : sizeof(io_t) == 2 ? softplus_fast(raw)
                                                                      : softplus_accurate(raw);
@@ -225,24 +286,23 @@ __global__ void __launch_bounds__(256, 4) state_update_ring_kernel(StateUpdateAr
             float acc = 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                // A = -exp(A_log) = -2^(A_log * log2 e); Abar = 2^(dt * A * log2 e)
-                const float A2 = -ex2_approx(A[i] * kLog2e) * kLog2e;
-                h[i] = fmaf(ex2_approx(dt * A2), h[i], dx * Bv[i]);
+                h[i] = fmaf(ex2_approx(dt * A2[ps][i]), h[i], dx * Bv[i]);
                 acc = fmaf(Cv[i], h[i], acc);
             }
             reinterpret_cast<float4*>(p.state + chain * N)[g] = make_float4(h[0], h[1], h[2], h[3]);
 #pragma unroll
             for (int off = G / 2; off > 0; off /= 2) acc += __shfl_xor_sync(gmask, acc, off, G);
             if (g == 0) {
-                if (p.D) acc = fmaf(sD[local], x, acc);
+                if (p.D) acc = fmaf(Dd[ps], x, acc);
                 if (has_z) acc *= silu_fast(float(sz[local]));
                 Io<io_t>::store(static_cast<io_t*>(p.out) + chain, acc);
             }
         }
+        }
         __syncthreads();  // every thread is done with this stage
-        if (tid == 0 && tile + int64_t(S) * gridDim.x < ntiles) {
+        if (tid == 0 && j + S < njobs) {
             fence_proxy_async_smem();
-            issue(tile + int64_t(S) * gridDim.x, st);
+            issue(j + S, st);
         }
     }
 }
@@ -256,27 +316,31 @@ bool try_ring(const StateUpdateArgs& a, cudaStream_t stream, cudaError_t* err) {
         return q == nullptr || reinterpret_cast<uintptr_t>(q) % n == 0;
     };
     if (a.dstate != C::N || a.dim % C::TC != 0 || !al(a.state, 16) || !al(a.A_log, 16) ||
-        !al(a.dt, 16) || !al(a.x, 16) || !al(a.z, 16) || !al(a.dt_bias, 16) || !al(a.D, 16) ||
-        !al(a.B, 4 * C::ES) || !al(a.C, 4 * C::ES))
+        !al(a.dt, 16) || !al(a.x, 16) || !al(a.z, 16) || !al(a.B, 4 * C::ES) ||
+        !al(a.C, 4 * C::ES) || a.batch > 0x7fffffff)
         return false;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return false;
-    const int64_t ntiles = a.batch * a.dim / C::TC;
+    auto kern = state_update_ring_kernel<io_t, G>;
     int per_sm = 0;
-    if (cudaFuncSetAttribute(state_update_ring_kernel<io_t, G>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, state_update_ring_kernel<io_t, G>,
-                                                      256, C::kSmem) != cudaSuccess ||
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, C::kSmem) !=
+            cudaSuccess ||
         per_sm < 1)
         return false;
-    const int64_t slots = int64_t(sms) * per_sm;  // one persistent CTA per slot
-    const int64_t grid = ntiles < slots ? ntiles : slots;
-    auto kern = state_update_ring_kernel<io_t, G>;
-    *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (*err != cudaSuccess) return true;
-    kern<<<unsigned(grid), 256, C::kSmem, stream>>>(a, ntiles);
+    // One persistent CTA per slot: T1 channel-block columns x R batch strides.
+    const int64_t slots = int64_t(sms) * per_sm, tpr = a.dim / C::TC;
+    int64_t T1 = tpr, R = 1;
+    if (tpr <= slots) {
+        R = slots / tpr;
+        if (R > a.batch) R = a.batch;
+    } else {
+        T1 = slots;
+    }
+    kern<<<unsigned(T1 * R), 256, C::kSmem, stream>>>(a, int(T1), int(R));
     *err = cudaGetLastError();
     return true;
 }
