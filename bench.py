@@ -377,11 +377,19 @@ def cpu_oracle_rate(cfg, x, seconds: float):
     of the workload sized to take about `seconds`."""
     import oracle
 
-    nb, k = choose_sample(cfg, x, seconds)
+    # A sample of about a third of the budget, timed three times over: a
+    # single sub-second call runs at the host's boost clock, a sustained
+    # all-core load (what the reference arm times, many calls in a row) does
+    # not, so the rate reported is the sustained one and the first call is
+    # kept beside it.
+    nb, k = choose_sample(cfg, x, seconds / 3)
     a, kw, chains, what = _oracle_sample(cfg, x, nb, k)
-    t0 = time.perf_counter()
-    _, _, used = oracle.selective_scan(*a, nthreads=0, **kw)
-    dt = time.perf_counter() - t0
+    times = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        _, _, used = oracle.selective_scan(*a, nthreads=0, **kw)
+        times.append(time.perf_counter() - t0)
+    dt = sum(times) / len(times)
     updates = chains * cfg.seqlen * cfg.dstate
     # the same oracle on one core, over channels of batch 0, for about a third
     # of the time budget
@@ -394,7 +402,9 @@ def cpu_oracle_rate(cfg, x, seconds: float):
     updates1 = chains1 * cfg.seqlen * cfg.dstate
     return {"value": updates / dt, "unit": UNIT, "cores": used, "kind": "oracle",
             "sample": f"fp64 oracle over {what}, full L={cfg.seqlen}, N={cfg.dstate} "
-                      f"({updates:.3g} updates in {dt:.2f} s)",
+                      f"({updates:.3g} updates per call, 3 calls in a row, "
+                      f"{sum(times):.2f} s in all)",
+            "first_call": updates / times[0],
             "one_core": {"value": updates1 / dt1, "unit": UNIT, "cores": 1,
                          "sample": f"fp64 oracle over {what1}, full L={cfg.seqlen} "
                                    f"({updates1:.3g} updates in {dt1:.2f} s)"}}
@@ -592,7 +602,8 @@ def bench_ex(args, cnt, xd, y, h, sfu, stream) -> dict:
             "us_per_step": round(t * 1e6, 1), "state_updates_per_s": cnt["updates"] / t,
             "roofline": {"bound": "alu", "achieved": round(cnt["exps"] / t / 1e9, 1),
                          "peak": round(sfu["ex2_per_s"] / 1e9, 1), "unit": "Gexp/s",
-                         "frac": round(cnt["exps"] / t / sfu["ex2_per_s"], 4), "traffic": None},
+                         "frac": round(cnt["exps"] / t / sfu["ex2_per_s"], 4),
+                         "traffic": stored_traffic("ex_" + args.workload, kernel_source_hash())},
             "steps": steps, "gpu_launches": steps}
 
 
@@ -830,9 +841,30 @@ def bench_e2e(args, cfg, x, device, world) -> dict:
             ev[("out", i)] = torch.cuda.Event()
             ev[("out", i)].record(s_out)
 
+    # the same host<->device copies alone (pinned memory, the streams above):
+    # the link's rate, against which the end-to-end step is copy-bound
+    def copies_alone(reps=5):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            with torch.cuda.stream(s_in):
+                for k in names:
+                    dev[0][k].copy_(host[k], non_blocking=True)
+        torch.cuda.synchronize()
+        t_in = (time.perf_counter() - t0) / reps
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            with torch.cuda.stream(s_out):
+                y_h[0].copy_(y_d[0], non_blocking=True)
+                h_h[0].copy_(h_d[0], non_blocking=True)
+        torch.cuda.synchronize()
+        t_out = (time.perf_counter() - t0) / reps
+        return {"h2d_gbs": round(h2d / t_in / 1e9, 2), "d2h_gbs": round(d2h / t_out / 1e9, 2)}
+
     for i in range(2):
         step(i)
     torch.cuda.synchronize()
+    link = copies_alone()
     ev.clear()
     steps = max(3, min(args.steps, args.e2e_steps))
     barrier(world)
@@ -847,6 +879,7 @@ def bench_e2e(args, cfg, x, device, world) -> dict:
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(t / steps * 1e3, 3),
             "api": "selective_state_space_140_b300.abi.mamba_selective_scan_fwd (C ABI)",
             "pipelining": "copy-in, scan and copy-out streams, two buffer sets",
+            "copies_alone": link,
             "note": "A_log, D and bias are parameters kept on the device"}
 
 
