@@ -193,7 +193,7 @@ __device__ __forceinline__ void chain_product(const float* sm, const float4* S, 
 // EX: h0, document resets and dh0 are handled (compiled separately so that the
 // plain backward's code is unchanged by them).
 template <typename io_t, int NPL, int G, int UA, int MODE, bool EX>
-__global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const int dblocks,
+__global__ void __launch_bounds__(kBNTH, NPL == 4 ? 8 : 1) scan_bwd_kernel(const BwdArgs a, const int dblocks,
                                                          const bool vec_red) {
     using C = BwdCfg<io_t, NPL, G>;
     constexpr int T = C::T, NTH = C::NTH, CH = C::CH, NP = C::NP, NQ = C::NQ, S = C::kS;
@@ -241,6 +241,14 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
         if (MODE == kBwdFull && chain_ok && n < N)
             h_in = hsg ? hsg[n] : ((EX && p.h0) ? p.h0[chain * N + n] : 0.f);
         h[i] = h_in;
+    }
+    // the same as pairs of states, for the packed f32x2 arithmetic of the reverse phase
+    constexpr int NH = NPL / 2;
+    f32x2 Ap[NH], A2p[NH];
+#pragma unroll
+    for (int q = 0; q < NH; ++q) {
+        Ap[q] = pack2(A[2 * q], A[2 * q + 1]);
+        A2p[q] = pack2(A2[2 * q], A2[2 * q + 1]);
     }
     float dtsum = 0.f;  // summary: sum of the decay steps over the segment
     const bool has_reset = EX && p.reset != nullptr;
@@ -384,25 +392,43 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
         // recompute the chunk's states into shared memory; C.h summed over the
         // chain's lanes by a butterfly per step
         {
-            float hh[NPL];
+            // states in pairs (packed f32x2), B and C of the lane's states as float4
+            f32x2 hh[NH];
 #pragma unroll
-            for (int i = 0; i < NPL; ++i) hh[i] = hs[i];
+            for (int q = 0; q < NH; ++q) hh[q] = pack2(hs[2 * q], hs[2 * q + 1]);
 #pragma unroll
             for (int t = 0; t < T; ++t) {
                 const float dt = sm[C::oDt + t * S + c];
                 const float du = dt * sm[C::oU + t * S + c];
                 const float de = has_reset ? sm[C::oDe + t * S + c] : dt;
-                float acc = 0.f;
+                const float4* Bt = reinterpret_cast<const float4*>(sm + C::oB + t * NP + g * NPL);
+                const float4* Ct = reinterpret_cast<const float4*>(sm + C::oC + t * NP + g * NPL);
+                const f32x2 des = pack2(de, de), dus = pack2(du, du);
+                f32x2 acc2 = pack2(0.f, 0.f);
 #pragma unroll
-                for (int i = 0; i < NPL; ++i) {
-                    const int n = g * NPL + i;
-                    hh[i] = fmaf(ex2_approx(de * A2[i]), hh[i], du * sm[C::oB + t * NP + n]);
-                    acc = fmaf(sm[C::oC + t * NP + n], hh[i], acc);
+                for (int v = 0; v < NQ; ++v) {
+                    const float4 bv = Bt[v], cv = Ct[v];
+                    const f32x2 bq[2] = {pack2(bv.x, bv.y), pack2(bv.z, bv.w)};
+                    const f32x2 cq[2] = {pack2(cv.x, cv.y), pack2(cv.z, cv.w)};
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int q = 2 * v + e;
+                        float x0, x1;
+                        unpack2(mul2(des, A2p[q]), x0, x1);
+                        hh[q] = fma2(pack2(ex2_approx(x0), ex2_approx(x1)), hh[q], mul2(dus, bq[e]));
+                        acc2 = fma2(cq[e], hh[q], acc2);
+                    }
                 }
+                float acc_lo, acc_hi;
+                unpack2(acc2, acc_lo, acc_hi);
+                float acc = acc_lo + acc_hi;
 #pragma unroll
-                for (int q = 0; q < NQ; ++q)
-                    sH[(t * NQ + q) * NTH + tid] =
-                        make_float4(hh[4 * q], hh[4 * q + 1], hh[4 * q + 2], hh[4 * q + 3]);
+                for (int v = 0; v < NQ; ++v) {
+                    float h0v, h1v, h2v, h3v;
+                    unpack2(hh[2 * v], h0v, h1v);
+                    unpack2(hh[2 * v + 1], h2v, h3v);
+                    sH[(t * NQ + v) * NTH + tid] = make_float4(h0v, h1v, h2v, h3v);
+                }
 #pragma unroll
                 for (int off = G / 2; off > 0; off /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, off);
                 if (g == 0) sm[C::oYs + t * S + c] = acc;
@@ -436,40 +462,55 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
 
         // adjoint, backwards through the chunk; g_t replaces h_t in the tile
         // once step t has read it (step t-1 reads only h_{t-1} and h_{t-2})
+        // packed f32x2 over pairs of states; gc and dA as pairs during the sweep
+        f32x2 gcp[NH], dAp[NH];
+#pragma unroll
+        for (int q = 0; q < NH; ++q) {
+            gcp[q] = pack2(gc[2 * q], gc[2 * q + 1]);
+            dAp[q] = pack2(dA[2 * q], dA[2 * q + 1]);
+        }
 #pragma unroll UA
         for (int t = T - 1; t >= 0; --t) {
             const int s = t * S + c;
             const float dy = sm[C::oDy + s], dt = sm[C::oDt + s], u = sm[C::oU + s];
             const float de = has_reset ? sm[C::oDe + s] : dt;  // Abar = 0 at a document start
-            float hp[NPL];
+            const float4* Bt = reinterpret_cast<const float4*>(sm + C::oB + t * NP + g * NPL);
+            const float4* Ct = reinterpret_cast<const float4*>(sm + C::oC + t * NP + g * NPL);
+            const f32x2 des = pack2(de, de), dys = pack2(dy, dy), dts = pack2(dt, dt);
+            f32x2 gu2 = pack2(0.f, 0.f), gd2 = pack2(0.f, 0.f);
 #pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-                if (t > 0) {
-                    const float4 vp = sH[((t - 1) * NQ + q) * NTH + tid];
-                    hp[4 * q] = vp.x; hp[4 * q + 1] = vp.y; hp[4 * q + 2] = vp.z; hp[4 * q + 3] = vp.w;
-                } else {
+            for (int v = 0; v < NQ; ++v) {
+                const float4 hv = t > 0 ? sH[((t - 1) * NQ + v) * NTH + tid]
+                                        : make_float4(hs[4 * v], hs[4 * v + 1], hs[4 * v + 2],
+                                                      hs[4 * v + 3]);
+                const float4 bv = Bt[v], cv = Ct[v];
+                const f32x2 hq[2] = {pack2(hv.x, hv.y), pack2(hv.z, hv.w)};
+                const f32x2 bq[2] = {pack2(bv.x, bv.y), pack2(bv.z, bv.w)};
+                const f32x2 cq[2] = {pack2(cv.x, cv.y), pack2(cv.z, cv.w)};
+                f32x2 gq[2];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) hp[4 * q + e] = hs[4 * q + e];
+                for (int e = 0; e < 2; ++e) {
+                    const int q = 2 * v + e;
+                    float x0, x1;
+                    unpack2(mul2(des, A2p[q]), x0, x1);
+                    const f32x2 ab = pack2(ex2_approx(x0), ex2_approx(x1));
+                    const f32x2 gn = fma2(dys, cq[e], gcp[q]);
+                    const f32x2 w = mul2(gn, mul2(ab, hq[e]));
+                    gq[e] = gn;
+                    gu2 = fma2(gn, bq[e], gu2);
+                    gd2 = fma2(Ap[q], w, gd2);
+                    dAp[q] = fma2(dts, w, dAp[q]);
+                    gcp[q] = mul2(ab, gn);
                 }
+                float g0, g1, g2, g3;
+                unpack2(gq[0], g0, g1);
+                unpack2(gq[1], g2, g3);
+                sH[(t * NQ + v) * NTH + tid] = make_float4(g0, g1, g2, g3);
             }
-            float gu = 0.f, gd = 0.f, gv[NPL];
-#pragma unroll
-            for (int i = 0; i < NPL; ++i) {
-                const int n = g * NPL + i;
-                const float Bn = sm[C::oB + t * NP + n], Cn = sm[C::oC + t * NP + n];
-                const float ab = ex2_approx(de * A2[i]);
-                const float gn = fmaf(dy, Cn, gc[i]);
-                const float w = gn * (ab * hp[i]);
-                gv[i] = gn;
-                gu = fmaf(gn, Bn, gu);
-                gd = fmaf(A[i], w, gd);
-                dA[i] = fmaf(dt, w, dA[i]);
-                gc[i] = ab * gn;
-            }
-#pragma unroll
-            for (int q = 0; q < NQ; ++q)
-                sH[(t * NQ + q) * NTH + tid] =
-                    make_float4(gv[4 * q], gv[4 * q + 1], gv[4 * q + 2], gv[4 * q + 3]);
+            float gu_lo, gu_hi, gd_lo, gd_hi;
+            unpack2(gu2, gu_lo, gu_hi);
+            unpack2(gd2, gd_lo, gd_hi);
+            float gu = gu_lo + gu_hi, gd = gd_lo + gd_hi;
             gd = fmaf(u, gu, gd);  // sum_n g (A Abar h_{t-1} + u B)
 #pragma unroll
             for (int off = G / 2; off > 0; off /= 2) {
@@ -480,6 +521,11 @@ __global__ void __launch_bounds__(kBNTH) scan_bwd_kernel(const BwdArgs a, const 
                 sm[C::oGu + s] = gu;
                 sm[C::oGdt + s] = gd;
             }
+        }
+#pragma unroll
+        for (int q = 0; q < NH; ++q) {
+            unpack2(gcp[q], gc[2 * q], gc[2 * q + 1]);
+            unpack2(dAp[q], dA[2 * q], dA[2 * q + 1]);
         }
         __syncthreads();
 
