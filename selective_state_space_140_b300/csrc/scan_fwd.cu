@@ -754,7 +754,10 @@ constexpr int kBarDone = 3;   // + (chunk & 1): recurrence of the chunk done
 //   state, writing only the state at its end and the sum of its dt (no y).
 constexpr int kScanFull = 0, kScanSummary = 1;
 
-template <typename io_t, int P, int NPL, int G, int NR, int NE, int MINB, int MODE>
+// FAST: the gate z is given, softplus is on, and there is no h0 and no reset
+// mask (the common case, compiled without their run-time tests).
+template <typename io_t, int P, int NPL, int G, int NR, int NE, int MINB, int MODE,
+          bool FAST = false>
 __global__ void __launch_bounds__(NR + NE, MINB)
     scan_ws_kernel(const ScanArgs p, const __grid_constant__ CUtensorMap tm_u,
                    const __grid_constant__ CUtensorMap tm_d,
@@ -787,7 +790,7 @@ __global__ void __launch_bounds__(NR + NE, MINB)
     const int tid = threadIdx.x;
     const int nchunks = (Ls + T - 1) / T;
     const int row0 = int(int64_t(b) * dim + d0);
-    const bool has_z = MODE == kScanFull && p.z != nullptr;
+    const bool has_z = FAST || (MODE == kScanFull && p.z != nullptr);
     const io_t* Bg = static_cast<const io_t*>(p.B) + (int64_t(b) * L + t0) * N;
     const io_t* Cg = static_cast<const io_t*>(p.C) + (int64_t(b) * L + t0) * N;
     auto chunk_len = [&](int k) { return Ls - k * T < T ? Ls - k * T : T; };
@@ -830,7 +833,7 @@ __global__ void __launch_bounds__(NR + NE, MINB)
                 const int64_t chain = int64_t(b) * dim + d0 + cc[q];
                 if (sg.hcarry)  // split: the carry pass left the entering state in slot tseg
                     load_state<NPL, G>(sg.hcarry + (chain * sg.nseg + tseg) * N, N, g, h[q]);
-                else if (p.h0)
+                else if (!FAST && p.h0)
                     load_state<NPL, G>(p.h0 + chain * N, N, g, h[q]);
             }
         }
@@ -922,7 +925,7 @@ __global__ void __launch_bounds__(NR + NE, MINB)
         // document boundaries of this lane's PV steps: one byte each (4-byte
         // aligned: the row length and every offset are multiples of 4)
         uint32_t rsw = 0;
-        if (kp >= 0 && p.reset && seg * PV < chunk_len(kp))
+        if (!FAST && kp >= 0 && p.reset && seg * PV < chunk_len(kp))
             rsw = __ldg(reinterpret_cast<const uint32_t*>(p.reset + int64_t(b) * L + t0 +
                                                           kp * T + seg * PV));
         if (kp >= 0) {
@@ -971,7 +974,7 @@ __global__ void __launch_bounds__(NR + NE, MINB)
 #pragma unroll
                 for (int e = 0; e < PV; ++e) {
                     float dt = __fadd_rn(io_elem<io_t>(pd[i], e), bias[i]);
-                    if (p.softplus) dt = softplus_io<io_t>(dt);
+                    if (FAST || p.softplus) dt = softplus_io<io_t>(dt);
                     const float du = __fmul_rn(dt, io_elem<io_t>(pu[i], e));
                     // exponent lanes of a step that starts a document: +inf
                     const float de = ((rsw >> (8 * e)) & 0xffu) ? kResetDt : dt;
@@ -1728,7 +1731,8 @@ bool ws_ok(const ScanArgs& a) {
            a.seqlen <= 0x7fffffff;
 }
 
-template <typename io_t, int P, int NPL, int G, int NR, int NE, int MINB, int MODE>
+template <typename io_t, int P, int NPL, int G, int NR, int NE, int MINB, int MODE,
+          bool FAST = false>
 cudaError_t launch_ws(const ScanArgs& a, const SegArgs& sg, cudaStream_t stream) {
     using C = WsCfg<io_t, P, NPL, G, NR, NE>;
     CUtensorMap mu, md, mz;
@@ -1739,16 +1743,16 @@ cudaError_t launch_ws(const ScanArgs& a, const SegArgs& sg, cudaStream_t stream)
         !make_map(&mz, a.z ? a.z : a.u, bf, rows, a.seqlen, C::T, C::CW))
         return cudaErrorInvalidValue;
     const int64_t dblocks = (a.dim + C::CH - 1) / C::CH;
-    return launch(scan_ws_kernel<io_t, P, NPL, G, NR, NE, MINB, MODE>, C::kSmem,
+    return launch(scan_ws_kernel<io_t, P, NPL, G, NR, NE, MINB, MODE, FAST>, C::kSmem,
                   dblocks * a.batch * sg.grid_nseg, C::NTH, stream, a, mu, md, mz, int(dblocks),
                   sg);
 }
 
-template <typename io_t, int P, int NPL, int G, int NR, int NE, int MINB>
+template <typename io_t, int P, int NPL, int G, int NR, int NE, int MINB, bool FAST = false>
 bool try_ws(const ScanArgs& a, cudaStream_t stream, cudaError_t* err) {
     if (!ws_ok<io_t, P, NPL, G, NR, NE>(a) || a.seqlen == 0) return false;
     const SegArgs whole{int(a.seqlen), 1, 1, nullptr, nullptr};
-    *err = launch_ws<io_t, P, NPL, G, NR, NE, MINB, kScanFull>(a, whole, stream);
+    *err = launch_ws<io_t, P, NPL, G, NR, NE, MINB, kScanFull, FAST>(a, whole, stream);
     return *err != cudaErrorInvalidValue;  // tensor map refused: another path
 }
 
@@ -1913,6 +1917,10 @@ cudaError_t dispatch(const ScanArgs& a, cudaStream_t stream, const ScanScratch& 
         // Few chains and a long sequence: split the sequence (see try_ws_split).
         if ((tile == 0 || tile == 4) && N == 16 && !force_reg() &&
             try_ws_split<io_t>(a, stream, sc, &err))
+            return err;
+        const bool fast = a.z && a.softplus && !a.h0 && !a.reset;
+        if ((tile == 4 || tile == 0) && N == 16 && !force_reg() && fast &&
+            try_ws<io_t, 1, 8, 2, 64, 64, 4, true>(a, stream, &err))
             return err;
         if ((tile == 4 || tile == 0) && N == 16 && !force_reg() &&
             try_ws<io_t, 1, 8, 2, 64, 64, 4>(a, stream, &err))
