@@ -159,3 +159,20 @@ def test_beyond_a_million_tokens_in_one_launch_and_in_blocks(cuda):
         yb, _ = _gpu(blk, h0=state, reset=rd[:, t0:t1].contiguous(), last_state=state)
         ys.append(yb)
     _check(x, torch.cat(ys, dim=-1), state, yr, hr, "three streamed blocks")
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+@pytest.mark.parametrize("batch,dim,L,N", [(2, 128, 2048, 16), (1, 72, 1537, 16)])
+def test_zero_state_and_empty_mask_equal_the_stateless_scan(cuda, io, batch, dim, L, N):
+    """A zero h0 and an all-zero reset mask change nothing: the scan that is
+    given them (general tile) equals, bit for bit, the one that is not (the
+    tile compiled for a gated softplus scan without state or mask)."""
+    x = workloads.make_scan_inputs(batch, dim, L, N, io, seed=66, d_mode="normal")
+    xd = to_device(x, cuda)
+    y0, h0 = _gpu(xd)
+    zero = torch.zeros((batch, dim, N), device=cuda)
+    none = torch.zeros((batch, L), dtype=torch.uint8, device=cuda)
+    y1, h1 = _gpu(xd, h0=zero, reset=none)
+    assert torch.equal(y0, y1) and torch.equal(h0, h1)
+    y2, h2 = _gpu(xd, h0=zero)
+    assert torch.equal(y0, y2) and torch.equal(h0, h2)
