@@ -4,7 +4,7 @@ import pytest
 import torch
 
 from golden_io import load_tiny_f32
-from fp32_emulation import emulate_scan_f32
+from fp32_emulation import fp32_envelope
 from parity_util import (FINE_FLOOR, FINE_TOL, TOL, assert_full_size, full_size_errors, gpu_scan,
                          normwise, oracle_scan, rel_err, to_device)
 from selective_state_space_140_b300 import abi, workloads
@@ -219,24 +219,32 @@ def test_full_size_configs_every_chain(cuda, name):
     assert_full_size(cfg.io_dtype, errs, name)
 
 
+@pytest.mark.parametrize("split", ["planned", "unsplit"])
 @pytest.mark.parametrize("io,L", [("f32", 1000), ("f32", 4096), ("bf16", 4096)])
-def test_wide_range_a_log(cuda, io, L):
+def test_wide_range_a_log(cuda, io, L, split, monkeypatch):
     """|A| log-uniform over [1e-2, 1e2] per (channel, state), as a trained
     layer drifts: at small dt the decay Abar = 2^(dt * A * log2 e) comes within
     1e-5 of 1, where an error in the exponential is amplified by the state's
     memory 1/(1 - Abar).  The bound is the larger of the fixed one and twice
-    what correctly rounded fp32 arithmetic reaches on the same inputs
-    (fp32_emulation): slow states that keep their whole history are long fp32
-    running sums, which no fp32 evaluation holds to 1e-4 at L = 4096
-    (test_fp32_emulation.py)."""
+    what correctly rounded fp32 arithmetic reaches on the same inputs, taken
+    over four fp32 evaluations that differ only in rounding (fp32_envelope):
+    slow states that keep their whole history are long fp32 running sums,
+    which fp32 arithmetic with exponentials a few ulp off (as the GPU's are)
+    does not hold to 1e-4 at L = 4096, and the largest error on small
+    elements is one cancelling element's rounding noise, which spreads over a
+    factor of 2-3 between equally correct evaluations
+    (test_fp32_emulation.py).  These 96 chains take the time-split path as
+    planned, and the one-pass tile when the split is switched off."""
+    if split == "unsplit":
+        monkeypatch.setenv("MAMBA_SCAN_SEGMENTS", "1")
     x = workloads.make_scan_inputs(2, 48, L, 16, io, seed=78 + L, d_mode="normal")
     x["A_log"] = workloads.wide_a_log(48, 16, 78 + L)
     yg, hg = _run(x, cuda)
     yr, hr = oracle_scan(x)
-    ye, he = emulate_scan_f32(x, out_bf16=io == "bf16")
-    for what, g, r, e in (("y", yg, yr, ye), ("state", hg, hr, he)):
+    env = fp32_envelope(x, out_bf16=io == "bf16")
+    for what, g, r, k in (("y", yg, yr, 0), ("state", hg, hr, 1)):
         for floor, fixed in ((0.1, TOL[io]), (FINE_FLOOR, FINE_TOL[io])):
-            bound = max(fixed, 2 * rel_err(e, r, floor))
+            bound = max(fixed, 2 * max(rel_err(e[k], r, floor) for e in env))
             err = rel_err(g, r, floor)
             assert err <= bound, f"{what} at floor {floor}: {err:.3e} > {bound:.3e}"
 
@@ -244,14 +252,15 @@ def test_wide_range_a_log(cuda, io, L):
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 @pytest.mark.parametrize("L,dim", [(336, 50), (4096, 33), (333, 50)])
 def test_all_tile_shapes_give_the_same_scan(cuda, io, L, dim, monkeypatch):
-    """dstate = 16 has four tile shapes: one chain x 8 states per thread with
-    separate recurrence and element warps (default), the same without the
-    split, one chain x 4 states, two chains x 4 states.  Each must match the
-    oracle and the others (odd channel counts leave half-used pairs)."""
+    """dstate = 16 has several tile shapes: one chain x 8 states per thread
+    with separate recurrence and element warps (default; 32 chains per CTA, or
+    16 with one warp of each role), the same without the split, one chain x 4
+    states, two chains x 4 states.  Each must match the oracle and the others
+    (odd channel counts leave half-used pairs)."""
     x = workloads.make_scan_inputs(2, dim, L, 16, io, seed=16, d_mode="normal")
     yr, hr = oracle_scan(x)
     outs = []
-    for tile in ("0", "1", "2", "3", "4", "5", "6", "7"):
+    for tile in ("0", "1", "2", "3", "4", "5", "6", "7", "8"):
         monkeypatch.setenv("MAMBA_SCAN_TILE", tile)
         y, h = _run(x, cuda)
         _assert_close(x, y, h, yr, hr, what=f"tile {tile}")
