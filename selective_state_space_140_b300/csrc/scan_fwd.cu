@@ -573,7 +573,8 @@ struct WsCfg {
     static constexpr int SEGROW = T / PV;
     static constexpr int NSEG = CH * SEGROW;
     static constexpr int SPT = NSEG / NE;   // segments per element thread
-    static constexpr int CW = CH / (NE / 32);  // chains per element warp
+    static constexpr int EW = NE / 32;         // element warps
+    static constexpr int CW = CH / EW;         // chains per element warp
     static constexpr size_t rnd(size_t x) { return (x + 127) / 128 * 128; }
     static constexpr size_t kTile = rnd(size_t(CH) * T * ES);
     static constexpr size_t kRaw = rnd(size_t(T) * NP * ES);
@@ -589,7 +590,8 @@ struct WsCfg {
     using quad_t = std::conditional_t<ES == 2, uint2, uint4>;
     static_assert(NR % 32 == 0 && NE % 32 == 0, "roles are whole warps");
     static_assert(NSEG % NE == 0, "element threads share the segments evenly");
-    static_assert(NE == 64, "two element warps: one copies B, the other C");
+    static_assert(NE == 32 || NE == 64,
+                  "one element warp copies B and C, or two: one copies B, the other C");
     static_assert(CW * SEGROW == 32 * SPT, "an element warp covers its chains exactly");
     static_assert((T * NP * ES) % (32 * 16) == 0, "B and C split into 16-byte pieces per lane");
     static_assert((size_t(CW) * T * ES) % 128 == 0, "per-warp tile rows stay 128-byte aligned");
@@ -807,11 +809,16 @@ __global__ void __launch_bounds__(NR + NE, MINB)
         const uint32_t rows_bytes = uint32_t(CW) * T * C::ES;
         uint64_t* br = &bar[(k & (S - 1)) * 2 + w];
         unsigned char* st = stage(k) + w * rows_bytes;
-        mbar_arrive_expect_tx(br, (has_z ? 3 : 2) * rows_bytes + bc_bytes);
+        mbar_arrive_expect_tx(br, (has_z ? 3 : 2) * rows_bytes + (3 - C::EW) * bc_bytes);
         tma_load_2d(st, &tm_u, t0 + k * T, row0 + w * CW, br);
         tma_load_2d(st + C::kTile, &tm_d, t0 + k * T, row0 + w * CW, br);
         if (has_z) tma_load_2d(st + 2 * C::kTile, &tm_z, t0 + k * T, row0 + w * CW, br);
-        bulk_g2s(raw(k, w), (w == 0 ? Bg : Cg) + int64_t(k) * T * N, bc_bytes, br);
+        if (C::EW == 1) {
+            bulk_g2s(raw(k, 0), Bg + int64_t(k) * T * N, bc_bytes, br);
+            bulk_g2s(raw(k, 1), Cg + int64_t(k) * T * N, bc_bytes, br);
+        } else {
+            bulk_g2s(raw(k, w), (w == 0 ? Bg : Cg) + int64_t(k) * T * N, bc_bytes, br);
+        }
     };
 
     if (tid == NR) {
@@ -921,7 +928,8 @@ __global__ void __launch_bounds__(NR + NE, MINB)
             }
         }
         constexpr int BCV = T * NP * C::ES / 32 / 16;  // 16-byte pieces of B or C per lane
-        uint4 rbc[BCV];
+        constexpr int NBC = 3 - C::EW;                 // B and C, or the warp's one of them
+        uint4 rbc[NBC][BCV];
         // document boundaries of this lane's PV steps: one byte each (4-byte
         // aligned: the row length and every offset are multiples of 4)
         uint32_t rsw = 0;
@@ -937,9 +945,12 @@ __global__ void __launch_bounds__(NR + NE, MINB)
                 pd[i] = td[tq[i]];
                 pu[i] = tu[tq[i]];
             }
-            const uint4* rw = reinterpret_cast<const uint4*>(raw(kp, w));
 #pragma unroll
-            for (int r = 0; r < BCV; ++r) rbc[r] = rw[lane * BCV + r];
+            for (int x = 0; x < NBC; ++x) {
+                const uint4* rw = reinterpret_cast<const uint4*>(raw(kp, NBC == 2 ? x : w));
+#pragma unroll
+                for (int r = 0; r < BCV; ++r) rbc[x][r] = rw[lane * BCV + r];
+            }
         }
         // ---- finish chunk ke ----
         if (ke >= 0) {
@@ -1000,17 +1011,21 @@ __global__ void __launch_bounds__(NR + NE, MINB)
             for (int i = 0; i < SPT; ++i)
 #pragma unroll
                 for (int e = 0; e < PV; ++e) sdu[dub[i] + e * CH] = o[i][e];
-            // fp32 copy of this warp's B (w = 0) or C (w = 1)
-            float* dst = bcbuf(kp) + w * T * NP + lane * BCV * (16 / C::ES);
+            // fp32 copy of B and C (one element warp), or of this warp's B
+            // (w = 0) or C (w = 1)
 #pragma unroll
-            for (int r = 0; r < BCV; ++r) {
-                if constexpr (C::ES == 2) {
-                    reinterpret_cast<ulonglong2*>(dst)[2 * r] =
-                        make_ulonglong2(get_pair<io_t>(rbc[r], 0), get_pair<io_t>(rbc[r], 1));
-                    reinterpret_cast<ulonglong2*>(dst)[2 * r + 1] =
-                        make_ulonglong2(get_pair<io_t>(rbc[r], 2), get_pair<io_t>(rbc[r], 3));
-                } else {
-                    reinterpret_cast<uint4*>(dst)[r] = rbc[r];
+            for (int x = 0; x < NBC; ++x) {
+                float* dst = bcbuf(kp) + (NBC == 2 ? x : w) * T * NP + lane * BCV * (16 / C::ES);
+#pragma unroll
+                for (int r = 0; r < BCV; ++r) {
+                    if constexpr (C::ES == 2) {
+                        reinterpret_cast<ulonglong2*>(dst)[2 * r] = make_ulonglong2(
+                            get_pair<io_t>(rbc[x][r], 0), get_pair<io_t>(rbc[x][r], 1));
+                        reinterpret_cast<ulonglong2*>(dst)[2 * r + 1] = make_ulonglong2(
+                            get_pair<io_t>(rbc[x][r], 2), get_pair<io_t>(rbc[x][r], 3));
+                    } else {
+                        reinterpret_cast<uint4*>(dst)[r] = rbc[x][r];
+                    }
                 }
             }
         }
@@ -1930,6 +1945,11 @@ cudaError_t dispatch(const ScanArgs& a, cudaStream_t stream, const ScanScratch& 
         if (tile == 6 && N == 16 && !force_reg() && try_ws<io_t, 2, 4, 4, 64, 64, 4>(a, stream, &err))
             return err;
         if (tile == 7 && N == 16 && !force_reg() && try_ws<io_t, 1, 4, 4, 128, 64, 4>(a, stream, &err))
+            return err;
+        if (tile == 8 && N == 16 && !force_reg() && fast &&
+            try_ws<io_t, 1, 8, 2, 32, 32, 8, true>(a, stream, &err))
+            return err;
+        if (tile == 8 && N == 16 && !force_reg() && try_ws<io_t, 1, 8, 2, 32, 32, 8>(a, stream, &err))
             return err;
         // dstate 16 falls back to the 8-state x 2-lane arrangement of the tile
         // above, so that both sum C.h in the same order.
