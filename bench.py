@@ -770,7 +770,9 @@ def bench_decode(args, dcfg, device, peaks) -> dict:
 
     for i in range(max(3, args.warmup)):
         step(i)
-    steps = max(20, min(args.steps, 2000))
+    # a step is ~25 us: time at least 500 of them (12 ms) so that the events'
+    # own resolution and the loop's start-up do not weigh on the average
+    steps = max(500, min(args.steps, 2000))
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)

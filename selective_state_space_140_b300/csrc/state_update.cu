@@ -124,6 +124,17 @@ cudaError_t launch(const StateUpdateArgs& a, cudaStream_t stream) {
 constexpr int kRingTileBytes = 16384;
 
 // Stage layout: state rows | dt | x | z (each a 16-byte multiple).
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their memory operations are visible; allow the grids
+// that depend on this one to be scheduled.  Both are no-ops unless the launch
+// carries the programmatic-serialization attribute.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 template <typename io_t, int G>
 struct RingCfg {
     static constexpr int NPL = 4, N = NPL * G, TC = kRingTileBytes / (N * 4), CPP = 256 / G;
@@ -167,6 +178,16 @@ __global__ void __launch_bounds__(256, 3) state_update_ring_kernel(StateUpdateAr
     if (tid == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);  // (S <= 16 fit in 128 bytes)
         fence_mbar_init();
+    }
+    // Launched as a programmatic dependent of the previous kernel on the
+    // stream (a decode loop's previous step), this CTA may start while that
+    // kernel drains: nothing above reads or writes global memory, and the wait
+    // returns once the previous grid has completed and its writes are
+    // visible.  The next launch may then be scheduled as this grid's CTAs
+    // exit.  Without the launch attribute both are no-ops.
+    grid_dependency_wait();
+    grid_launch_dependents();
+    if (tid == 0) {
         for (int s = 0; s < S && s < njobs; ++s) issue(s, s);
     }
     __syncthreads();
@@ -340,8 +361,20 @@ bool try_ring(const StateUpdateArgs& a, cudaStream_t stream, cudaError_t* err) {
     } else {
         T1 = slots;
     }
-    kern<<<unsigned(T1 * R), 256, C::kSmem, stream>>>(a, int(T1), int(R));
-    *err = cudaGetLastError();
+    // Programmatic dependent launch (MAMBA_DECODE_PDL=0 turns it off): the
+    // CTAs of consecutive decode steps overlap the previous step's tail.
+    const char* pdl = getenv("MAMBA_DECODE_PDL");
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(T1 * R));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = (pdl && pdl[0] == '0') ? 0 : 1;
+    *err = cudaLaunchKernelEx(&cfg, kern, a, int(T1), int(R));
     return true;
 }
 
