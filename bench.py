@@ -98,9 +98,9 @@ def launches_per_step(cfg, sms: int) -> int:
 PROFILED_SOURCES = {
     "scan_fwd": ("scan_fwd.cu", "common.cuh"),
     "scan_bwd": ("scan_bwd.cu", "scan_bwd.cuh", "common.cuh"),
-    "conv1d": ("conv1d.cu", "common.cuh"),
+    "conv1d": ("conv1d.cu", "common.cuh", "launch_dep.cuh"),
     "scan_complex": ("scan_complex.cu", "common.cuh"),
-    "state_update": ("state_update.cu", "common.cuh"),
+    "state_update": ("state_update.cu", "common.cuh", "launch_dep.cuh"),
 }
 
 

@@ -12,6 +12,7 @@
 #include <cstdlib>
 
 #include "common.cuh"
+#include "launch_dep.cuh"
 
 namespace mamba {
 
@@ -124,17 +125,6 @@ cudaError_t launch(const StateUpdateArgs& a, cudaStream_t stream) {
 constexpr int kRingTileBytes = 16384;
 
 // Stage layout: state rows | dt | x | z (each a 16-byte multiple).
-// Programmatic dependent launch: wait until the grids this one depends on
-// have completed and their memory operations are visible; allow the grids
-// that depend on this one to be scheduled.  Both are no-ops unless the launch
-// carries the programmatic-serialization attribute.
-__device__ __forceinline__ void grid_dependency_wait() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void grid_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 template <typename io_t, int G>
 struct RingCfg {
     static constexpr int NPL = 4, N = NPL * G, TC = kRingTileBytes / (N * 4), CPP = 256 / G;
@@ -363,18 +353,8 @@ bool try_ring(const StateUpdateArgs& a, cudaStream_t stream, cudaError_t* err) {
     }
     // Programmatic dependent launch (MAMBA_DECODE_PDL=0 turns it off): the
     // CTAs of consecutive decode steps overlap the previous step's tail.
-    const char* pdl = getenv("MAMBA_DECODE_PDL");
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(T1 * R));
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = C::kSmem;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = (pdl && pdl[0] == '0') ? 0 : 1;
-    *err = cudaLaunchKernelEx(&cfg, kern, a, int(T1), int(R));
+    *err = launch_dependent(kern, dim3(unsigned(T1 * R)), dim3(256), C::kSmem, stream,
+                            "MAMBA_DECODE_PDL", a, int(T1), int(R));
     return true;
 }
 
