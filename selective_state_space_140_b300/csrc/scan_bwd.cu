@@ -152,7 +152,10 @@ __device__ __forceinline__ void fetch(const BwdArgs& a, Raw<io_t, NPL, G>& r, in
 
 // dst[t][n0 .. n0+3] of chunk rows (b, t0 + t) += sum over the CTA's chains of
 // w[t][c] * S[t][c][n0 .. n0+3], for every step and state quad of the chunk
-// (S: the [T][NQ][NTH] float4 tile; w: a [t][chain] field or dt * u).
+// (S: the [T][NQ][NTH] float4 tile; w: a [t][chain] field or dt * u).  At odd
+// steps chain c's column of the tile is that of chain c ^ 1 (tile_col), so
+// the lanes of a quarter-warp -- two steps, the same chains -- read different
+// banks while the chain loop runs in a fixed order with constant offsets.
 template <typename io_t, int NPL, int G, bool DTU>
 __device__ __forceinline__ void chain_product(const float* sm, const float4* S, int wfield,
                                               float* dst, int tlen, int N, bool vec_red, int tid) {
@@ -162,13 +165,18 @@ __device__ __forceinline__ void chain_product(const float* sm, const float4* S, 
         const int t = o / NP4, n0 = (o % NP4) * 4;
         if (t >= tlen || n0 >= N) continue;
         const int g = n0 / NPL, q = (n0 % NPL) / 4;
+        const int sw = (t & 1) * G;
+        // chain c at step t: column (c ^ (t & 1)) * G + g, i.e. c * G + g + sw
+        // for even c and c * G + g - sw for odd c
+        const float4* se = S + (t * C::NQ + q) * C::NTH + g + sw;
+        const float4* so = S + (t * C::NQ + q) * C::NTH + g - sw;
+        const float* w0 = sm + (DTU ? C::oDt : wfield) + t * C::kS;
+        const float* w1 = sm + C::oU + t * C::kS;
         float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-        for (int cc = 0; cc < C::CH; ++cc) {
-            const int c = (cc + t) % C::CH;  // rotate: lanes of other steps read other chains
-            const float w = DTU ? sm[C::oDt + t * C::kS + c] * sm[C::oU + t * C::kS + c]
-                                : sm[wfield + t * C::kS + c];
-            const float4 x = S[(t * C::NQ + q) * C::NTH + c * G + g];
+        for (int c = 0; c < C::CH; ++c) {
+            const float w = DTU ? w0[c] * w1[c] : w0[c];
+            const float4 x = (c & 1) ? so[c * G] : se[c * G];
             sum.x = fmaf(w, x.x, sum.x);
             sum.y = fmaf(w, x.y, sum.y);
             sum.z = fmaf(w, x.z, sum.z);
@@ -211,6 +219,9 @@ __global__ void __launch_bounds__(kBNTH, NPL == 4 ? 8 : 1) scan_bwd_kernel(const
     const int64_t d0 = int64_t(cblk % dblocks) * CH;
     // recurrence role: chain c, states g * NPL ..; element role: chain ce, steps te0 ..
     const int tid = threadIdx.x, c = tid / G, g = tid % G;
+    // this thread's column of the state / adjoint tile at step t: its own at
+    // even steps, chain c ^ 1's at odd steps (see chain_product)
+    auto tile_col = [&](int t) { return (t & 1) ? (tid ^ G) : tid; };
     const int e0 = tid * EPT, ce = e0 / T, te0 = e0 % T;
     const bool e_live = e0 < C::kE && d0 + ce < dim;  // this thread owns real elements
     const int64_t de = e_live ? d0 + ce : 0;
@@ -427,7 +438,7 @@ __global__ void __launch_bounds__(kBNTH, NPL == 4 ? 8 : 1) scan_bwd_kernel(const
                     float h0v, h1v, h2v, h3v;
                     unpack2(hh[2 * v], h0v, h1v);
                     unpack2(hh[2 * v + 1], h2v, h3v);
-                    sH[(t * NQ + v) * NTH + tid] = make_float4(h0v, h1v, h2v, h3v);
+                    sH[(t * NQ + v) * NTH + tile_col(t)] = make_float4(h0v, h1v, h2v, h3v);
                 }
 #pragma unroll
                 for (int off = G / 2; off > 0; off /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -480,7 +491,7 @@ __global__ void __launch_bounds__(kBNTH, NPL == 4 ? 8 : 1) scan_bwd_kernel(const
             f32x2 gu2 = pack2(0.f, 0.f), gd2 = pack2(0.f, 0.f);
 #pragma unroll
             for (int v = 0; v < NQ; ++v) {
-                const float4 hv = t > 0 ? sH[((t - 1) * NQ + v) * NTH + tid]
+                const float4 hv = t > 0 ? sH[((t - 1) * NQ + v) * NTH + tile_col(t - 1)]
                                         : make_float4(hs[4 * v], hs[4 * v + 1], hs[4 * v + 2],
                                                       hs[4 * v + 3]);
                 const float4 bv = Bt[v], cv = Ct[v];
@@ -505,19 +516,24 @@ __global__ void __launch_bounds__(kBNTH, NPL == 4 ? 8 : 1) scan_bwd_kernel(const
                 float g0, g1, g2, g3;
                 unpack2(gq[0], g0, g1);
                 unpack2(gq[1], g2, g3);
-                sH[(t * NQ + v) * NTH + tid] = make_float4(g0, g1, g2, g3);
+                sH[(t * NQ + v) * NTH + tile_col(t)] = make_float4(g0, g1, g2, g3);
             }
             float gu_lo, gu_hi, gd_lo, gd_hi;
             unpack2(gu2, gu_lo, gu_hi);
             unpack2(gd2, gd_lo, gd_hi);
             float gu = gu_lo + gu_hi, gd = gd_lo + gd_hi;
             gd = fmaf(u, gu, gd);  // sum_n g (A Abar h_{t-1} + u B)
+            if constexpr (G >= 2) {
+                // Both sums over the chain's G lanes at once: in the first
+                // round lane g keeps gu (g even) or gd (g odd) and sends the
+                // other to its partner; the remaining rounds reduce the one
+                // kept value, which lane 0 (gu) and lane 1 (gd) then store.
+                const bool odd = g & 1;
+                float v = (odd ? gd : gu) + __shfl_xor_sync(0xffffffffu, odd ? gu : gd, 1);
 #pragma unroll
-            for (int off = G / 2; off > 0; off /= 2) {
-                gu += __shfl_xor_sync(0xffffffffu, gu, off);
-                gd += __shfl_xor_sync(0xffffffffu, gd, off);
-            }
-            if (g == 0) {
+                for (int off = 2; off < G; off *= 2) v += __shfl_xor_sync(0xffffffffu, v, off);
+                if (g < 2) sm[(odd ? C::oGdt : C::oGu) + s] = v;
+            } else {
                 sm[C::oGu + s] = gu;
                 sm[C::oGdt + s] = gd;
             }
