@@ -49,7 +49,8 @@ struct CxCfg {
     static constexpr int kS = ((CH + 2) / 2) % 2 == 1 ? CH + 2 : CH + 4;
     static constexpr int kF = T * kS;
     static constexpr int oDt = 0, oDu = kF, oU = 2 * kF, oYs = 3 * kF;
-    static constexpr int oB = 4 * kF, oC = oB + T * NP * 2;  // [T][NP][re, im]
+    // B and C as planes: [T][re | im][NP], C's imaginary plane negated
+    static constexpr int oB = 4 * kF, oC = oB + T * NP * 2;
     static constexpr int kFloats = oC + T * NP * 2;
     // fp32 io only: the step dt in fp64, [t][chain] like oDt, after the floats
     static constexpr bool kDt64 = sizeof(io_t) == 4;
@@ -197,6 +198,7 @@ __global__ void __launch_bounds__(kCNTH) scan_complex_kernel(const CxArgs p, con
     const bool chain_ok = d < dim;
 
     float A2[NPL], Aim[NPL], hr[NPL], hi[NPL];
+    static_assert(C::kDt64 || NPL % 4 == 0, "the packed path reads B and C as float4");
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
         const int n = g * NPL + i;
@@ -204,6 +206,15 @@ __global__ void __launch_bounds__(kCNTH) scan_complex_kernel(const CxArgs p, con
         A2[i] = ok ? -expf(__ldg(p.A_log_re + d * N + n)) * kLog2e : 0.f;
         Aim[i] = ok ? __ldg(p.A_im + d * N + n) : 0.f;
         hr[i] = hi[i] = 0.f;
+    }
+
+    // the same as pairs of states for the packed arithmetic of bf16 io
+    f32x2 A2p[NPL / 2], Aim2[NPL / 2], hr2[NPL / 2], hi2[NPL / 2];
+#pragma unroll
+    for (int q = 0; q < NPL / 2; ++q) {
+        A2p[q] = pack2(A2[2 * q], A2[2 * q + 1]);
+        Aim2[q] = pack2(Aim[2 * q], Aim[2 * q + 1]);
+        hr2[q] = hi2[q] = pack2(0.f, 0.f);
     }
 
     const int64_t nchunks = (L + T - 1) / T;
@@ -241,11 +252,15 @@ __global__ void __launch_bounds__(kCNTH) scan_complex_kernel(const CxArgs p, con
         }
         if constexpr (C::PREB) {
 #pragma unroll
-            for (int j = 0; j < C::BPT; ++j)
-                if (tid + j * NTH < T * NP * 2) {
-                    sm[C::oB + tid + j * NTH] = cx_f(r.B[j]);
-                    sm[C::oC + tid + j * NTH] = cx_f(r.Cc[j]);
+            for (int j = 0; j < C::BPT; ++j) {
+                const int e = tid + j * NTH;  // [t][n][re, im] of the chunk
+                if (e < T * NP * 2) {
+                    const int t = e / (NP * 2), n = (e / 2) % NP, ri = e % 2;
+                    const int o = t * NP * 2 + ri * NP + n;
+                    sm[C::oB + o] = cx_f(r.B[j]);
+                    sm[C::oC + o] = ri ? -cx_f(r.Cc[j]) : cx_f(r.Cc[j]);
                 }
+            }
         } else {
             const io_t* Bg = static_cast<const io_t*>(p.B) + int64_t(b) * L * N * 2;
             const io_t* Cg = static_cast<const io_t*>(p.C) + int64_t(b) * L * N * 2;
@@ -253,8 +268,10 @@ __global__ void __launch_bounds__(kCNTH) scan_complex_kernel(const CxArgs p, con
                 const int t = e / (NP * 2), n = (e / 2) % NP, ri = e % 2;
                 const bool ok = n < N && t0 + t < L;
                 const int64_t off = ok ? ((t0 + t) * N + n) * 2 + ri : 0;
-                sm[C::oB + e] = ok ? Io<io_t>::load(Bg + off) : 0.f;
-                sm[C::oC + e] = ok ? Io<io_t>::load(Cg + off) : 0.f;
+                const int o = t * NP * 2 + ri * NP + n;
+                const float cv = ok ? Io<io_t>::load(Cg + off) : 0.f;
+                sm[C::oB + o] = ok ? Io<io_t>::load(Bg + off) : 0.f;
+                sm[C::oC + o] = ri ? -cv : cv;
             }
         }
         __syncthreads();
@@ -263,20 +280,67 @@ __global__ void __launch_bounds__(kCNTH) scan_complex_kernel(const CxArgs p, con
 #pragma unroll
         for (int t = 0; t < T; ++t) {
             const float dt = sm[C::oDt + t * S + c], du = sm[C::oDu + t * S + c];
-            const double dt64 = C::kDt64 ? smd[C::oDt64 + t * S + c] : 0.0;
+            const float* Bt = sm + C::oB + t * NP * 2 + g * NPL;  // re plane; im at + NP
+            const float* Ct = sm + C::oC + t * NP * 2 + g * NPL;
             float acc = 0.f;
+            if constexpr (C::kDt64) {
+                const double dt64 = smd[C::oDt64 + t * S + c];
 #pragma unroll
-            for (int i = 0; i < NPL; ++i) {
-                const int n = g * NPL + i;
-                float ar, ai;
-                cx_decay<sizeof(io_t) == 4>(dt, dt64, A2[i], Aim[i], ar, ai);
-                const float2 Bn = *reinterpret_cast<const float2*>(sm + C::oB + (t * NP + n) * 2);
-                const float2 Cn = *reinterpret_cast<const float2*>(sm + C::oC + (t * NP + n) * 2);
-                const float nr = fmaf(ar, hr[i], fmaf(-ai, hi[i], Bn.x * du));
-                const float ni = fmaf(ar, hi[i], fmaf(ai, hr[i], Bn.y * du));
-                hr[i] = nr;
-                hi[i] = ni;
-                acc = fmaf(Cn.x, nr, fmaf(-Cn.y, ni, acc));
+                for (int i = 0; i < NPL; ++i) {
+                    float ar, ai;
+                    cx_decay<true>(dt, dt64, A2[i], Aim[i], ar, ai);
+                    const float nr = fmaf(ar, hr[i], fmaf(-ai, hi[i], Bt[i] * du));
+                    const float ni = fmaf(ar, hi[i], fmaf(ai, hr[i], Bt[NP + i] * du));
+                    hr[i] = nr;
+                    hi[i] = ni;
+                    acc = fmaf(Ct[i], nr, fmaf(Ct[NP + i], ni, acc));  // Ct[NP + i] = -Im C
+                }
+            } else {
+                // pairs of states in packed f32x2 arithmetic; each state's decay
+                // and update round exactly as the scalar form, and C.h sums the
+                // even and the odd states separately
+                const f32x2 dts = pack2(dt, dt), dus = pack2(du, du);
+                f32x2 acc2 = pack2(0.f, 0.f);
+#pragma unroll
+                for (int v = 0; v < NPL / 4; ++v) {
+                    const float4 brv = reinterpret_cast<const float4*>(Bt)[v];
+                    const float4 biv = reinterpret_cast<const float4*>(Bt + NP)[v];
+                    const float4 crv = reinterpret_cast<const float4*>(Ct)[v];
+                    const float4 civ = reinterpret_cast<const float4*>(Ct + NP)[v];
+                    const f32x2 br[2] = {pack2(brv.x, brv.y), pack2(brv.z, brv.w)};
+                    const f32x2 bi[2] = {pack2(biv.x, biv.y), pack2(biv.z, biv.w)};
+                    const f32x2 cr[2] = {pack2(crv.x, crv.y), pack2(crv.z, crv.w)};
+                    const f32x2 ci[2] = {pack2(civ.x, civ.y), pack2(civ.z, civ.w)};
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int q = 2 * v + e;
+                        // angle reduced to [-pi, pi]: ang - q 2pi with q = rint(ang / 2pi)
+                        const f32x2 ang = mul2(dts, Aim2[q]);
+                        float w0, w1;
+                        unpack2(mul2(ang, pack2(kInvTwoPi, kInvTwoPi)), w0, w1);
+                        const f32x2 qq = pack2(rintf(w0), rintf(w1));
+                        float r0, r1;
+                        unpack2(fma2(qq, pack2(-kTwoPiLo, -kTwoPiLo),
+                                     fma2(qq, pack2(-kTwoPiHi, -kTwoPiHi), ang)),
+                                r0, r1);
+                        float s0, c0, s1, c1;
+                        __sincosf(r0, &s0, &c0);
+                        __sincosf(r1, &s1, &c1);
+                        float x0, x1;
+                        unpack2(mul2(dts, A2p[q]), x0, x1);
+                        const f32x2 mag = pack2(ex2_approx(x0), ex2_approx(x1));
+                        const f32x2 ar = mul2(mag, pack2(c0, c1)), ai = mul2(mag, pack2(s0, s1));
+                        const f32x2 nai = mul2(ai, pack2(-1.f, -1.f));  // -ai, exactly
+                        const f32x2 nr = fma2(ar, hr2[q], fma2(nai, hi2[q], mul2(br[e], dus)));
+                        const f32x2 ni = fma2(ar, hi2[q], fma2(ai, hr2[q], mul2(bi[e], dus)));
+                        hr2[q] = nr;
+                        hi2[q] = ni;
+                        acc2 = fma2(cr[e], nr, fma2(ci[e], ni, acc2));
+                    }
+                }
+                float lo, hi_;
+                unpack2(acc2, lo, hi_);
+                acc = lo + hi_;
             }
 #pragma unroll
             for (int off = G / 2; off > 0; off /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -293,6 +357,13 @@ __global__ void __launch_bounds__(kCNTH) scan_complex_kernel(const CxArgs p, con
             float y = fmaf(e_D, sm[C::oU + s], sm[C::oYs + s]);
             if (p.z) y = gate_silu(y, e_z[j]);
             Io<io_t>::store(static_cast<io_t*>(p.y) + (int64_t(b) * dim + de) * L + t0 + t, y);
+        }
+    }
+    if constexpr (!C::kDt64) {
+#pragma unroll
+        for (int q = 0; q < NPL / 2; ++q) {
+            unpack2(hr2[q], hr[2 * q], hr[2 * q + 1]);
+            unpack2(hi2[q], hi[2 * q], hi[2 * q + 1]);
         }
     }
     if (chain_ok && p.last_state) {
