@@ -273,6 +273,14 @@ int mamba_selective_scan_bwd_ex(const void *u, const void *delta, const float *A
  *   out         : [batch, dim] io_dtype, written
  *
  * Same as one step of mamba_selective_scan_fwd started from `state`.
+ *
+ * Launch: the fast path (dstate a power of two 4..128, dim a multiple of the
+ * kernel's tile, 16-byte aligned rows) is launched as a programmatic
+ * dependent of the work before it on `stream`: its blocks may become resident
+ * while that work drains, and they wait for it to complete, with its memory
+ * writes visible, before any access to global memory -- stream order holds
+ * for every argument (a decode loop's state is read after the previous step
+ * wrote it).  The environment variable MAMBA_DECODE_PDL=0 launches it plainly.
  */
 int mamba_selective_state_update(float *state, const void *x, const void *dt,
                                  const float *A_log, const void *B, const void *C,
@@ -337,6 +345,9 @@ int mamba_selective_scan_complex_fwd(const void *u, const void *delta, const flo
  * Fast path: seqlen a multiple of 8 (bf16) or 4 (fp32), x and out 16-byte
  * aligned and width-1 at most that vector length; other inputs take a scalar
  * path with the same arithmetic.  Errors as for mamba_selective_scan_fwd.
+ * The fast path is launched as a programmatic dependent of the work before it
+ * on `stream`, with the same ordering guarantee as the decode step
+ * (MAMBA_CONV_PDL=0 launches it plainly).
  */
 int mamba_causal_conv1d_fwd(const void *x, const float *weight, const float *bias,
                             const void *initial_state, int silu_flag, void *out,
