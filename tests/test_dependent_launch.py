@@ -80,3 +80,55 @@ def test_conv_chain_with_and_without_dependent_launch(cuda, io, monkeypatch):
     f = workloads.to_f64
     ref, _ = oracle.causal_conv1d(f(x["x"]), f(x["weight"]), bias=f(x["bias"]), silu=True)
     assert rel_err(one, ref) <= (1e-5 if io == "f32" else 1e-2)
+
+
+def test_decode_and_conv_captured_in_a_cuda_graph(cuda):
+    """A decode loop captured into a CUDA graph (as a serving loop runs it) with
+    the dependent launches inside: replaying the graph equals running the same
+    calls eagerly, bit for bit."""
+    batch, dim, N, io = 4, 1024, 16, "bf16"
+    xs = [to_device(workloads.make_decode_inputs(batch, dim, N, io, seed=400 + i), cuda)
+          for i in range(6)]
+    cx = to_device(workloads.make_conv_inputs(batch, dim, 64, 4, io, seed=33), cuda)
+    state0 = xs[0]["state"].clone()
+
+    def run(st, outs, conv_out):
+        for i, xd in enumerate(xs):
+            abi.mamba_selective_state_update(
+                st, xd["x"], xd["dt"], xd["A_log"], xd["B"], xd["C"], D=xd["D"], z=xd["z"],
+                dt_bias=xd["dt_bias"], softplus=xd["softplus"], out=outs[i],
+                stream=torch.cuda.current_stream())
+        abi.mamba_causal_conv1d_fwd(cx["x"], cx["weight"], bias=cx["bias"], silu=True,
+                                    out=conv_out, want_final_state=False,
+                                    stream=torch.cuda.current_stream())
+
+    st_e = state0.clone()
+    outs_e = [torch.empty_like(xs[0]["x"]) for _ in xs]
+    conv_e = torch.empty_like(cx["x"])
+    run(st_e, outs_e, conv_e)
+    torch.cuda.synchronize()
+
+    st_g = state0.clone()
+    outs_g = [torch.empty_like(xs[0]["x"]) for _ in xs]
+    conv_g = torch.empty_like(cx["x"])
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        st_g.copy_(state0)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=side):
+            run(st_g, outs_g, conv_g)
+    st_g.copy_(state0)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(st_g, st_e)
+    for a, b in zip(outs_g, outs_e):
+        assert torch.equal(a, b)
+    assert torch.equal(conv_g, conv_e)
+    # a second replay continues from the state the first one left
+    graph.replay()
+    run(st_e, outs_e, conv_e)
+    torch.cuda.synchronize()
+    assert torch.equal(st_g, st_e)
+    assert abi.mamba_device_status() == 0
