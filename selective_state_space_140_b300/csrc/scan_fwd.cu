@@ -756,8 +756,10 @@ constexpr int kBarDone = 3;   // + (chunk & 1): recurrence of the chunk done
 //   state, writing only the state at its end and the sum of its dt (no y).
 constexpr int kScanFull = 0, kScanSummary = 1;
 
-// FAST: the gate z is given, softplus is on, and there is no h0 and no reset
-// mask (the common case, compiled without their run-time tests).
+// FAST: the gate z is given, softplus is on and there is no reset mask (the
+// common case, compiled without those run-time tests and without the
+// per-element reset decoding; h0 and a split's carried state are read once
+// per CTA either way).
 template <typename io_t, int P, int NPL, int G, int NR, int NE, int MINB, int MODE,
           bool FAST = false>
 __global__ void __launch_bounds__(NR + NE, MINB)
@@ -792,7 +794,7 @@ __global__ void __launch_bounds__(NR + NE, MINB)
     const int tid = threadIdx.x;
     const int nchunks = (Ls + T - 1) / T;
     const int row0 = int(int64_t(b) * dim + d0);
-    const bool has_z = FAST || (MODE == kScanFull && p.z != nullptr);
+    const bool has_z = MODE == kScanFull && (FAST || p.z != nullptr);
     const io_t* Bg = static_cast<const io_t*>(p.B) + (int64_t(b) * L + t0) * N;
     const io_t* Cg = static_cast<const io_t*>(p.C) + (int64_t(b) * L + t0) * N;
     auto chunk_len = [&](int k) { return Ls - k * T < T ? Ls - k * T : T; };
@@ -840,7 +842,7 @@ __global__ void __launch_bounds__(NR + NE, MINB)
                 const int64_t chain = int64_t(b) * dim + d0 + cc[q];
                 if (sg.hcarry)  // split: the carry pass left the entering state in slot tseg
                     load_state<NPL, G>(sg.hcarry + (chain * sg.nseg + tseg) * N, N, g, h[q]);
-                else if (!FAST && p.h0)
+                else if (p.h0)
                     load_state<NPL, G>(p.h0 + chain * N, N, g, h[q]);
             }
         }
@@ -1870,7 +1872,9 @@ bool try_ws_split(const ScanArgs& a, cudaStream_t stream, const ScanScratch& sc,
     const size_t hbytes = rnd(size_t(chains) * nseg * a.dstate * sizeof(float));
     SegArgs sg{seg_len, nseg, nseg - 1, static_cast<float*>(buf),
                reinterpret_cast<float*>(static_cast<char*>(buf) + hbytes)};
-    *err = launch_ws<io_t, 1, 8, 2, 64, 64, 4, kScanSummary>(a, sg, stream);
+    const bool fast = a.z && a.softplus && !a.reset;
+    *err = fast ? launch_ws<io_t, 1, 8, 2, 64, 64, 4, kScanSummary, true>(a, sg, stream)
+                : launch_ws<io_t, 1, 8, 2, 64, 64, 4, kScanSummary>(a, sg, stream);
     if (*err == cudaSuccess) {
         const int64_t threads = chains * a.dstate;
         scan_carry_kernel<<<unsigned((threads + 255) / 256), 256, 0, stream>>>(
@@ -1879,7 +1883,8 @@ bool try_ws_split(const ScanArgs& a, cudaStream_t stream, const ScanScratch& sc,
     }
     if (*err == cudaSuccess) {
         sg.grid_nseg = nseg;
-        *err = launch_ws<io_t, 1, 8, 2, 64, 64, 4, kScanFull>(a, sg, stream);
+        *err = fast ? launch_ws<io_t, 1, 8, 2, 64, 64, 4, kScanFull, true>(a, sg, stream)
+                    : launch_ws<io_t, 1, 8, 2, 64, 64, 4, kScanFull>(a, sg, stream);
     }
     if (owned) {
         const cudaError_t ferr = cudaFreeAsync(buf, stream);
@@ -1933,7 +1938,7 @@ cudaError_t dispatch(const ScanArgs& a, cudaStream_t stream, const ScanScratch& 
         if ((tile == 0 || tile == 4) && N == 16 && !force_reg() &&
             try_ws_split<io_t>(a, stream, sc, &err))
             return err;
-        const bool fast = a.z && a.softplus && !a.h0 && !a.reset;
+        const bool fast = a.z && a.softplus && !a.reset;
         if ((tile == 4 || tile == 0) && N == 16 && !force_reg() && fast &&
             try_ws<io_t, 1, 8, 2, 64, 64, 4, true>(a, stream, &err))
             return err;
