@@ -330,17 +330,23 @@ bool try_ring(const StateUpdateArgs& a, cudaStream_t stream, cudaError_t* err) {
         !al(a.dt, 16) || !al(a.x, 16) || !al(a.z, 16) || !al(a.B, 4 * C::ES) ||
         !al(a.C, 4 * C::ES) || a.batch > 0x7fffffff)
         return false;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return false;
     auto kern = state_update_ring_kernel<io_t, G>;
-    int per_sm = 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
-            cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, C::kSmem) !=
-            cudaSuccess ||
-        per_sm < 1)
+    // SM count, shared-memory attribute and resident CTAs: once per device
+    static LaunchShapeCache shape;
+    int sms = 0, per_sm = 0;
+    if (!cached_launch_shape(
+            shape,
+            [&](int* s, int* r) {
+                int dev = 0;
+                return cudaGetDevice(&dev) == cudaSuccess &&
+                       cudaDeviceGetAttribute(s, cudaDevAttrMultiProcessorCount, dev) ==
+                           cudaSuccess &&
+                       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            C::kSmem) == cudaSuccess &&
+                       cudaOccupancyMaxActiveBlocksPerMultiprocessor(r, kern, 256, C::kSmem) ==
+                           cudaSuccess;
+            },
+            &sms, &per_sm))
         return false;
     // One persistent CTA per slot: T1 channel-block columns x R batch strides.
     const int64_t slots = int64_t(sms) * per_sm, tpr = a.dim / C::TC;
