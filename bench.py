@@ -96,8 +96,8 @@ def launches_per_step(cfg, sms: int) -> int:
 
 # kernel sources behind each stored ncu summary (profiles/<prefix>_<workload>.md)
 PROFILED_SOURCES = {
-    "scan_fwd": ("scan_fwd.cu", "common.cuh"),
-    "scan_bwd": ("scan_bwd.cu", "scan_bwd.cuh", "common.cuh"),
+    "scan_fwd": ("scan_fwd.cu", "common.cuh", "scratch_pool.cu"),
+    "scan_bwd": ("scan_bwd.cu", "scan_bwd.cuh", "common.cuh", "scratch_pool.cu"),
     "conv1d": ("conv1d.cu", "common.cuh", "launch_dep.cuh"),
     "scan_complex": ("scan_complex.cu", "common.cuh"),
     "state_update": ("state_update.cu", "common.cuh", "launch_dep.cuh"),

@@ -105,9 +105,14 @@ typedef enum {
  * and the full pass, the three launched on `stream`.  The carried states
  * (batch * dim * segments * (dstate + 1) fp32 values, at most about
  * 256 * SMs * (dstate + 1) * 4 bytes) live in stream-ordered scratch taken
- * with cudaMallocAsync and returned with cudaFreeAsync on `stream`, so calls
- * on different streams never share it.  If that allocation fails the scan
- * runs unsplit.  Results of a split and an unsplit scan agree to rounding.
+ * on `stream` and returned on `stream` (cudaMallocFromPoolAsync /
+ * cudaFreeAsync), so calls on different streams never share it.  The scratch
+ * comes from a memory pool the library creates on each device, which keeps
+ * freed memory mapped across synchronisation points (up to
+ * MAMBA_SCRATCH_RETAIN_MB megabytes; all of it when unset) instead of
+ * returning it to the driver as the device's default pool does.  If that
+ * allocation fails the scan runs unsplit.  Results of a split and an unsplit
+ * scan agree to rounding.
  */
 int mamba_selective_scan_fwd(const void *u, const void *delta, const float *A_log,
                              const void *B, const void *C, const float *D, const void *z,
@@ -212,7 +217,8 @@ int mamba_selective_scan_fwd_ex(const void *u, const void *delta, const float *A
  *
  * Scratch: per chain one fp32 state every 16 steps (batch * dim *
  * ceil(seqlen/16) * dstate * 4 bytes), allocated and freed on `stream` in
- * the call (stream-ordered), where the page's recomputation keeps O(1).
+ * the call (stream-ordered, from the library's pool described at
+ * mamba_selective_scan_fwd), where the page's recomputation keeps O(1).
  * Errors as for mamba_selective_scan_fwd.
  */
 int mamba_selective_scan_bwd(const void *u, const void *delta, const float *A_log,

@@ -39,6 +39,7 @@
 #include <cstdlib>
 
 #include "scan_bwd.cuh"
+#include "scratch_pool.cuh"
 
 namespace mamba {
 namespace {
@@ -668,7 +669,7 @@ cudaError_t launch_bwd_impl(const BwdArgs& a0, bool vec_red, cudaStream_t stream
     if (nseg > 1) {
         const int64_t chains = a.f.batch * a.f.dim;
         const size_t nst = size_t(chains) * nseg * a.f.dstate;
-        if ((err = cudaMallocAsync(&seg_mem, (2 * nst + size_t(chains) * nseg) * sizeof(float),
+        if ((err = scratch_alloc(&seg_mem, (2 * nst + size_t(chains) * nseg) * sizeof(float),
                                    stream)) != cudaSuccess)
             return err;
         a.hseg = static_cast<float*>(seg_mem);
@@ -698,7 +699,7 @@ cudaError_t launch_bwd_impl(const BwdArgs& a0, bool vec_red, cudaStream_t stream
         err = cudaGetLastError();
     }
     if (seg_mem) {
-        const cudaError_t ferr = cudaFreeAsync(seg_mem, stream);
+        const cudaError_t ferr = scratch_free(seg_mem, stream);
         if (err == cudaSuccess) err = ferr;
     }
     return err;
@@ -770,7 +771,7 @@ cudaError_t launch_scan_bwd_ex(const ScanBwdArgs& s, float* dh0, bool bf16, cuda
     // checkpoints: the state at the start of every chunk, stream-ordered scratch
     void* ck = nullptr;
     const size_t ckb = size_t(chains) * nchunks * s.f.dstate * sizeof(float);
-    if ((err = cudaMallocAsync(&ck, ckb, stream)) != cudaSuccess) return err;
+    if ((err = scratch_alloc(&ck, ckb, stream)) != cudaSuccess) return err;
     BwdArgs a;
     static_cast<ScanBwdArgs&>(a) = s;
     a.ckpt = static_cast<float*>(ck);
@@ -780,7 +781,7 @@ cudaError_t launch_scan_bwd_ex(const ScanBwdArgs& s, float* dh0, bool bf16, cuda
                          (reinterpret_cast<uintptr_t>(s.dC) & 15) == 0;
     err = bf16 ? dispatch_bwd<__nv_bfloat16>(a, vec_red, stream)
                : dispatch_bwd<float>(a, vec_red, stream);
-    const cudaError_t ferr = cudaFreeAsync(ck, stream);
+    const cudaError_t ferr = scratch_free(ck, stream);
     return err != cudaSuccess ? err : ferr;
 }
 

@@ -48,6 +48,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "scratch_pool.cuh"
 
 namespace mamba {
 
@@ -1863,7 +1864,7 @@ bool try_ws_split(const ScanArgs& a, cudaStream_t stream, const ScanScratch& sc,
         // set, but only when no error was pending before it.
         const bool pending = cudaPeekAtLastError() != cudaSuccess;
         if (!sc.may_alloc) return false;
-        if (cudaMallocAsync(&buf, bytes_for(nseg), stream) != cudaSuccess) {
+        if (scratch_alloc(&buf, bytes_for(nseg), stream) != cudaSuccess) {
             if (!pending) cudaGetLastError();
             return false;
         }
@@ -1887,7 +1888,7 @@ bool try_ws_split(const ScanArgs& a, cudaStream_t stream, const ScanScratch& sc,
                     : launch_ws<io_t, 1, 8, 2, 64, 64, 4, kScanFull>(a, sg, stream);
     }
     if (owned) {
-        const cudaError_t ferr = cudaFreeAsync(buf, stream);
+        const cudaError_t ferr = scratch_free(buf, stream);
         if (*err == cudaSuccess) *err = ferr;
     }
     return true;
