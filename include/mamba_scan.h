@@ -27,10 +27,14 @@
  *
  * Conventions shared by every entry point
  *   - All pointers are DEVICE pointers owned by the caller.  Arrays are dense
- *     row-major with the shapes given below.  The library keeps no state
+ *     row-major with the shapes given below.  The library keeps no data
  *     between calls.  Only mamba_selective_scan_fwd (see there and
  *     mamba_selective_scan_fwd_noalloc) and mamba_selective_scan_bwd take
  *     scratch memory, stream-ordered on the call's stream.
+ *   - Per device the library caches what it looks up once: the scratch
+ *     memory pool, the decode kernel's launch shape (with the shared-memory
+ *     attribute it sets) and the no-alloc buffer's address.  A cudaDeviceReset
+ *     invalidates them; call the library again only from a fresh process.
  *   - io_dtype (MAMBA_F32 or MAMBA_BF16) is the element type of every
  *     "io" array (u, delta, z, B, C, y; x, dt, z, B, C, out for decode; dout,
  *     du, ddelta, dz for the backward; x, out and the conv state for conv1d).
