@@ -61,6 +61,9 @@ SHAPES = [
     (1, 5, 70, 17, "f32"), (1, 6, 50, 32, "bf16"), (1, 6, 50, 64, "f32"), (1, 4, 40, 100, "f32"),
     (1, 3, 30, 256, "f32"), (1, 130, 40, 8, "bf16"), (2, 70, 1000, 16, "f32"),
     (2, 70, 1000, 16, "bf16"), (1, 16, 2049, 16, "f32"),
+    # bf16 (packed pairs of states) at every tile width, with padded lanes
+    (1, 9, 63, 3, "bf16"), (1, 5, 70, 17, "bf16"), (1, 6, 50, 64, "bf16"),
+    (1, 4, 40, 100, "bf16"), (1, 3, 30, 256, "bf16"),
 ]
 
 
