@@ -137,7 +137,7 @@ struct RingCfg {
 };
 
 template <typename io_t, int G>
-__global__ void __launch_bounds__(256, 3) state_update_ring_kernel(StateUpdateArgs p, int T1,
+__global__ void __launch_bounds__(256, 4) state_update_ring_kernel(StateUpdateArgs p, int T1,
                                                                    int R) {
     using C = RingCfg<io_t, G>;
     constexpr int N = C::N, TC = C::TC, CPP = C::CPP, PASSES = C::PASSES, S = C::S;
